@@ -1,0 +1,113 @@
+"""FP64 CPU oracle of the hyper-connection read (test infrastructure only).
+
+Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's CPU
+baseline / reference arm may import this package.  The CUDA library never
+uses it.  ``hc_oracle.cpp`` holds the arithmetic; this module compiles it with
+plain ``g++`` and wraps it with ctypes.
+
+The compile flags keep the arithmetic as written: ``-O2`` without fast-math,
+and ``-ffp-contract=off`` so that no multiply-add is fused (GCC fuses by
+default on aarch64).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(HERE, "hc_oracle.cpp")
+LIB = os.path.join(HERE, "libhcoracle.so")
+
+CXXFLAGS = ["-O2", "-std=c++17", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math"]
+
+
+def compile_cmd(src: str = SRC, out: str = LIB) -> list[str]:
+    return ["g++", *CXXFLAGS, "-o", out, src]
+
+
+def build(src: str = SRC, out: str = LIB) -> str:
+    """Compile the oracle into a shared library and return its path."""
+    subprocess.run(compile_cmd(src, out), check=True)
+    return out
+
+
+_f32p = np.ctypeslib.ndpointer(dtype=np.float32, flags="C_CONTIGUOUS")
+_f64p = np.ctypeslib.ndpointer(dtype=np.float64, flags="C_CONTIGUOUS")
+_u16p = np.ctypeslib.ndpointer(dtype=np.uint16, flags="C_CONTIGUOUS")
+
+
+@dataclass
+class OracleResult:
+    r_out: np.ndarray  # [T][N] float32, R' = fl32(R + P)
+    ss: np.ndarray     # [T][n] float64
+    rs: np.ndarray     # [T][n] float64
+    lo: np.ndarray     # [T][K] float64
+    u: np.ndarray      # [T][N] float64
+    out: np.ndarray    # [T][N] float64
+    mean: np.ndarray   # [T][d] float64
+
+
+class Oracle:
+    """ctypes handle on a compiled oracle library."""
+
+    def __init__(self, path: str = LIB):
+        if not os.path.exists(path):
+            raise FileNotFoundError(f"oracle library not built: {path} (call oracle.build())")
+        self.path = path
+        lib = ctypes.CDLL(path)
+        lib.hc_oracle_read.restype = ctypes.c_int
+        lib.hc_oracle_read.argtypes = [
+            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+            _f32p, ctypes.c_void_p, _f32p, _u16p, _u16p, _f32p,
+            _f32p, _f64p, _f64p, _f64p, _f64p, _f64p, _f64p,
+        ]
+        self._lib = lib
+
+    def read(self, n: int, d: int, K: int, R, w_norm, W_down, W_up, gate,
+             P=None, eps: float = 1e-6) -> OracleResult:
+        """Run the whole read on host arrays.
+
+        R, P: [T][n*d] float32; w_norm, gate: [n*d] float32;
+        W_down: [K][n*d] uint16 (BF16 bits); W_up: [n*d][K] uint16.
+        """
+        N = n * d
+        R = np.ascontiguousarray(R, dtype=np.float32).reshape(-1, N)
+        T = R.shape[0]
+        w_norm = np.ascontiguousarray(w_norm, dtype=np.float32).reshape(N)
+        gate = np.ascontiguousarray(gate, dtype=np.float32).reshape(N)
+        W_down = np.ascontiguousarray(W_down, dtype=np.uint16).reshape(K, N)
+        W_up = np.ascontiguousarray(W_up, dtype=np.uint16).reshape(N, K)
+        if P is not None:
+            P = np.ascontiguousarray(P, dtype=np.float32).reshape(T, N)
+            p_ptr = P.ctypes.data_as(ctypes.c_void_p)
+        else:
+            p_ptr = None
+        res = OracleResult(
+            r_out=np.empty((T, N), np.float32), ss=np.empty((T, n)), rs=np.empty((T, n)),
+            lo=np.empty((T, K)), u=np.empty((T, N)), out=np.empty((T, N)),
+            mean=np.empty((T, d)),
+        )
+        rc = self._lib.hc_oracle_read(
+            n, d, K, T, float(eps), R, p_ptr, w_norm, W_down, W_up, gate,
+            res.r_out, res.ss, res.rs, res.lo, res.u, res.out, res.mean)
+        if rc != 0:
+            raise ValueError(f"hc_oracle_read rejected its arguments (rc={rc})")
+        return res
+
+
+_default: Oracle | None = None
+
+
+def default() -> Oracle:
+    """The oracle built from this directory's source (built on first use)."""
+    global _default
+    if _default is None:
+        if not os.path.exists(LIB) or os.path.getmtime(LIB) < os.path.getmtime(SRC):
+            build()
+        _default = Oracle(LIB)
+    return _default

@@ -1,0 +1,149 @@
+"""Seeded synthetic inputs shared by the CUDA path's tests/benchmark and the oracle.
+
+This package draws random numbers only (see ``hc_synth.c``); it holds none of
+the read's arithmetic and imports neither the CUDA binding nor the oracle.
+
+Input recipe (one read at geometry (n, d, K), T tokens):
+
+===========  ==========================  =====================  ===========
+tensor       shape                       distribution           tensor id
+===========  ==========================  =====================  ===========
+R            [T][n*d] float32            N(0, 1)                0
+P (pending)  [T][n*d] float32            N(0, 0.1)              1
+w_norm       [n*d] float32               1 + N(0, 0.05)         2
+gate g       [n*d] float32               N(0, 1)                3
+W_down       [K][n*d] BF16 (uint16)      N(0, w_std)            4
+W_up         [n*d][K] BF16 (uint16)      N(0, w_std)            5
+===========  ==========================  =====================  ===========
+
+Activations (R, P) use seed ``s0``; weight set ``j`` (W_down, W_up, w_norm,
+gate) uses seed ``s0 + 1 + j``.  ``w_std`` is 0.02 at d=2560, K=320 and 0.015
+at d=4096, K=512.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(HERE, "hc_synth.c")
+LIB = os.path.join(HERE, "libhcsynth.so")
+CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math", "-pthread"]
+
+TID_R, TID_P, TID_WNORM, TID_GATE, TID_WDOWN, TID_WUP = range(6)
+
+
+def compile_cmd(out: str = LIB) -> list[str]:
+    return ["gcc", *CFLAGS, "-o", out, SRC, "-lm"]
+
+
+def build(out: str = LIB) -> str:
+    subprocess.run(compile_cmd(out), check=True)
+    return out
+
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB) or os.path.getmtime(LIB) < os.path.getmtime(SRC):
+            build()
+        lib = ctypes.CDLL(LIB)
+        for name, ptr in (("hc_synth_normal_f32", ctypes.c_void_p),
+                          ("hc_synth_normal_bf16", ctypes.c_void_p)):
+            f = getattr(lib, name)
+            f.restype = None
+            f.argtypes = [ctypes.c_uint64, ctypes.c_uint32, ctypes.c_double, ctypes.c_double,
+                          ptr, ctypes.c_size_t, ctypes.c_int]
+        lib.hc_synth_raw.restype = ctypes.c_uint64
+        lib.hc_synth_raw.argtypes = [ctypes.c_uint64, ctypes.c_uint64]
+        lib.hc_synth_mix64.restype = ctypes.c_uint64
+        lib.hc_synth_mix64.argtypes = [ctypes.c_uint64]
+        _lib = lib
+    return _lib
+
+
+def _threads() -> int:
+    return max(1, min(32, os.cpu_count() or 1))
+
+
+def normal_f32(seed: int, tensor_id: int, mean: float, std: float, shape, out=None) -> np.ndarray:
+    """float32 array of N(mean, std) draws (optionally written into ``out``)."""
+    a = np.empty(shape, np.float32) if out is None else out
+    assert a.dtype == np.float32 and a.flags.c_contiguous
+    _load().hc_synth_normal_f32(seed, tensor_id, mean, std, a.ctypes.data, a.size, _threads())
+    return a
+
+
+def normal_bf16(seed: int, tensor_id: int, mean: float, std: float, shape, out=None) -> np.ndarray:
+    """uint16 array holding BF16 bits of N(mean, std) draws, rounded to nearest even."""
+    a = np.empty(shape, np.uint16) if out is None else out
+    assert a.dtype == np.uint16 and a.flags.c_contiguous
+    _load().hc_synth_normal_bf16(seed, tensor_id, mean, std, a.ctypes.data, a.size, _threads())
+    return a
+
+
+def raw(key: int, j: int) -> int:
+    return int(_load().hc_synth_raw(key, j))
+
+
+def mix64(z: int) -> int:
+    return int(_load().hc_synth_mix64(z))
+
+
+def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Widen BF16 bit patterns to float32 (exact)."""
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+@dataclass(frozen=True)
+class Geometry:
+    n: int
+    d: int
+    K: int
+    w_std: float
+
+    @property
+    def N(self) -> int:
+        return self.n * self.d
+
+
+G1 = Geometry(n=4, d=2560, K=320, w_std=0.02)    # the real geometry
+G2 = Geometry(n=4, d=4096, K=512, w_std=0.015)   # the scaled-up width
+
+
+@dataclass
+class WeightSet:
+    w_norm: np.ndarray  # [N] float32
+    gate: np.ndarray    # [N] float32
+    W_down: np.ndarray  # [K][N] uint16 (BF16)
+    W_up: np.ndarray    # [N][K] uint16 (BF16)
+
+
+@dataclass
+class Activations:
+    R: np.ndarray             # [T][N] float32
+    P: np.ndarray | None      # [T][N] float32 or None (pending write off)
+
+
+def weight_set(g: Geometry, j: int = 0, s0: int = 0) -> WeightSet:
+    seed = s0 + 1 + j
+    return WeightSet(
+        w_norm=normal_f32(seed, TID_WNORM, 1.0, 0.05, (g.N,)),
+        gate=normal_f32(seed, TID_GATE, 0.0, 1.0, (g.N,)),
+        W_down=normal_bf16(seed, TID_WDOWN, 0.0, g.w_std, (g.K, g.N)),
+        W_up=normal_bf16(seed, TID_WUP, 0.0, g.w_std, (g.N, g.K)),
+    )
+
+
+def activations(g: Geometry, T: int, pending: bool, s0: int = 0) -> Activations:
+    R = normal_f32(s0, TID_R, 0.0, 1.0, (T, g.N))
+    P = normal_f32(s0, TID_P, 0.0, 0.1, (T, g.N)) if pending else None
+    return Activations(R=R, P=P)

@@ -1,0 +1,60 @@
+"""The seeded input generator (no GPU): SplitMix64 against its published
+output, Box-Muller moments, BF16 rounding, thread-count independence."""
+
+import numpy as np
+
+import synth
+
+
+def test_splitmix64_published_sequence():
+    # SplitMix64 seeded with 1234567 (state += gamma, then mix): the first five
+    # outputs as listed with the reference C implementation.
+    want = [6457827717110365317, 3203168211198807973, 9817491932198370423,
+            4593380528125082431, 16408922859458223821]
+    assert [synth.raw(1234567, j) for j in range(5)] == want
+
+
+def test_normal_moments_and_determinism():
+    a = synth.normal_f32(0, synth.TID_R, 0.0, 1.0, (1 << 20,))
+    assert abs(float(a.mean())) < 5e-3
+    assert abs(float(a.std()) - 1.0) < 5e-3
+    b = synth.normal_f32(0, synth.TID_R, 0.0, 1.0, (1 << 20,))
+    assert np.array_equal(a, b)
+    c = synth.normal_f32(1, synth.TID_R, 0.0, 1.0, (1 << 20,))
+    assert not np.array_equal(a, c)
+
+
+def test_prefix_property():
+    # Element j does not depend on the array length (counter form), so T=1
+    # activations are row 0 of the T=8 ones.
+    g = synth.G1
+    a8 = synth.activations(g, 8, True)
+    a1 = synth.activations(g, 1, True)
+    assert np.array_equal(a8.R[:1], a1.R) and np.array_equal(a8.P[:1], a1.P)
+
+
+def test_bf16_round_to_nearest_even():
+    f = synth.normal_f32(3, synth.TID_WDOWN, 0.0, 0.02, (1 << 18,))
+    h = synth.normal_bf16(3, synth.TID_WDOWN, 0.0, 0.02, (1 << 18,))
+    back = synth.bf16_to_f32(h).astype(np.float64)
+    f64 = f.astype(np.float64)
+    # |x - bf16(x)| <= half an ulp of bf16 (8 significant bits)
+    ulp = np.exp2(np.floor(np.log2(np.abs(f64))) - 7)
+    assert np.all(np.abs(back - f64) <= ulp / 2)
+    # ties go to the even pattern
+    ties = np.array([0x3F808000, 0x3F818000], np.uint32).view(np.float32)
+    bits = np.empty(2, np.uint16)
+    # a tie can only be tested through the generator's rounding routine indirectly:
+    # draw values, keep those that are exact ties, and check even results
+    raw = f.view(np.uint32)
+    tie = (raw & 0xFFFF) == 0x8000
+    if tie.any():
+        assert np.all((h[tie] & 1) == 0)
+    del ties, bits
+
+
+def test_weight_set_shapes():
+    ws = synth.weight_set(synth.Geometry(n=4, d=16, K=8, w_std=0.02), j=2)
+    assert ws.W_down.shape == (8, 64) and ws.W_up.shape == (64, 8)
+    assert ws.w_norm.shape == (64,) and ws.gate.shape == (64,)
+    assert ws.W_down.dtype == np.uint16
