@@ -1,0 +1,526 @@
+"""Benchmark of the GB300 hyper-connection read.
+
+Metric: microseconds per hyper-connection read and achieved HBM GB/s with cold
+weights at T = 1..8.  One step is the cold read sweep at n=4, d=2560, K=320:
+for every T in (1, 2, 3, 4, 5, 6, 8) with the pending write off and on, 300
+reads rotated over 16 weight sets (16 x 13.1 MB > the 129 MB L2), each case
+captured once as a CUDA graph and replayed.  `value` is the algorithmic bytes
+of every read of the step divided by the step time (GB/s, higher is better);
+`us_per_read` gives the per-case times.
+
+Also reported on the same line: the 96-read chained window graph (T=4), the
+scaled-up width (d=4096, K=512) and the T=16/32/64 batches, the roofline of the
+read, an end-to-end figure through host buffers, and the FP64 oracle timed on
+one host core (a baseline only).
+
+`--impl reference` times the FP64 oracle as the reference arm (host cores, a
+bounded sample of the same workload per step).
+
+Multi-GPU: one process per GPU (torchrun); every rank runs the same workload
+on its own GPU (replicas, weak scaling, no collective on the data path).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "µs per hyper-connection read and achieved HBM GB/s (cold weights) at T=1..8"
+EPS = 1e-6
+SWEEP_T = (1, 2, 3, 4, 5, 6, 8)
+CALLS = 300
+SETS = 16
+WINDOW_READS = 96
+WINDOW_T = 4
+
+
+def read_bytes(g: synth.Geometry, T: int, pending: bool) -> int:
+    """Algorithmic bytes of one read: each byte the read must move, once.
+
+    weights 4*K*N (W_down + W_up, BF16) + w_norm and gate 8*N + per token:
+    R in and out 8*N, mean 4*d, lo 4*K, pending 4*N when on.
+    """
+    per_token = 8 * g.N + 4 * g.d + 4 * g.K + (4 * g.N if pending else 0)
+    return 4 * g.K * g.N + 8 * g.N + T * per_token
+
+
+def sweep_cases():
+    return [(T, p) for T in SWEEP_T for p in (False, True)]
+
+
+# --------------------------------------------------------------------- helpers
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "hyper_connection_residual_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def profiled_traffic() -> dict | None:
+    """DRAM bytes per read from a committed ncu summary, if it matches these kernels."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    if d.get("kernel_hash") != kernel_source_hash():
+        return None
+    return d
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while it runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines: list[str] = []
+        self._t = None
+
+    def __enter__(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if self.gpu_id:
+            cmd[1:1] = ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+            self._t = threading.Thread(target=self._drain, daemon=True)
+            self._t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _drain(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self._t is not None:
+                self._t.join(timeout=2)
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[3:7]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_uuid(dev) -> str | None:
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:  # noqa: BLE001 - older torch
+        return None
+    return u if u.startswith("GPU-") else f"GPU-{u}"
+
+
+# --------------------------------------------------------------------- oracle arms
+
+class OracleWork:
+    """The FP64 oracle, as it stands, on the sweep's inputs (prepared once,
+    outside any timed region); one host thread."""
+
+    def __init__(self):
+        import oracle
+        self.g = synth.G1
+        self.orc = oracle.default()
+        self.ws = [synth.weight_set(self.g, j) for j in range(2)]
+        self.act = synth.activations(self.g, max(SWEEP_T), True)
+        self.k = 0
+
+    def read(self, case) -> int:
+        """One oracle read of `case` = (T, pending); returns its algorithmic bytes."""
+        T, p = case
+        g, w, act = self.g, self.ws[self.k % len(self.ws)], self.act
+        self.k += 1
+        self.orc.read(g.n, g.d, g.K, R=act.R[:T], P=act.P[:T] if p else None, w_norm=w.w_norm,
+                      W_down=w.W_down, W_up=w.W_up, gate=w.gate, eps=EPS)
+        return read_bytes(g, T, p)
+
+    def sample(self, seconds: float, cases):
+        """Cycle the cases, one read each, until `seconds` have passed."""
+        done, reads = 0, 0
+        t0 = time.perf_counter()
+        while True:
+            done += self.read(cases[reads % len(cases)])
+            reads += 1
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                return done, reads, el
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    cases = sweep_cases()
+    work = OracleWork()
+    # one step = one oracle read of one case of the sweep, cycling through the cases
+    for s in range(args.warmup):
+        work.read(cases[s % len(cases)])
+    total_bytes = 0
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        total_bytes += work.read(cases[s % len(cases)])
+    elapsed = time.perf_counter() - t0
+    gbs = total_bytes / elapsed / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * elapsed / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "cold read sweep, n=4 d=2560 K=320, T in (1,2,3,4,5,6,8), "
+                               "pending off/on; one FP64 oracle read per step, cycling the cases"},
+        "us_per_read": 1e6 * elapsed / max(1, args.steps),
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{args.steps} oracle reads, one per step over the sweep's 14 cases"},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------- GPU arm
+
+class Sweep:
+    """Device-resident inputs and one captured graph per case."""
+
+    def __init__(self, hc, torch, dev, g: synth.Geometry, Ts, pendings, sets: int, calls: int,
+                 stream):
+        self.g, self.calls = g, calls
+        self.torch, self.hc, self.dev, self.stream = torch, hc, dev, stream
+        Tmax = max(Ts)
+        self.ws = []
+        for j in range(sets):
+            w = synth.weight_set(g, j)
+            self.ws.append(dict(
+                w_norm=torch.from_numpy(w.w_norm).to(dev), gate=torch.from_numpy(w.gate).to(dev),
+                W_down=torch.from_numpy(w.W_down.view(np.int16)).to(dev),
+                W_up=torch.from_numpy(w.W_up.view(np.int16)).to(dev)))
+        act = synth.activations(g, Tmax, True)
+        self.R = torch.from_numpy(act.R).to(dev)
+        self.P = torch.from_numpy(act.P).to(dev)
+        self.out = torch.empty(Tmax, g.N, device=dev)
+        self.mean = torch.empty(Tmax, g.d, device=dev)
+        self.lo = torch.empty(Tmax, g.K, device=dev)
+        self.rd = hc.Read(g.n, g.d, g.K, T_max=max(8, Tmax), eps=EPS)
+        self.cases = [(T, p) for T in Ts for p in pendings]
+        self.graphs = {}
+        for case in self.cases:
+            self.graphs[case] = self._capture(*case)
+
+    def _launch(self, T, pending, j):
+        w = self.ws[j % len(self.ws)]
+        self.rd(self.R, w["w_norm"], w["W_down"], w["W_up"], w["gate"],
+                self.P if pending else None, T, self.out, self.mean, self.lo, stream=self.stream)
+
+    def _capture(self, T, pending):
+        hc = self.hc
+        with self.torch.cuda.stream(self.stream):
+            hc.hc_graph_begin(self.stream)
+            for j in range(self.calls):
+                self._launch(T, pending, j)
+            return hc.hc_graph_end(self.stream)
+
+    def replay(self, case):
+        self.hc.hc_graph_launch(self.graphs[case], self.stream)
+
+    def bytes_per_replay(self, case):
+        return self.calls * read_bytes(self.g, *case)
+
+    def close(self):
+        for gr in self.graphs.values():
+            self.hc.hc_graph_destroy(gr)
+        self.graphs = {}
+        self.rd.close()
+
+
+def time_cases(torch, sweep: Sweep, steps: int, warmup: int, stream):
+    """Replay every case `steps` times; returns (total seconds, per-case seconds)."""
+    for _ in range(warmup):
+        for case in sweep.cases:
+            sweep.replay(case)
+    stream.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(sweep.cases) + 1)]
+           for _ in range(steps)]
+    per_case = {c: 0.0 for c in sweep.cases}
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for s in range(steps):
+        evs[s][0].record(stream)
+        for i, case in enumerate(sweep.cases):
+            sweep.replay(case)
+            evs[s][i + 1].record(stream)
+    stop.record(stream)
+    stop.synchronize()
+    for s in range(steps):
+        for i, case in enumerate(sweep.cases):
+            per_case[case] += evs[s][i].elapsed_time(evs[s][i + 1]) / 1e3
+    return start.elapsed_time(stop) / 1e3, per_case
+
+
+def run_window(torch, hc, dev, stream, replays: int):
+    """96 chained reads (out_i is R_{i+1}) with distinct weight sets, T=4,
+    captured once and replayed."""
+    g = synth.G1
+    T = WINDOW_T
+    ws = []
+    for j in range(WINDOW_READS):
+        w = synth.weight_set(g, 100 + j)
+        ws.append(dict(w_norm=torch.from_numpy(w.w_norm).to(dev), gate=torch.from_numpy(w.gate).to(dev),
+                       W_down=torch.from_numpy(w.W_down.view(np.int16)).to(dev),
+                       W_up=torch.from_numpy(w.W_up.view(np.int16)).to(dev)))
+    act = synth.activations(g, T, False)
+    R0 = torch.from_numpy(act.R).to(dev)
+    bufs = [torch.empty(T, g.N, device=dev) for _ in range(WINDOW_READS + 1)]
+    mean = torch.empty(T, g.d, device=dev)
+    lo = torch.empty(T, g.K, device=dev)
+    rd = hc.Read(g.n, g.d, g.K, T_max=8, eps=EPS)
+    with torch.cuda.stream(stream):
+        hc.hc_graph_begin(stream)
+        for i in range(WINDOW_READS):
+            w = ws[i]
+            rd(bufs[i], w["w_norm"], w["W_down"], w["W_up"], w["gate"], None, T,
+               bufs[i + 1], mean, lo, stream=stream)
+        graph = hc.hc_graph_end(stream)
+    bufs[0].copy_(R0)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        hc.hc_graph_launch(graph, stream)
+    stream.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(replays):
+        hc.hc_graph_launch(graph, stream)
+    b.record(stream)
+    b.synchronize()
+    sec = a.elapsed_time(b) / 1e3 / replays
+    hc.hc_graph_destroy(graph)
+    rd.close()
+    nbytes = WINDOW_READS * read_bytes(g, T, False)
+    return {"reads": WINDOW_READS, "T": T, "replays": replays,
+            "us_per_replay": sec * 1e6, "us_per_read": sec * 1e6 / WINDOW_READS,
+            "GBps": nbytes / sec / 1e9, "bytes_per_replay": nbytes}
+
+
+def run_gpu(args):
+    import torch
+    import hyper_connection_residual_gb300 as hc
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the read has no CPU path)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    hc.load()
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    stream = torch.cuda.Stream(device=dev)
+    g = synth.G1
+    sweep = Sweep(hc, torch, dev, g, SWEEP_T, (False, True), SETS, CALLS, stream)
+    step_bytes = sum(sweep.bytes_per_replay(c) for c in sweep.cases)
+
+    # ---- timed region (device-resident inputs)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_uuid(dev) if rank == 0 else None) as clocks:
+        total, per_case = time_cases(torch, sweep, args.steps, args.warmup, stream)
+    torch.cuda.synchronize()
+    if pg:
+        t = torch.tensor([total], device=dev, dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total = float(t.item())
+        pg.barrier()
+    value = world * step_bytes * args.steps / total / 1e9
+    us_per_read = {f"T{T}_{'pend' if p else 'nopend'}": 1e6 * per_case[(T, p)] / (args.steps * CALLS)
+                   for (T, p) in sweep.cases}
+    gbs_per_case = {f"T{T}_{'pend' if p else 'nopend'}":
+                    read_bytes(g, T, p) * args.steps * CALLS / per_case[(T, p)] / 1e9
+                    for (T, p) in sweep.cases}
+
+    # ---- end to end: pinned host inputs in, results out, every step
+    pin_R = torch.from_numpy(synth.activations(g, max(SWEEP_T), True).R).pin_memory()
+    pin_P = torch.from_numpy(synth.activations(g, max(SWEEP_T), True).P).pin_memory()
+    host_out = torch.empty(max(SWEEP_T), g.N).pin_memory()
+    host_mean = torch.empty(max(SWEEP_T), g.d).pin_memory()
+    h2d = sum(T * g.N * 4 * (2 if p else 1) for (T, p) in sweep.cases)
+    d2h = sum(T * (g.N + g.d) * 4 for (T, p) in sweep.cases)
+    e2e_steps = max(3, min(args.steps, 20))
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    ea = torch.cuda.Event(enable_timing=True)
+    eb = torch.cuda.Event(enable_timing=True)
+    ea.record(stream)
+    for _ in range(e2e_steps):
+        for (T, p) in sweep.cases:
+            with torch.cuda.stream(stream):
+                sweep.R[:T].copy_(pin_R[:T], non_blocking=True)
+                if p:
+                    sweep.P[:T].copy_(pin_P[:T], non_blocking=True)
+            sweep.replay((T, p))
+            with torch.cuda.stream(stream):
+                host_out[:T].copy_(sweep.out[:T], non_blocking=True)
+                host_mean[:T].copy_(sweep.mean[:T], non_blocking=True)
+    eb.record(stream)
+    eb.synchronize()
+    e2e_sec = ea.elapsed_time(eb) / 1e3
+    if pg:
+        t = torch.tensor([e2e_sec], device=dev, dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_sec = float(t.item())
+    e2e_value = world * step_bytes * e2e_steps / e2e_sec / 1e9
+    sweep.close()
+
+    extra = {}
+    if not args.quick:
+        extra["window_96_reads_T4"] = run_window(torch, hc, dev, stream, replays=100)
+        big = Sweep(hc, torch, dev, g, (16, 32, 64), (False,), SETS, CALLS, stream)
+        tb, pc = time_cases(torch, big, 5, 3, stream)
+        extra["batch_T16_32_64"] = {f"T{T}": {"us_per_read": 1e6 * pc[(T, p)] / (5 * CALLS),
+                                              "GBps": read_bytes(g, T, p) * 5 * CALLS / pc[(T, p)] / 1e9}
+                                    for (T, p) in big.cases}
+        big.close()
+        g2 = synth.G2
+        wide = Sweep(hc, torch, dev, g2, SWEEP_T, (True,), 12, CALLS, stream)
+        tw, pc = time_cases(torch, wide, 5, 3, stream)
+        extra["wide_d4096_K512_pend"] = {f"T{T}": {"us_per_read": 1e6 * pc[(T, p)] / (5 * CALLS),
+                                                   "GBps": read_bytes(g2, T, p) * 5 * CALLS / pc[(T, p)] / 1e9}
+                                         for (T, p) in wide.cases}
+        wide.close()
+
+    if rank != 0:
+        if pg:
+            pg.barrier()
+            pg.destroy_process_group()
+        return 0
+
+    peaks = measured_peaks()
+    # the read (down kernel + up kernel) is the unit: its average duration is
+    # the sweep's per-read time at T=1 with the pending write off
+    t1 = per_case[(1, False)] / (args.steps * CALLS)
+    achieved = read_bytes(g, 1, False) / t1 / 1e9
+    traffic = profiled_traffic()
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"],
+                "traffic": traffic["dram_bytes_per_read_T1"] if traffic else None,
+                "unit_of_work": "one read (down + up kernel) at T=1, pending off",
+                "peak_source": peaks["source"]}
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        b, n, el = OracleWork().sample(args.cpu_seconds, sweep_cases())
+        cpu = {"value": b / el / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"{n} FP64 oracle reads cycling the sweep's 14 cases ({el:.1f} s, 1 thread)",
+               "us_per_read": 1e6 * el / n}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32 (bf16 weights)", "data": "synthetic",
+        "config": {"workload": "cold read sweep: n=4 streams, d=2560, K=320, T in (1,2,3,4,5,6,8), "
+                               "pending write off and on, 300 reads per case rotated over 16 weight "
+                               "sets, CUDA-graph replay",
+                   "l2": "inputs larger than L2 (16 x 13.1 MB weight sets rotated)",
+                   "parallelism": f"replicas x{world}"},
+        "us_per_read": us_per_read, "GBps_per_case": gbs_per_case,
+        "roofline": roofline, "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": 2 * CALLS * len(sweep_cases()) * args.steps,
+        "clocks": clocks.summary(),
+        "extra": extra,
+        "kernel_hash": kernel_source_hash(),
+    }
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
+    ap.add_argument("--quick", action="store_true", help="skip the extra configurations")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

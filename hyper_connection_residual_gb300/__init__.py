@@ -1,0 +1,34 @@
+"""GB300 (sm_103a) hyper-connection read.
+
+The read runs only in the CUDA library ``libhcread.so`` (two hand-written
+kernels behind the C ABI of ``include/hc_read.h``).  This package is a thin
+ctypes binding with the same entry-point names; it has no CPU path.
+"""
+
+from ._binding import (  # noqa: F401
+    EXPORTS,
+    HC_ERR_ALIGN,
+    HC_ERR_ARG,
+    HC_ERR_CUDA,
+    HC_ERR_SHAPE,
+    HC_ERR_TIMEOUT,
+    HC_OK,
+    HcError,
+    Read,
+    hc_graph_begin,
+    hc_graph_destroy,
+    hc_graph_end,
+    hc_graph_launch,
+    hc_read,
+    hc_read_check,
+    hc_read_create,
+    hc_read_destroy,
+    hc_read_ex,
+    hc_read_reset,
+    hc_read_scratch_bytes,
+    library_path,
+    load,
+    status_str,
+)
+
+GEOMETRIES = {"d2560_K320": (4, 2560, 320), "d4096_K512": (4, 4096, 512)}

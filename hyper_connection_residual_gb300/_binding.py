@@ -1,0 +1,239 @@
+"""ctypes binding of libhcread.so (argument marshalling only).
+
+Every function here has the name of the C entry point it calls and does no
+arithmetic of the read: tensors are checked for device, dtype, size and
+contiguity, turned into pointers, and handed to the library.  There is no
+fallback: if the library is missing, every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+HC_OK, HC_ERR_ARG, HC_ERR_ALIGN, HC_ERR_SHAPE, HC_ERR_CUDA, HC_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
+
+# Every symbol the C header declares.
+EXPORTS = (
+    "hc_read_create", "hc_read", "hc_read_ex", "hc_read_check", "hc_read_reset",
+    "hc_read_destroy", "hc_read_scratch_bytes", "hc_status_str",
+    "hc_graph_begin", "hc_graph_end", "hc_graph_launch", "hc_graph_destroy",
+)
+
+
+class HcError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_str(status)} ({status})")
+
+
+_lib = None
+_vp = ctypes.c_void_p
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(path: str | None = None):
+    """Load libhcread.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or _build.LIB
+    if not os.path.exists(p):
+        raise RuntimeError(
+            f"CUDA library not built: {p}. Run __graft_entry__.build() "
+            "(the read has no CPU path).")
+    lib = ctypes.CDLL(p)
+    lib.hc_read_create.restype = ctypes.c_int
+    lib.hc_read_create.argtypes = [ctypes.POINTER(_vp), ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                   ctypes.c_int, ctypes.c_float, ctypes.c_int]
+    lib.hc_read.restype = ctypes.c_int
+    lib.hc_read.argtypes = [_vp] * 7 + [ctypes.c_int] + [_vp] * 4
+    lib.hc_read_ex.restype = ctypes.c_int
+    lib.hc_read_ex.argtypes = [_vp] * 7 + [ctypes.c_int] + [_vp] * 6
+    lib.hc_read_check.restype = ctypes.c_int
+    lib.hc_read_check.argtypes = [_vp]
+    lib.hc_read_reset.restype = ctypes.c_int
+    lib.hc_read_reset.argtypes = [_vp, _vp]
+    lib.hc_read_destroy.restype = None
+    lib.hc_read_destroy.argtypes = [_vp]
+    lib.hc_read_scratch_bytes.restype = ctypes.c_int64
+    lib.hc_read_scratch_bytes.argtypes = [_vp]
+    lib.hc_status_str.restype = ctypes.c_char_p
+    lib.hc_status_str.argtypes = [ctypes.c_int]
+    lib.hc_graph_begin.restype = ctypes.c_int
+    lib.hc_graph_begin.argtypes = [_vp]
+    lib.hc_graph_end.restype = ctypes.c_int
+    lib.hc_graph_end.argtypes = [_vp, ctypes.POINTER(_vp)]
+    lib.hc_graph_launch.restype = ctypes.c_int
+    lib.hc_graph_launch.argtypes = [_vp, _vp]
+    lib.hc_graph_destroy.restype = None
+    lib.hc_graph_destroy.argtypes = [_vp]
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def status_str(status: int) -> str:
+    try:
+        return load().hc_status_str(status).decode()
+    except RuntimeError:
+        return {0: "ok", -1: "invalid argument", -2: "pointer not 16-byte aligned",
+                -3: "geometry not supported", -4: "CUDA runtime error",
+                -5: "a kernel gave up on a bounded wait"}.get(status, "unknown status")
+
+
+def _check(status: int, where: str) -> None:
+    if status != HC_OK:
+        raise HcError(status, where)
+
+
+def _stream_ptr(stream) -> int | None:
+    """cudaStream_t of a torch.cuda.Stream / int / None (None = current torch stream)."""
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream or None
+    if isinstance(stream, int):
+        return stream or None
+    return stream.cuda_stream or None
+
+
+def _ptr(t, name: str, dtype_names: tuple[str, ...], numel: int | None):
+    """Device pointer of a tensor after checking it; None stays NULL; ints pass through."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor, an int pointer or None")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor (the read has no CPU path)")
+    if str(t.dtype).replace("torch.", "") not in dtype_names:
+        raise TypeError(f"{name}: dtype {t.dtype} not in {dtype_names}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if numel is not None and t.numel() < numel:
+        raise ValueError(f"{name}: has {t.numel()} elements, needs {numel}")
+    return t.data_ptr()
+
+
+_F32 = ("float32",)
+_BF16 = ("bfloat16", "uint16", "int16")
+
+
+def hc_read_create(n: int, d: int, K: int, T_max: int, eps: float = 1e-6, device: int = 0) -> int:
+    """Create a handle; returns it as an integer (free with hc_read_destroy)."""
+    h = _vp()
+    _check(load().hc_read_create(ctypes.byref(h), n, d, K, T_max, eps, device), "hc_read_create")
+    return h.value
+
+
+def hc_read_ex(h: int, geometry, R, w_norm, W_down, W_up, gate, pending, T: int,
+               out, mean, lo, r_out=None, rs=None, stream=None) -> None:
+    """Enqueue one read (see include/hc_read.h); ``geometry`` = (n, d, K) for size checks."""
+    n, d, K = geometry
+    N = n * d
+    args = (
+        _ptr(R, "R", _F32, T * N), _ptr(w_norm, "w_norm", _F32, N),
+        _ptr(W_down, "W_down", _BF16, K * N), _ptr(W_up, "W_up", _BF16, N * K),
+        _ptr(gate, "gate", _F32, N), _ptr(pending, "pending", _F32, T * N),
+    )
+    outs = (_ptr(out, "out", _F32, T * N), _ptr(mean, "mean", _F32, T * d),
+            _ptr(lo, "lo", _F32, T * K), _ptr(r_out, "r_out", _F32, T * N),
+            _ptr(rs, "rs", _F32, T * n))
+    _check(load().hc_read_ex(h, *args, T, *outs, _stream_ptr(stream)), "hc_read_ex")
+
+
+def hc_read(h: int, geometry, R, w_norm, W_down, W_up, gate, pending, T: int,
+            out, mean, lo, stream=None) -> None:
+    n, d, K = geometry
+    N = n * d
+    args = (
+        _ptr(R, "R", _F32, T * N), _ptr(w_norm, "w_norm", _F32, N),
+        _ptr(W_down, "W_down", _BF16, K * N), _ptr(W_up, "W_up", _BF16, N * K),
+        _ptr(gate, "gate", _F32, N), _ptr(pending, "pending", _F32, T * N),
+    )
+    outs = (_ptr(out, "out", _F32, T * N), _ptr(mean, "mean", _F32, T * d),
+            _ptr(lo, "lo", _F32, T * K))
+    _check(load().hc_read(h, *args, T, *outs, _stream_ptr(stream)), "hc_read")
+
+
+def hc_read_check(h: int) -> int:
+    """HC_OK or HC_ERR_TIMEOUT (synchronises the device)."""
+    st = load().hc_read_check(h)
+    if st not in (HC_OK, HC_ERR_TIMEOUT):
+        _check(st, "hc_read_check")
+    return st
+
+
+def hc_read_reset(h: int, stream=None) -> None:
+    _check(load().hc_read_reset(h, _stream_ptr(stream)), "hc_read_reset")
+
+
+def hc_read_destroy(h: int) -> None:
+    load().hc_read_destroy(h)
+
+
+def hc_read_scratch_bytes(h: int) -> int:
+    return int(load().hc_read_scratch_bytes(h))
+
+
+def hc_graph_begin(stream=None) -> None:
+    _check(load().hc_graph_begin(_stream_ptr(stream)), "hc_graph_begin")
+
+
+def hc_graph_end(stream=None) -> int:
+    g = _vp()
+    _check(load().hc_graph_end(_stream_ptr(stream), ctypes.byref(g)), "hc_graph_end")
+    return g.value
+
+
+def hc_graph_launch(graph: int, stream=None) -> None:
+    _check(load().hc_graph_launch(graph, _stream_ptr(stream)), "hc_graph_launch")
+
+
+def hc_graph_destroy(graph: int) -> None:
+    load().hc_graph_destroy(graph)
+
+
+class Read:
+    """Owning wrapper of one handle for geometry (n, d, K)."""
+
+    def __init__(self, n: int, d: int, K: int, T_max: int, eps: float = 1e-6, device: int = 0):
+        self.geometry = (n, d, K)
+        self.T_max = T_max
+        self.eps = eps
+        self.h = hc_read_create(n, d, K, T_max, eps, device)
+
+    def __call__(self, R, w_norm, W_down, W_up, gate, pending, T, out, mean, lo,
+                 r_out=None, rs=None, stream=None) -> None:
+        hc_read_ex(self.h, self.geometry, R, w_norm, W_down, W_up, gate, pending, T,
+                   out, mean, lo, r_out, rs, stream)
+
+    def check(self) -> int:
+        return hc_read_check(self.h)
+
+    def reset(self, stream=None) -> None:
+        hc_read_reset(self.h, stream)
+
+    def close(self) -> None:
+        if self.h:
+            hc_read_destroy(self.h)
+            self.h = 0
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # noqa: BLE001 - interpreter shutdown
+            pass

@@ -1,0 +1,302 @@
+// Host side of the C ABI declared in include/hc_read.h: handle and scratch
+// management, argument validation, kernel selection and launch with
+// programmatic dependent launch, CUDA-graph helpers.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <new>
+
+#include "hc_kernels.cuh"
+#include "hc_read.h"
+
+#define HC_EXPORT extern "C" __attribute__((visibility("default")))
+
+struct hc_read_s {
+  int n, d, K, T_max, device;
+  float eps;
+  void* scratch;
+  size_t scratch_bytes;
+  float* part;
+  float* ss_part;
+  unsigned* counters;
+  unsigned* err;
+  int row_groups;
+};
+
+namespace {
+
+using hc::DownArgs;
+using hc::UpArgs;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+cudaLaunchConfig_t pdl_config(dim3 grid, size_t smem, cudaStream_t st, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(hc::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+template <int D, int KD, int TT>
+cudaError_t configure_one() {
+  cudaError_t e = cudaFuncSetAttribute(hc::hc_down_kernel<D, KD, TT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       hc::DownSmem<D, KD, TT>::BYTES);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(hc::hc_up_kernel<D, KD, TT>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              hc::UpSmem<D, KD, TT>::BYTES);
+}
+
+template <int D, int KD>
+cudaError_t configure_geometry() {
+  cudaError_t e;
+  if ((e = configure_one<D, KD, 1>()) != cudaSuccess) return e;
+  if ((e = configure_one<D, KD, 2>()) != cudaSuccess) return e;
+  if ((e = configure_one<D, KD, 3>()) != cudaSuccess) return e;
+  if ((e = configure_one<D, KD, 4>()) != cudaSuccess) return e;
+  if ((e = configure_one<D, KD, 5>()) != cudaSuccess) return e;
+  if ((e = configure_one<D, KD, 6>()) != cudaSuccess) return e;
+  if ((e = configure_one<D, KD, 7>()) != cudaSuccess) return e;
+  return configure_one<D, KD, 8>();
+}
+
+template <int D, int KD, int TT>
+cudaError_t launch_pair(const DownArgs& da, const UpArgs& ua, cudaStream_t st) {
+  using G = hc::Geo<D, KD>;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t c1 = pdl_config(dim3(G::SLABS, G::ROW_GROUPS),
+                                      hc::DownSmem<D, KD, TT>::BYTES, st, attr);
+  cudaError_t e = cudaLaunchKernelEx(&c1, hc::hc_down_kernel<D, KD, TT>, da);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr2[1];
+  cudaLaunchConfig_t c2 = pdl_config(dim3(G::UP_CTAS), hc::UpSmem<D, KD, TT>::BYTES, st, attr2);
+  return cudaLaunchKernelEx(&c2, hc::hc_up_kernel<D, KD, TT>, ua);
+}
+
+template <int D, int KD>
+cudaError_t launch_geometry(int T, const DownArgs& da, const UpArgs& ua, cudaStream_t st) {
+  switch (T) {
+    case 1: return launch_pair<D, KD, 1>(da, ua, st);
+    case 2: return launch_pair<D, KD, 2>(da, ua, st);
+    case 3: return launch_pair<D, KD, 3>(da, ua, st);
+    case 4: return launch_pair<D, KD, 4>(da, ua, st);
+    case 5: return launch_pair<D, KD, 5>(da, ua, st);
+    case 6: return launch_pair<D, KD, 6>(da, ua, st);
+    case 7: return launch_pair<D, KD, 7>(da, ua, st);
+    default: return launch_pair<D, KD, 8>(da, ua, st);  // groups of 8 tokens
+  }
+}
+
+bool geometry_supported(int n, int d, int K) {
+  return n == hc::kStreams && ((d == 2560 && K == 320) || (d == 4096 && K == 512));
+}
+
+}  // namespace
+
+HC_EXPORT int hc_read_create(hc_read_t* out, int n, int d, int K, int T_max, float eps, int device) {
+  if (out == nullptr) return HC_ERR_ARG;
+  *out = nullptr;
+  if (!geometry_supported(n, d, K)) return HC_ERR_SHAPE;
+  if (T_max < 1 || T_max > hc::kMaxT || !(eps >= 0.0f) || device < 0) return HC_ERR_ARG;
+
+  int prev = -1;
+  if (cudaGetDevice(&prev) != cudaSuccess) return HC_ERR_CUDA;
+  if (cudaSetDevice(device) != cudaSuccess) return HC_ERR_CUDA;
+
+  cudaError_t e = (d == 2560) ? configure_geometry<2560, 320>() : configure_geometry<4096, 512>();
+  hc_read_s* h = nullptr;
+  if (e == cudaSuccess) {
+    h = new (std::nothrow) hc_read_s();
+    if (h == nullptr) {
+      cudaSetDevice(prev);
+      return HC_ERR_ARG;
+    }
+    const int N = n * d;
+    const int slabs = N / (d / 4);
+    h->n = n;
+    h->d = d;
+    h->K = K;
+    h->T_max = T_max;
+    h->device = device;
+    h->eps = eps;
+    h->row_groups = K / 32;
+    const size_t part_b = round_up((size_t)slabs * T_max * K * sizeof(float), 256);
+    const size_t ss_b = round_up((size_t)h->row_groups * slabs * T_max * sizeof(float), 256);
+    const size_t cnt_b = round_up((size_t)h->row_groups * sizeof(unsigned), 256);
+    const size_t err_b = 256;
+    h->scratch_bytes = part_b + ss_b + cnt_b + err_b;
+    e = cudaMalloc(&h->scratch, h->scratch_bytes);
+    if (e == cudaSuccess) {
+      char* base = static_cast<char*>(h->scratch);
+      h->part = reinterpret_cast<float*>(base);
+      h->ss_part = reinterpret_cast<float*>(base + part_b);
+      h->counters = reinterpret_cast<unsigned*>(base + part_b + ss_b);
+      h->err = reinterpret_cast<unsigned*>(base + part_b + ss_b + cnt_b);
+      e = cudaMemset(h->scratch, 0, h->scratch_bytes);
+      if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    } else {
+      h->scratch = nullptr;
+    }
+  }
+  cudaSetDevice(prev);
+  if (e != cudaSuccess) {
+    if (h != nullptr) {
+      if (h->scratch != nullptr) cudaFree(h->scratch);
+      delete h;
+    }
+    return HC_ERR_CUDA;
+  }
+  *out = h;
+  return HC_OK;
+}
+
+HC_EXPORT int hc_read_ex(hc_read_t h, const float* R, const float* w_norm, const uint16_t* W_down,
+                         const uint16_t* W_up, const float* gate, const float* pending, int T,
+                         float* out, float* mean, float* lo, float* r_out, float* rs,
+                         hc_stream_t stream) {
+  if (h == nullptr) return HC_ERR_ARG;
+  if (T < 1 || T > h->T_max) return HC_ERR_ARG;
+  if (!R || !w_norm || !W_down || !W_up || !gate || !out || !mean || !lo) return HC_ERR_ARG;
+  const void* ptrs[] = {R, w_norm, W_down, W_up, gate, pending, out, mean, lo, r_out, rs};
+  for (const void* p : ptrs) {
+    if (p != nullptr && !aligned16(p)) return HC_ERR_ALIGN;
+  }
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return HC_ERR_CUDA;
+  if (cur != h->device) return HC_ERR_ARG;
+
+  DownArgs da;
+  da.R = R;
+  da.P = pending;
+  da.w_norm = w_norm;
+  da.W_down = W_down;
+  da.part = h->part;
+  da.ss_part = h->ss_part;
+  da.counters = h->counters;
+  da.err = h->err;
+  da.lo = lo;
+  da.rs_out = rs;
+  da.T = T;
+  da.T_max = h->T_max;
+  da.eps = h->eps;
+
+  UpArgs ua;
+  ua.R = R;
+  ua.P = pending;
+  ua.gate = gate;
+  ua.W_up = W_up;
+  ua.lo = lo;
+  ua.out = out;
+  ua.mean = mean;
+  ua.r_out = r_out;
+  ua.err = h->err;
+  ua.T = T;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = (h->d == 2560) ? launch_geometry<2560, 320>(T, da, ua, st)
+                                 : launch_geometry<4096, 512>(T, da, ua, st);
+  if (e != cudaSuccess) {
+    cudaGetLastError();  // clear the sticky launch error for this thread
+    return HC_ERR_CUDA;
+  }
+  return HC_OK;
+}
+
+HC_EXPORT int hc_read(hc_read_t h, const float* R, const float* w_norm, const uint16_t* W_down,
+                      const uint16_t* W_up, const float* gate, const float* pending, int T,
+                      float* out, float* mean, float* lo, hc_stream_t stream) {
+  return hc_read_ex(h, R, w_norm, W_down, W_up, gate, pending, T, out, mean, lo, nullptr, nullptr,
+                    stream);
+}
+
+HC_EXPORT int hc_read_check(hc_read_t h) {
+  if (h == nullptr) return HC_ERR_ARG;
+  int prev = -1;
+  if (cudaGetDevice(&prev) != cudaSuccess) return HC_ERR_CUDA;
+  if (cudaSetDevice(h->device) != cudaSuccess) return HC_ERR_CUDA;
+  unsigned word = 0;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(&word, h->err, sizeof word, cudaMemcpyDeviceToHost);
+  cudaSetDevice(prev);
+  if (e != cudaSuccess) return HC_ERR_CUDA;
+  return word == 0 ? HC_OK : HC_ERR_TIMEOUT;
+}
+
+HC_EXPORT int hc_read_reset(hc_read_t h, hc_stream_t stream) {
+  if (h == nullptr) return HC_ERR_ARG;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return HC_ERR_CUDA;
+  if (cur != h->device) return HC_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t cnt_b = (size_t)h->row_groups * sizeof(unsigned);
+  cudaError_t e = cudaMemsetAsync(h->counters, 0, cnt_b, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(h->err, 0, sizeof(unsigned), st);
+  return e == cudaSuccess ? HC_OK : HC_ERR_CUDA;
+}
+
+HC_EXPORT void hc_read_destroy(hc_read_t h) {
+  if (h == nullptr) return;
+  int prev = -1;
+  if (cudaGetDevice(&prev) == cudaSuccess && cudaSetDevice(h->device) == cudaSuccess) {
+    cudaDeviceSynchronize();
+    cudaFree(h->scratch);
+    cudaSetDevice(prev);
+  }
+  delete h;
+}
+
+HC_EXPORT int64_t hc_read_scratch_bytes(hc_read_t h) {
+  return h == nullptr ? -1 : static_cast<int64_t>(h->scratch_bytes);
+}
+
+HC_EXPORT const char* hc_status_str(int status) {
+  switch (status) {
+    case HC_OK: return "ok";
+    case HC_ERR_ARG: return "invalid argument";
+    case HC_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case HC_ERR_SHAPE: return "geometry not supported";
+    case HC_ERR_CUDA: return "CUDA runtime error";
+    case HC_ERR_TIMEOUT: return "a kernel gave up on a bounded wait";
+    default: return "unknown status";
+  }
+}
+
+HC_EXPORT int hc_graph_begin(hc_stream_t stream) {
+  cudaError_t e = cudaStreamBeginCapture(static_cast<cudaStream_t>(stream),
+                                         cudaStreamCaptureModeThreadLocal);
+  return e == cudaSuccess ? HC_OK : HC_ERR_CUDA;
+}
+
+HC_EXPORT int hc_graph_end(hc_stream_t stream, hc_graph_t* exec) {
+  if (exec == nullptr) return HC_ERR_ARG;
+  *exec = nullptr;
+  cudaGraph_t g = nullptr;
+  cudaError_t e = cudaStreamEndCapture(static_cast<cudaStream_t>(stream), &g);
+  if (e != cudaSuccess) return HC_ERR_CUDA;
+  cudaGraphExec_t ge = nullptr;
+  e = cudaGraphInstantiate(&ge, g, 0);
+  cudaGraphDestroy(g);
+  if (e != cudaSuccess) return HC_ERR_CUDA;
+  *exec = ge;
+  return HC_OK;
+}
+
+HC_EXPORT int hc_graph_launch(hc_graph_t exec, hc_stream_t stream) {
+  if (exec == nullptr) return HC_ERR_ARG;
+  cudaError_t e = cudaGraphLaunch(static_cast<cudaGraphExec_t>(exec), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? HC_OK : HC_ERR_CUDA;
+}
+
+HC_EXPORT void hc_graph_destroy(hc_graph_t exec) {
+  if (exec != nullptr) cudaGraphExecDestroy(static_cast<cudaGraphExec_t>(exec));
+}

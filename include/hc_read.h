@@ -1,0 +1,132 @@
+/* hc_read.h - C ABI of the GB300 (sm_103a) hyper-connection read.
+ *
+ * The read (sources cited by page title and section):
+ *   "#2812 sycl: STRATA_GR_FUSED=1, the two-kernel BF16 hyper-connection read
+ *   (opt-in)", sections "Summary" and "What changed": the pending write is
+ *   committed (R_out), a per-stream RMS norm's sums of squares give rs, the
+ *   BF16 down projection of R' * w_norm is scaled by rs per stream into lo, and
+ *   the BF16 up projection of lo feeds an epilogue of pending write, gate and
+ *   stream mean.  Strata pull request #2070 (Turing up/down kernels): 96 reads
+ *   per window, 13 MB of BF16 weights per read.  The pages give no formula for
+ *   the epilogue; this library defines it as written below.
+ *
+ * For T tokens, n = 4 streams of width d, N = n*d, down width K, i = s*d + c:
+ *   R'[t][i]  = fl32(R[t][i] + P[t][i])          (P = 0 when pending == NULL)
+ *   ss[t][s]  = sum_c R'[t][s*d+c]^2,  rs[t][s] = 1 / sqrt(ss[t][s] / d + eps)
+ *   lo[t][k]  = sum_s rs[t][s] * sum_c W_down[k][s*d+c] * R'[t][s*d+c] * w_norm[s*d+c]
+ *   u[t][i]   = sum_k W_up[i][k] * lo[t][k]
+ *   out[t][i] = R'[t][i] + sigmoid(gate[i]) * u[t][i]
+ *   mean[t][c]= (1/n) * sum_s out[t][s*d+c]
+ *
+ * Supported geometries (compiled in): n = 4 with (d, K) = (2560, 320) or
+ * (4096, 512).  1 <= T <= T_max <= 64.
+ *
+ * Layouts (all row-major, contiguous, device memory, 16-byte aligned):
+ *   R, pending, out, r_out : float  [T][N]
+ *   w_norm, gate           : float  [N]
+ *   W_down                 : uint16 [K][N]  (BF16 bit patterns)
+ *   W_up                   : uint16 [N][K]  (BF16 bit patterns)
+ *   lo                     : float  [T][K]
+ *   mean                   : float  [T][d]
+ *   rs                     : float  [T][n]
+ *
+ * Ownership: the caller owns every tensor.  A handle owns its scratch
+ * (partial sums, per-slab sums of squares, arrival counters, an error word),
+ * allocated and zeroed by hc_read_create and freed by hc_read_destroy.
+ *
+ * Aliasing: out may equal R (in-place update of the residual).  pending must
+ * not overlap out; lo, mean, r_out and rs must not overlap any input.
+ *
+ * Asynchrony: hc_read only validates and enqueues two kernels on `stream`; it
+ * never synchronises.  Calls on one handle must be issued to one stream at a
+ * time (the scratch belongs to the handle).  The call can be captured into a
+ * CUDA graph; replays give the same bits as direct calls.  The kernels use
+ * programmatic dependent launch: each kernel prefetches its BF16 weights,
+ * w_norm and gate before it waits for the preceding kernel in the stream, so
+ * those four arrays must not be written by a kernel that immediately precedes
+ * the read on the stream and itself triggers its dependents early (kernels
+ * that do not use programmatic completion are always waited for in full).
+ *
+ * Errors: every entry point returns an hc_status (0 = HC_OK).  Argument errors
+ * are detected on the host before anything is enqueued.  HC_ERR_CUDA reports
+ * a CUDA runtime error at launch.  A kernel that gives up on a bounded wait
+ * records it in the handle's error word; hc_read_check reports it as
+ * HC_ERR_TIMEOUT, after which hc_read_reset must be called.
+ */
+#ifndef HC_READ_H
+#define HC_READ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct hc_read_s* hc_read_t;
+typedef void* hc_stream_t;  /* a cudaStream_t; NULL = the legacy default stream */
+typedef void* hc_graph_t;   /* an instantiated CUDA graph (cudaGraphExec_t) */
+
+typedef enum {
+  HC_OK = 0,
+  HC_ERR_ARG = -1,      /* null handle/pointer, T out of range, bad eps, wrong device */
+  HC_ERR_ALIGN = -2,    /* a pointer is not 16-byte aligned */
+  HC_ERR_SHAPE = -3,    /* geometry not compiled in */
+  HC_ERR_CUDA = -4,     /* CUDA runtime error (allocation, launch, capture) */
+  HC_ERR_TIMEOUT = -5   /* a kernel gave up on a bounded wait (see hc_read_check) */
+} hc_status;
+
+/* Create a read handle for geometry (n, d, K) on CUDA device `device`, for up
+ * to T_max tokens per call, with the RMS epsilon `eps` (>= 0).  Allocates and
+ * zeroes the handle's scratch on that device (synchronous).  On success *h
+ * holds the handle; on failure *h is NULL. */
+int hc_read_create(hc_read_t* h, int n, int d, int K, int T_max, float eps, int device);
+
+/* Enqueue one read of T tokens on `stream` (see the formulas above).
+ * pending may be NULL (no pending write).  The calling thread's current CUDA
+ * device must be the handle's device.  Outputs: out [T][N], mean [T][d],
+ * lo [T][K]. */
+int hc_read(hc_read_t h, const float* R, const float* w_norm, const uint16_t* W_down,
+            const uint16_t* W_up, const float* gate, const float* pending, int T,
+            float* out, float* mean, float* lo, hc_stream_t stream);
+
+/* hc_read with two optional debug outputs: r_out [T][N] receives R' (the
+ * committed residual, bit for bit one fp32 add), rs [T][n] the per-stream
+ * inverse RMS.  Either may be NULL. */
+int hc_read_ex(hc_read_t h, const float* R, const float* w_norm, const uint16_t* W_down,
+               const uint16_t* W_up, const float* gate, const float* pending, int T,
+               float* out, float* mean, float* lo, float* r_out, float* rs,
+               hc_stream_t stream);
+
+/* Synchronise with the handle's device and report the kernels' error word:
+ * HC_OK, or HC_ERR_TIMEOUT if any kernel gave up on a bounded wait since the
+ * last hc_read_reset. */
+int hc_read_check(hc_read_t h);
+
+/* Re-zero the handle's arrival counters and error word on `stream` (needed
+ * only after a read was aborted or reported HC_ERR_TIMEOUT). */
+int hc_read_reset(hc_read_t h, hc_stream_t stream);
+
+/* Free the handle's scratch.  Synchronises with the handle's device first.
+ * NULL is ignored. */
+void hc_read_destroy(hc_read_t h);
+
+/* Bytes of device scratch a handle holds (for accounting). */
+int64_t hc_read_scratch_bytes(hc_read_t h);
+
+/* Static text for a status code. */
+const char* hc_status_str(int status);
+
+/* CUDA-graph helpers for callers without a graph API of their own.
+ * hc_graph_begin starts a thread-local stream capture on `stream`;
+ * hc_graph_end ends it and instantiates the graph into *exec;
+ * hc_graph_launch replays it on `stream`; hc_graph_destroy frees it. */
+int hc_graph_begin(hc_stream_t stream);
+int hc_graph_end(hc_stream_t stream, hc_graph_t* exec);
+int hc_graph_launch(hc_graph_t exec, hc_stream_t stream);
+void hc_graph_destroy(hc_graph_t exec);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HC_READ_H */

@@ -1,0 +1,206 @@
+"""GPU parity of the CUDA read against the FP64 oracle, through the C ABI.
+
+Bar: max|gpu - oracle| <= 1e-4 * max|oracle| for lo, out, mean (and rs);
+R' (r_out) bit for bit; graph replays and repeated calls bit for bit equal to
+a direct call.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_util import EPS, assert_parity, bits, dev_act, dev_weights, outputs, run
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+hc = pytest.importorskip("hyper_connection_residual_gb300")
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    d = torch.device("cuda:0")
+    torch.cuda.set_device(d)
+    return d
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.default()
+
+
+@pytest.fixture(scope="module")
+def g1(dev):
+    g = synth.G1
+    ws = synth.weight_set(g, 0)
+    return g, ws, dev_weights(ws, dev)
+
+
+@pytest.fixture(scope="module")
+def rd1(dev):
+    r = hc.Read(4, 2560, 320, T_max=64, eps=EPS)
+    yield r
+    r.close()
+
+
+def oracle_read(orc, g, ws, act):
+    return orc.read(g.n, g.d, g.K, R=act.R, P=act.P, w_norm=ws.w_norm, W_down=ws.W_down,
+                    W_up=ws.W_up, gate=ws.gate, eps=EPS)
+
+
+@pytest.mark.parametrize("pending", [False, True], ids=["pend_off", "pend_on"])
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 6, 7, 8])
+def test_parity_real_geometry(dev, orc, g1, rd1, T, pending):
+    g, ws, w = g1
+    act = synth.activations(g, T, pending, s0=100 + T)
+    a = dev_act(act, dev)
+    o = outputs(g, T, dev)
+    run(rd1, w, a, T, o)
+    torch.cuda.synchronize()
+    assert rd1.check() == hc.HC_OK
+    assert_parity(o, oracle_read(orc, g, ws, act), T, f"T={T} pending={pending}")
+
+
+@pytest.mark.parametrize("T", [9, 13, 16, 33, 64])
+def test_parity_token_groups(dev, orc, g1, rd1, T):
+    """T > 8 runs in groups of 8 tokens with a ragged last group."""
+    g, ws, w = g1
+    act = synth.activations(g, T, True, s0=200 + T)
+    a = dev_act(act, dev)
+    o = outputs(g, T, dev)
+    run(rd1, w, a, T, o)
+    torch.cuda.synchronize()
+    assert_parity(o, oracle_read(orc, g, ws, act), T, f"T={T}")
+
+
+@pytest.mark.parametrize("T", [1, 5, 8, 12])
+def test_parity_scaled_geometry(dev, orc, T):
+    g = synth.G2
+    ws = synth.weight_set(g, 0)
+    w = dev_weights(ws, dev)
+    act = synth.activations(g, T, True, s0=300 + T)
+    a = dev_act(act, dev)
+    o = outputs(g, T, dev)
+    with hc.Read(4, 4096, 512, T_max=16, eps=EPS) as rd:
+        run(rd, w, a, T, o)
+        torch.cuda.synchronize()
+        assert rd.check() == hc.HC_OK
+    assert_parity(o, oracle_read(orc, g, ws, act), T, f"G2 T={T}")
+
+
+def test_zero_weights_give_committed_residual(dev, rd1):
+    """Invariant: zero projections give out = R' bit for bit."""
+    g = synth.G1
+    T = 3
+    ws = synth.weight_set(g, 1)
+    ws.W_down[:] = 0
+    ws.W_up[:] = 0
+    w = dev_weights(ws, dev)
+    act = synth.activations(g, T, True, s0=7)
+    a = dev_act(act, dev)
+    o = outputs(g, T, dev)
+    run(rd1, w, a, T, o)
+    torch.cuda.synchronize()
+    rp = (act.R + act.P).astype(np.float32)
+    assert np.array_equal(bits(o["out"]), rp.view(np.uint32))
+    assert np.array_equal(bits(o["r_out"]), rp.view(np.uint32))
+    assert float(o["lo"].abs().max()) == 0.0
+
+
+def test_repeat_and_graph_replay_bitwise(dev, g1, rd1):
+    g, ws, w = g1
+    T = 4
+    act = synth.activations(g, T, True, s0=11)
+    a = dev_act(act, dev)
+    o1 = outputs(g, T, dev)
+    run(rd1, w, a, T, o1)
+    torch.cuda.synchronize()
+    ref = {k: bits(v) for k, v in o1.items()}
+    # a second direct call (counters must have been reset by the first)
+    o2 = outputs(g, T, dev)
+    run(rd1, w, a, T, o2)
+    torch.cuda.synchronize()
+    for k in ref:
+        assert np.array_equal(bits(o2[k]), ref[k]), f"repeat {k}"
+    # captured once, replayed twice
+    s = torch.cuda.Stream()
+    o3 = outputs(g, T, dev)
+    with torch.cuda.stream(s):
+        hc.hc_graph_begin(s)
+        run(rd1, w, a, T, o3, stream=s)
+        graph = hc.hc_graph_end(s)
+    try:
+        for rep in range(2):
+            for v in o3.values():
+                v.fill_(float("nan"))
+            torch.cuda.synchronize()
+            hc.hc_graph_launch(graph, s)
+            s.synchronize()
+            for k in ref:
+                assert np.array_equal(bits(o3[k]), ref[k]), f"replay {rep} {k}"
+    finally:
+        hc.hc_graph_destroy(graph)
+
+
+def test_in_place_update(dev, g1, rd1):
+    """out may alias R: the residual is updated in place."""
+    g, ws, w = g1
+    T = 2
+    act = synth.activations(g, T, True, s0=12)
+    a = dev_act(act, dev)
+    o = outputs(g, T, dev)
+    run(rd1, w, a, T, o)
+    a2 = dev_act(act, dev)
+    o2 = outputs(g, T, dev)
+    rd1(a2["R"], w["w_norm"], w["W_down"], w["W_up"], w["gate"], a2["P"], T,
+        a2["R"], o2["mean"], o2["lo"])
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(a2["R"]), bits(o["out"]))
+    assert np.array_equal(bits(o2["mean"]), bits(o["mean"]))
+
+
+def test_t1_is_row0_of_repeated_rows(dev, g1, rd1):
+    """A T=8 call whose 8 tokens are copies of one token gives, on every row,
+    the T=1 result bit for bit (tokens are independent)."""
+    g, ws, w = g1
+    act1 = synth.activations(g, 1, True, s0=13)
+    a1 = dev_act(act1, dev)
+    o1 = outputs(g, 1, dev)
+    run(rd1, w, a1, 1, o1)
+    a8 = {k: v.repeat(8, 1) for k, v in a1.items()}
+    o8 = outputs(g, 8, dev)
+    run(rd1, w, a8, 8, o8)
+    torch.cuda.synchronize()
+    for k in ("out", "mean", "lo", "r_out", "rs"):
+        b1 = bits(o1[k])
+        b8 = bits(o8[k])
+        for t in range(8):
+            assert np.array_equal(b8[t], b1[0]), f"{k} row {t}"
+
+
+def test_argument_errors(dev, g1, rd1):
+    g, ws, w = g1
+    act = synth.activations(g, 2, False)
+    a = dev_act(act, dev)
+    o = outputs(g, 2, dev)
+    lib = hc.load()
+    ptrs = [a["R"].data_ptr(), w["w_norm"].data_ptr(), w["W_down"].data_ptr(),
+            w["W_up"].data_ptr(), w["gate"].data_ptr(), None]
+    outs = [o["out"].data_ptr(), o["mean"].data_ptr(), o["lo"].data_ptr()]
+    assert lib.hc_read(rd1.h, *ptrs, 0, *outs, None) == hc.HC_ERR_ARG
+    assert lib.hc_read(rd1.h, *ptrs, 65, *outs, None) == hc.HC_ERR_ARG
+    bad = list(ptrs)
+    bad[0] += 4
+    assert lib.hc_read(rd1.h, *bad, 1, *outs, None) == hc.HC_ERR_ALIGN
+    bad = list(ptrs)
+    bad[2] = None
+    assert lib.hc_read(rd1.h, *bad, 1, *outs, None) == hc.HC_ERR_ARG
+    with pytest.raises(ValueError):
+        rd1(a["R"].cpu(), w["w_norm"], w["W_down"], w["W_up"], w["gate"], None, 1,
+            o["out"], o["mean"], o["lo"])
+    with pytest.raises(hc.HcError):
+        hc.Read(4, 2560, 320, T_max=0)
+    assert rd1.check() == hc.HC_OK
