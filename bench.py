@@ -364,6 +364,38 @@ def run_window(torch, hc, dev, stream, replays: int):
             "GBps": nbytes / sec / 1e9, "bytes_per_replay": nbytes}
 
 
+def run_profile_case():
+    """Four cold reads at T=1 and four at T=8 (pending on), each after a 256 MB
+    write that flushes L2; used as the small case of ncu captures."""
+    import torch
+    import hyper_connection_residual_gb300 as hc
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    g = synth.G1
+    ws = []
+    for j in range(4):
+        w = synth.weight_set(g, j)
+        ws.append(dict(w_norm=torch.from_numpy(w.w_norm).to(dev), gate=torch.from_numpy(w.gate).to(dev),
+                       W_down=torch.from_numpy(w.W_down.view(np.int16)).to(dev),
+                       W_up=torch.from_numpy(w.W_up.view(np.int16)).to(dev)))
+    act = synth.activations(g, 8, True)
+    R = torch.from_numpy(act.R).to(dev)
+    P = torch.from_numpy(act.P).to(dev)
+    out = torch.empty(8, g.N, device=dev)
+    mean = torch.empty(8, g.d, device=dev)
+    lo = torch.empty(8, g.K, device=dev)
+    flush = torch.empty(64 * 1024 * 1024, device=dev)
+    with hc.Read(g.n, g.d, g.K, T_max=8, eps=EPS) as rd:
+        for T in (1, 8):
+            for w in ws:
+                flush.zero_()
+                rd(R, w["w_norm"], w["W_down"], w["W_up"], w["gate"], P, T, out, mean, lo)
+        torch.cuda.synchronize()
+        assert rd.check() == hc.HC_OK
+    print("profile case done")
+    return 0
+
+
 def run_gpu(args):
     import torch
     import hyper_connection_residual_gb300 as hc
@@ -382,7 +414,8 @@ def run_gpu(args):
 
     stream = torch.cuda.Stream(device=dev)
     g = synth.G1
-    sweep = Sweep(hc, torch, dev, g, SWEEP_T, (False, True), SETS, CALLS, stream)
+    calls = args.calls
+    sweep = Sweep(hc, torch, dev, g, SWEEP_T, (False, True), SETS, calls, stream)
     step_bytes = sum(sweep.bytes_per_replay(c) for c in sweep.cases)
 
     # ---- timed region (device-resident inputs)
@@ -398,10 +431,10 @@ def run_gpu(args):
         total = float(t.item())
         pg.barrier()
     value = world * step_bytes * args.steps / total / 1e9
-    us_per_read = {f"T{T}_{'pend' if p else 'nopend'}": 1e6 * per_case[(T, p)] / (args.steps * CALLS)
+    us_per_read = {f"T{T}_{'pend' if p else 'nopend'}": 1e6 * per_case[(T, p)] / (args.steps * calls)
                    for (T, p) in sweep.cases}
     gbs_per_case = {f"T{T}_{'pend' if p else 'nopend'}":
-                    read_bytes(g, T, p) * args.steps * CALLS / per_case[(T, p)] / 1e9
+                    read_bytes(g, T, p) * args.steps * calls / per_case[(T, p)] / 1e9
                     for (T, p) in sweep.cases}
 
     # ---- end to end: pinned host inputs in, results out, every step
@@ -464,7 +497,7 @@ def run_gpu(args):
     peaks = measured_peaks()
     # the read (down kernel + up kernel) is the unit: its average duration is
     # the sweep's per-read time at T=1 with the pending write off
-    t1 = per_case[(1, False)] / (args.steps * CALLS)
+    t1 = per_case[(1, False)] / (args.steps * calls)
     achieved = read_bytes(g, 1, False) / t1 / 1e9
     traffic = profiled_traffic()
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -494,7 +527,7 @@ def run_gpu(args):
         "roofline": roofline, "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-        "gpu_launches": 2 * CALLS * len(sweep_cases()) * args.steps,
+        "gpu_launches": 2 * calls * len(sweep_cases()) * args.steps,
         "clocks": clocks.summary(),
         "extra": extra,
         "kernel_hash": kernel_source_hash(),
@@ -515,10 +548,16 @@ def main(argv=None):
     ap.add_argument("--quick", action="store_true", help="skip the extra configurations")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--calls", type=int, default=CALLS, help="reads per case (default 300)")
+    ap.add_argument("--profile", action="store_true",
+                    help="no timing: a few cold direct reads at T=1 and T=8 (L2 flushed "
+                         "before each), a small case for ncu captures")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     if args.impl == "reference":
         return run_reference(args)
+    if args.profile:
+        return run_profile_case()
     return run_gpu(args)
 
 
