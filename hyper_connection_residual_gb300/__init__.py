@@ -12,6 +12,8 @@ from ._binding import (  # noqa: F401
     HC_ERR_CUDA,
     HC_ERR_SHAPE,
     HC_ERR_TIMEOUT,
+    HC_ERR_TOO_LARGE,
+    HC_NOALLOC_MAX_T,
     HC_OK,
     HcError,
     Read,
@@ -24,6 +26,7 @@ from ._binding import (  # noqa: F401
     hc_read_create,
     hc_read_destroy,
     hc_read_ex,
+    hc_read_noalloc,
     hc_read_reset,
     hc_read_scratch_bytes,
     library_path,

@@ -14,12 +14,15 @@ import os
 from . import build as _build
 
 HC_OK, HC_ERR_ARG, HC_ERR_ALIGN, HC_ERR_SHAPE, HC_ERR_CUDA, HC_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
+HC_ERR_TOO_LARGE = -6
+HC_NOALLOC_MAX_T = 8
 
 # Every symbol the C header declares.
 EXPORTS = (
     "hc_read_create", "hc_read", "hc_read_ex", "hc_read_check", "hc_read_reset",
     "hc_read_destroy", "hc_read_scratch_bytes", "hc_status_str",
     "hc_graph_begin", "hc_graph_end", "hc_graph_launch", "hc_graph_destroy",
+    "hc_read_noalloc",
 )
 
 
@@ -73,6 +76,9 @@ def load(path: str | None = None):
     lib.hc_graph_launch.argtypes = [_vp, _vp]
     lib.hc_graph_destroy.restype = None
     lib.hc_graph_destroy.argtypes = [_vp]
+    lib.hc_read_noalloc.restype = ctypes.c_int
+    lib.hc_read_noalloc.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float] + \
+        [_vp] * 6 + [ctypes.c_int] + [_vp] * 4
     if path is None:
         _lib = lib
     return lib
@@ -84,7 +90,8 @@ def status_str(status: int) -> str:
     except RuntimeError:
         return {0: "ok", -1: "invalid argument", -2: "pointer not 16-byte aligned",
                 -3: "geometry not supported", -4: "CUDA runtime error",
-                -5: "a kernel gave up on a bounded wait"}.get(status, "unknown status")
+                -5: "a kernel gave up on a bounded wait",
+                -6: "T exceeds the no-allocation entry point's maximum"}.get(status, "unknown status")
 
 
 def _check(status: int, where: str) -> None:
@@ -161,6 +168,26 @@ def hc_read(h: int, geometry, R, w_norm, W_down, W_up, gate, pending, T: int,
     outs = (_ptr(out, "out", _F32, T * N), _ptr(mean, "mean", _F32, T * d),
             _ptr(lo, "lo", _F32, T * K))
     _check(load().hc_read(h, *args, T, *outs, _stream_ptr(stream)), "hc_read")
+
+
+def hc_read_noalloc(geometry, eps, R, w_norm, W_down, W_up, gate, pending, T: int,
+                    out, mean, lo, stream=None) -> None:
+    """The read without a handle or any device allocation (T <= HC_NOALLOC_MAX_T).
+
+    For callers that cannot allocate device memory at the point of use; see
+    include/hc_read.h.  The first call on a device does a one-time set-up and
+    should come before any stream capture; overlapping calls race."""
+    n, d, K = geometry
+    N = n * d
+    args = (
+        _ptr(R, "R", _F32, T * N), _ptr(w_norm, "w_norm", _F32, N),
+        _ptr(W_down, "W_down", _BF16, K * N), _ptr(W_up, "W_up", _BF16, N * K),
+        _ptr(gate, "gate", _F32, N), _ptr(pending, "pending", _F32, T * N),
+    )
+    outs = (_ptr(out, "out", _F32, T * N), _ptr(mean, "mean", _F32, T * d),
+            _ptr(lo, "lo", _F32, T * K))
+    _check(load().hc_read_noalloc(n, d, K, eps, *args, T, *outs, _stream_ptr(stream)),
+           "hc_read_noalloc")
 
 
 def hc_read_check(h: int) -> int:

@@ -5,6 +5,7 @@
 
 #include <cstdint>
 #include <cstdlib>
+#include <mutex>
 #include <new>
 
 #include "hc_kernels.cuh"
@@ -267,6 +268,7 @@ HC_EXPORT const char* hc_status_str(int status) {
     case HC_ERR_SHAPE: return "geometry not supported";
     case HC_ERR_CUDA: return "CUDA runtime error";
     case HC_ERR_TIMEOUT: return "a kernel gave up on a bounded wait";
+    case HC_ERR_TOO_LARGE: return "T exceeds the no-allocation entry point's maximum";
     default: return "unknown status";
   }
 }
@@ -299,4 +301,108 @@ HC_EXPORT int hc_graph_launch(hc_graph_t exec, hc_stream_t stream) {
 
 HC_EXPORT void hc_graph_destroy(hc_graph_t exec) {
   if (exec != nullptr) cudaGraphExecDestroy(static_cast<cudaGraphExec_t>(exec));
+}
+
+// ---------------------------------------------------------------------------
+// No-allocation entry point.  Its scratch is one file-scope device array
+// (partials, per-slab sums of squares, arrival counters, error word), sized
+// for the largest supported geometry (d = 4096, K = 512: 16 row groups) at
+// T <= HC_NOALLOC_MAX_T.  Host code must not hand the array's name to a
+// kernel (on the host it only stands for the symbol); the device address is
+// looked up once per device with cudaGetSymbolAddress.
+namespace {
+
+constexpr size_t kNoallocPartBytes = (size_t)16 * HC_NOALLOC_MAX_T * 512 * sizeof(float);
+constexpr size_t kNoallocSsBytes = (size_t)16 * 16 * HC_NOALLOC_MAX_T * sizeof(float);
+constexpr size_t kNoallocTailBytes = 256;  // 16 counters + the error word
+static_assert(kNoallocPartBytes + kNoallocSsBytes + kNoallocTailBytes == HC_NOALLOC_SCRATCH_BYTES,
+              "scratch size in the header and here disagree");
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_scratch_addr[kMaxDevices];
+
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[HC_NOALLOC_SCRATCH_BYTES];
+
+HC_EXPORT int hc_read_noalloc(int n, int d, int K, float eps, const float* R, const float* w_norm,
+                              const uint16_t* W_down, const uint16_t* W_up, const float* gate,
+                              const float* pending, int T, float* out, float* mean, float* lo,
+                              hc_stream_t stream) {
+  if (!geometry_supported(n, d, K)) return HC_ERR_SHAPE;
+  if (!(eps >= 0.0f) || T < 1) return HC_ERR_ARG;
+  if (T > HC_NOALLOC_MAX_T) return HC_ERR_TOO_LARGE;
+  if (!R || !w_norm || !W_down || !W_up || !gate || !out || !mean || !lo) return HC_ERR_ARG;
+  const void* ptrs[] = {R, w_norm, W_down, W_up, gate, pending, out, mean, lo};
+  for (const void* p : ptrs) {
+    if (p != nullptr && !aligned16(p)) return HC_ERR_ALIGN;
+  }
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return HC_ERR_CUDA;
+
+  // Set-up, once per device, with that device current: the scratch array's
+  // device address and the kernels' shared-memory attributes.
+  void* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (g_noalloc_scratch_addr[dev] == nullptr) {
+      void* addr = nullptr;
+      if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr) {
+        cudaGetLastError();
+        return HC_ERR_CUDA;
+      }
+      if (configure_geometry<2560, 320>() != cudaSuccess ||
+          configure_geometry<4096, 512>() != cudaSuccess) {
+        cudaGetLastError();
+        return HC_ERR_CUDA;
+      }
+      g_noalloc_scratch_addr[dev] = addr;
+    }
+    base = g_noalloc_scratch_addr[dev];
+  }
+
+  char* b = static_cast<char*>(base);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned* counters = reinterpret_cast<unsigned*>(b + kNoallocPartBytes + kNoallocSsBytes);
+  // The arrival counters and the error word must start at zero.
+  if (cudaMemsetAsync(counters, 0, kNoallocTailBytes, st) != cudaSuccess) {
+    cudaGetLastError();
+    return HC_ERR_CUDA;
+  }
+
+  DownArgs da;
+  da.R = R;
+  da.P = pending;
+  da.w_norm = w_norm;
+  da.W_down = W_down;
+  da.part = reinterpret_cast<float*>(b);
+  da.ss_part = reinterpret_cast<float*>(b + kNoallocPartBytes);
+  da.counters = counters;
+  da.err = counters + 16;
+  da.lo = lo;
+  da.rs_out = nullptr;
+  da.T = T;
+  da.T_max = HC_NOALLOC_MAX_T;
+  da.eps = eps;
+
+  UpArgs ua;
+  ua.R = R;
+  ua.P = pending;
+  ua.gate = gate;
+  ua.W_up = W_up;
+  ua.lo = lo;
+  ua.out = out;
+  ua.mean = mean;
+  ua.r_out = nullptr;
+  ua.err = counters + 16;
+  ua.T = T;
+
+  cudaError_t e = (d == 2560) ? launch_geometry<2560, 320>(T, da, ua, st)
+                              : launch_geometry<4096, 512>(T, da, ua, st);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return HC_ERR_CUDA;
+  }
+  return HC_OK;
 }

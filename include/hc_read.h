@@ -72,7 +72,8 @@ typedef enum {
   HC_ERR_ALIGN = -2,    /* a pointer is not 16-byte aligned */
   HC_ERR_SHAPE = -3,    /* geometry not compiled in */
   HC_ERR_CUDA = -4,     /* CUDA runtime error (allocation, launch, capture) */
-  HC_ERR_TIMEOUT = -5   /* a kernel gave up on a bounded wait (see hc_read_check) */
+  HC_ERR_TIMEOUT = -5,  /* a kernel gave up on a bounded wait (see hc_read_check) */
+  HC_ERR_TOO_LARGE = -6 /* T above the no-allocation entry point's maximum */
 } hc_status;
 
 /* Create a read handle for geometry (n, d, K) on CUDA device `device`, for up
@@ -112,6 +113,36 @@ void hc_read_destroy(hc_read_t h);
 
 /* Bytes of device scratch a handle holds (for accounting). */
 int64_t hc_read_scratch_bytes(hc_read_t h);
+
+/* hc_read without a handle and without any device allocation.
+ *
+ * The pages have no counterpart of this entry point; it exists for callers
+ * that cannot allocate device memory when they need the read: engines that
+ * reserve nearly all of HBM for weights and KV cache at start-up (a later
+ * cudaMalloc fails), code that runs inside another framework's allocator,
+ * and code paths that cannot afford cudaMalloc's implicit device-wide
+ * synchronisation.  hc_read_create needs cudaMalloc for its scratch; this
+ * entry point uses a fixed scratch array compiled into the library instead
+ * (HC_NOALLOC_SCRATCH_BYTES, held on every device that loads the library
+ * until the process exits) and calls no allocating routine.
+ *
+ * Geometry (n, d, K) and eps are passed per call (same supported set as
+ * hc_read_create); 1 <= T <= HC_NOALLOC_MAX_T, larger T returns
+ * HC_ERR_TOO_LARGE.  Other arguments, layouts and errors as hc_read.  The
+ * current device must be the device the pointers live on.
+ *
+ * The first call on a device sets that device up (it looks up the scratch
+ * array's device address and sets kernel attributes); make that first call
+ * before any stream capture.  Every call on a device shares the one scratch
+ * array: calls that overlap on the GPU (two streams, or two threads) race and
+ * give wrong results, so serialise them.  Each call clears the parts of the
+ * scratch that must start at zero on `stream` before its kernels run. */
+#define HC_NOALLOC_MAX_T 8
+#define HC_NOALLOC_SCRATCH_BYTES (16 * HC_NOALLOC_MAX_T * 512 * 4 + 16 * 16 * HC_NOALLOC_MAX_T * 4 + 256)
+int hc_read_noalloc(int n, int d, int K, float eps, const float* R, const float* w_norm,
+                    const uint16_t* W_down, const uint16_t* W_up, const float* gate,
+                    const float* pending, int T, float* out, float* mean, float* lo,
+                    hc_stream_t stream);
 
 /* Static text for a status code. */
 const char* hc_status_str(int status);
