@@ -1,39 +1,58 @@
 // CUDA-core kernels of the hyper-connection read for sm_103a.
 //
-// The read (defined in include/hc_read.h) is two dependent weight streams:
-// W_down (K x N BF16) and W_up (N x K BF16), 13.1 MB per read at d = 2560,
-// K = 320.  At T <= 8 tokens it is bound by HBM bandwidth, so both kernels are
-// built around one idea: every CTA issues bulk async copies (TMA engine) of its
-// whole weight tile into shared memory at entry, before it waits for the
-// previous kernel (programmatic dependent launch), so the weights of this
-// kernel and of the kernels queued behind it stream continuously.
+// The read (defined in include/hc_read.h) streams two BF16 weight matrices,
+// W_down (K x N) and W_up (N x K): 13.1 MB per read at d = 2560, K = 320.
+// On GB300 that is under 2 us of HBM time, so what limits a stream of reads is
+// the chain of dependent latencies per read, not bandwidth.  The kernels are
+// shaped to keep that chain short:
+//
+//  * every CTA issues bulk async copies (TMA engine) of its whole weight tile
+//    into shared memory at entry, before it waits for the previous kernel
+//    (programmatic dependent launch).  Weight prefetch is the only work done
+//    before that wait, so nothing can race.  The down kernel lets the up
+//    kernel launch at once (the up kernel's W_up streams while the down
+//    kernel runs); the up kernel lets the next read launch once its own wait
+//    has returned, which keeps waiting CTAs of later reads off the SMs while
+//    this read computes;
+//  * the down kernel's cross-CTA reduction stays on chip: the four CTAs that
+//    cover one stream's four column slabs form a thread-block cluster; each
+//    pushes its partial sums and sums of squares into the leader CTA's shared
+//    memory (distributed shared memory), one cluster barrier later the leader
+//    applies rs and writes the stream's partial; no global atomics, no last
+//    arriver;
+//  * after its dependency wait, each kernel issues all of its global loads
+//    (R and P, or the partials and R and P) before using any of them.
 //
 // Kernel 1, hc_down_kernel (design ancestor: gr_fused_down_kernel in "#2812
 // sycl: STRATA_GR_FUSED=1, the two-kernel BF16 hyper-connection read
 // (opt-in)", section "What changed"): a CTA owns 32 rows of W_down x one slab
-// of d/4 columns (a quarter of a stream).  It commits the pending write for
-// its slab, stages x = R' * w_norm unscaled in shared memory with the slab's
-// sums of squares, and forms 32 partial dot products per token over the slab.
-// The last CTA of a row group to arrive (atomic ticket) combines the 16
-// slabs' partials in a fixed order, applies rs per stream, writes lo and
-// resets the ticket.
+// of d/4 columns.  It commits the pending write for its slab, stages
+// x = R' * w_norm unscaled with the slab's sums of squares and forms 32
+// partial dot products per token (lane = row, so the x reads are shared-memory
+// broadcasts).  The cluster of the stream's four slabs then sums the slabs in
+// a fixed order, applies rs and writes part[s][t][k] = rs[t][s] * (slab sum).
+// Partials live in one scratch slot per handle: a read's down kernel writes
+// it only after the previous read has completed.
 //
 // Kernel 2, hc_up_kernel (design ancestor: gr_fused_up_kernel, same section):
 // a CTA owns 16 columns x 4 streams = 64 rows of W_up, so the stream mean of
-// its columns stays inside the CTA.  Four quarters of K are summed in a fixed
-// order, then the epilogue writes out = R' + sigmoid(g) * u and the mean.
+// its columns stays inside the CTA.  lo[t][k] = sum over the 4 streams of
+// part (fixed order); four quarters of K are summed in a fixed order; the
+// epilogue writes out = R' + sigmoid(g) * u and the mean.
 //
-// Both kernels process tokens in groups of TT (TT = T for T <= 8) with the
-// weight tile held in shared memory across groups.  Every reduction has a
-// fixed order, so results do not depend on scheduling: direct calls and graph
-// replays give the same bits.
+// Every reduction has a fixed order, so results do not depend on scheduling:
+// direct calls and graph replays give the same bits.
 #pragma once
+
+#include <cooperative_groups.h>
 
 #include <cstdint>
 
 #include "hc_ptx.cuh"
 
 namespace hc {
+
+namespace cg = cooperative_groups;
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
@@ -43,7 +62,7 @@ constexpr int kMaxT = 64;
 // microseconds) and records an error bit instead of hanging.
 constexpr uint64_t kWaitNs = 1000000000ull;
 
-// Error bits of the handle's device error word.
+// Error bits of the device error word.
 constexpr unsigned kErrDownNorm = 1u;
 constexpr unsigned kErrDownWeights = 2u;
 constexpr unsigned kErrUpGate = 4u;
@@ -52,15 +71,17 @@ constexpr unsigned kErrUpWeights = 8u;
 template <int D, int KD>
 struct Geo {
   static constexpr int N = kStreams * D;
-  // ---- down kernel: 32 rows x SLAB columns per CTA
+  // ---- down kernel: 32 rows x SLAB columns per CTA, 4 slabs per stream
   static constexpr int SLAB = D / 4;
   static constexpr int SLABS = N / SLAB;             // 16
-  static constexpr int SLABS_PER_STREAM = D / SLAB;  // 4
+  static constexpr int SLABS_PER_STREAM = D / SLAB;  // 4 = cluster size
   static constexpr int DN_ROWS = 32;
   static constexpr int ROW_GROUPS = KD / DN_ROWS;
   static constexpr int DN_PITCH = SLAB * 2 + 16;     // bytes; = 16 (mod 128): conflict-free rows
   static constexpr int DN_CPW = SLAB / kWarps;       // columns per warp
   static constexpr int DN_CHUNKS = DN_CPW / 8;       // 16-byte chunks per warp row
+  static constexpr int DN_F4 = SLAB / 4;             // float4 per token of a slab
+  static constexpr int DN_F4_PER_THREAD = (DN_F4 + kThreads - 1) / kThreads;
   // ---- up kernel: 16 columns x 4 streams = 64 rows per CTA
   static constexpr int UP_COLS = 16;
   static constexpr int UP_ROWS = UP_COLS * kStreams;
@@ -68,11 +89,14 @@ struct Geo {
   static constexpr int UP_PITCH = KD * 2 + 16;       // bytes; = 16 (mod 128)
   static constexpr int UP_KQ = KD / 4;               // K per quarter
   static constexpr int UP_CHUNKS = UP_KQ / 8;
+  static constexpr int LO_PER_CTA = KD / UP_CTAS;    // lo entries each up CTA writes
 
   static_assert(SLAB % (8 * kWarps) == 0, "slab must split into 16-byte chunks per warp");
-  static_assert(KD % DN_ROWS == 0 && KD % 32 == 0, "K must be a multiple of 32");
+  static_assert(SLABS_PER_STREAM == 4, "cluster of four slabs per stream");
+  static_assert(KD % DN_ROWS == 0, "K must be a multiple of 32");
   static_assert(DN_PITCH % 128 == 16 && UP_PITCH % 128 == 16, "pitch must be 16 mod 128");
   static_assert(D % UP_COLS == 0, "d must be a multiple of 16");
+  static_assert(KD % UP_CTAS == 0, "lo must split evenly over the up CTAs");
 };
 
 template <int D, int KD, int TT>
@@ -85,8 +109,12 @@ struct DownSmem {
   static constexpr int X = WN + G::SLAB * 4;
   static constexpr int RED = X + TT * G::SLAB * 4;
   static constexpr int SSW = RED + kWarps * TT * 32 * 4;
-  static constexpr int RS = SSW + kWarps * TT * 4;
-  static constexpr int BYTES = RS + kMaxT * kStreams * 4;
+  static constexpr int RS = SSW + kWarps * TT * 4;       // [kMaxT] rs (cluster leader)
+  // Pushed by the cluster's four CTAs into the leader: [4][T] sums of squares,
+  // then [4][T][32] partials.  Sized by the launch's T.
+  static constexpr int RECV = RS + kMaxT * 4;
+  static constexpr int bytes(int T) { return RECV + 4 * T * 4 + 4 * T * 32 * 4; }
+  static constexpr int BYTES_MAX = RECV + 4 * kMaxT * 4 + 4 * kMaxT * 32 * 4;
 };
 
 template <int D, int KD, int TT>
@@ -100,7 +128,10 @@ struct UpSmem {
   static constexpr int LO = SIG + G::UP_ROWS * 4;
   static constexpr int RED = LO + TT * KD * 4;
   static constexpr int OUT = RED + 4 * TT * G::UP_ROWS * 4;
-  static constexpr int BYTES = OUT + TT * G::UP_ROWS * 4;
+  static constexpr int RP = OUT + TT * G::UP_ROWS * 4;    // [TT][64] committed residual
+  static constexpr int BYTES = RP + TT * G::UP_ROWS * 4;
+  static constexpr int bytes(int) { return BYTES; }
+  static constexpr int BYTES_MAX = BYTES;
 };
 
 struct DownArgs {
@@ -108,11 +139,8 @@ struct DownArgs {
   const float* P;          // [T][N] or null
   const float* w_norm;     // [N]
   const uint16_t* W_down;  // [K][N] BF16
-  float* part;             // scratch [SLABS][T_max][K]
-  float* ss_part;          // scratch [ROW_GROUPS][SLABS][T_max]
-  unsigned* counters;      // scratch [ROW_GROUPS], zero between reads
+  float* part;             // scratch [4][T_max][K]: rs-scaled per-stream partials
   unsigned* err;           // scratch error word
-  float* lo;               // [T][K]
   float* rs_out;           // [T][4] or null
   int T;
   int T_max;
@@ -124,12 +152,14 @@ struct UpArgs {
   const float* P;        // [T][N] or null
   const float* gate;     // [N]
   const uint16_t* W_up;  // [N][K] BF16
-  const float* lo;       // [T][K]
+  const float* part;     // scratch [4][T_max][K]
   float* out;            // [T][N]
   float* mean;           // [T][d]
+  float* lo;             // [T][K]
   float* r_out;          // [T][N] or null
   unsigned* err;
   int T;
+  int T_max;
 };
 
 // Eight BF16 values (one 16-byte chunk) widened to fp32: a BF16 is the upper
@@ -145,46 +175,35 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float (&w)[8]) {
   w[7] = __uint_as_float(v.w & 0xffff0000u);
 }
 
-// Thread 0 waits (bounded) for the barrier's phase `parity`; the outcome is
-// shared through `flag`.  On success every thread then observes the completed
-// phase itself (which returns at once), so the bulk-copied data is visible to
-// all.  Returns false after recording `code` in *err on a timeout.
-__device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, unsigned* err,
-                                         unsigned code, volatile int* flag) {
-  if (threadIdx.x == 0) {
-    const uint64_t t0 = ptx::globaltimer_ns();
-    bool ok = true;
-    while (!ptx::mbar_try_wait(bar, parity)) {
-      if (ptx::globaltimer_ns() - t0 > kWaitNs) {
-        ok = false;
-        break;
-      }
-    }
-    if (!ok) atomicOr(err, code);
-    *flag = ok ? 1 : 0;
-  }
-  __syncthreads();
-  const bool ok = *flag != 0;
-  if (ok) {
-    for (uint32_t i = 0; !ptx::mbar_try_wait(bar, parity) && i < (1u << 20); ++i) {
+// Every thread waits for the barrier's phase `parity` itself (observing the
+// completed phase makes the bulk-copied bytes visible to that thread).  The
+// wait is bounded: after kWaitNs the thread records `code` in *err and
+// returns false; the kernel then carries on with whatever is in shared
+// memory (its results are void and the error word says so) and drains the
+// copies before it exits, so no CTA leaves with copies still in flight.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, unsigned* err,
+                                         unsigned code) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (ptx::globaltimer_ns() - t0 > kWaitNs) {
+      atomicOr(err, code);
+      return false;
     }
   }
-  __syncthreads();
-  return ok;
+  return true;
 }
 
-// After a timeout: wait (bounded again) for copies still in flight into this
-// CTA's shared memory before the CTA exits.
+// Before a CTA whose wait timed out exits: wait (bounded again) for copies
+// still in flight into its shared memory.
 __device__ __forceinline__ void drain(uint64_t* bar, uint32_t parity) {
-  if (threadIdx.x == 0) {
-    const uint64_t t0 = ptx::globaltimer_ns();
-    while (!ptx::mbar_try_wait(bar, parity) && ptx::globaltimer_ns() - t0 < kWaitNs) {
-    }
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, parity) && ptx::globaltimer_ns() - t0 < kWaitNs) {
   }
-  __syncthreads();
 }
 
 // ------------------------------------------------------------------ kernel 1
+// Grid (16 slabs, K/32 row groups), clusters of 4 along x (one stream).
 template <int D, int KD, int TT>
 __global__ void __launch_bounds__(kThreads, 2) hc_down_kernel(const DownArgs a) {
   using G = Geo<D, KD>;
@@ -192,7 +211,6 @@ __global__ void __launch_bounds__(kThreads, 2) hc_down_kernel(const DownArgs a) 
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* bar_w = reinterpret_cast<uint64_t*>(smem + S::BAR);
   uint64_t* bar_n = bar_w + 1;
-  volatile int* flag = reinterpret_cast<volatile int*>(smem + S::FLAG);
   unsigned char* w_s = smem + S::W;
   const float* wn_s = reinterpret_cast<const float*>(smem + S::WN);
   float* x_s = reinterpret_cast<float*>(smem + S::X);
@@ -201,57 +219,82 @@ __global__ void __launch_bounds__(kThreads, 2) hc_down_kernel(const DownArgs a) 
   float* rs_s = reinterpret_cast<float*>(smem + S::RS);
 
   const int slab = blockIdx.x;
+  const int stream = slab / G::SLABS_PER_STREAM;
   const int rg = blockIdx.y;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int col0 = slab * G::SLAB;
   const int row0 = rg * G::DN_ROWS;
+  const int T = a.T;
 
-  // Parameters first: they do not depend on the previous kernel.
+  cg::cluster_group cluster = cg::this_cluster();
+  const unsigned rank = cluster.block_rank();  // = slab within the stream
+  // The leader's receive area: [4][T] sums of squares, then [4][T][32] partials.
+  float* recv_ss = cluster.map_shared_rank(reinterpret_cast<float*>(smem + S::RECV), 0);
+  float* recv_p = recv_ss + 4 * T;
+
+  // Announce this CTA to its cluster; the matching wait below guarantees that
+  // every CTA of the cluster runs before anyone writes the leader's memory.
+  ptx::cluster_arrive_relaxed();
+
+  // Weights first (w_norm, needed earliest, before the W_down rows); they do
+  // not depend on the previous kernel.  Then let the next kernel launch.
   if (warp == 0) {
     if (lane == 0) {
       ptx::mbar_init(bar_w, 1);
       ptx::mbar_init(bar_n, 1);
       ptx::fence_barrier_init();
-      ptx::mbar_arrive_expect_tx(bar_w, G::DN_ROWS * G::SLAB * 2);
       ptx::mbar_arrive_expect_tx(bar_n, G::SLAB * 4);
+      ptx::mbar_arrive_expect_tx(bar_w, G::DN_ROWS * G::SLAB * 2);
+      // w_norm's slab is read by every row group: keep it in L2.
+      ptx::bulk_g2s(smem + S::WN, a.w_norm + col0, G::SLAB * 4, bar_n, ptx::policy_evict_last());
     }
     __syncwarp();
     const uint64_t once = ptx::policy_evict_first();  // each weight byte is read once
     ptx::bulk_g2s(w_s + lane * G::DN_PITCH, a.W_down + (size_t)(row0 + lane) * G::N + col0,
                   G::SLAB * 2, bar_w, once);
-    if (lane == 0) {
-      // w_norm's slab is read by every row group: keep it in L2.
-      ptx::bulk_g2s(smem + S::WN, a.w_norm + col0, G::SLAB * 4, bar_n, ptx::policy_evict_last());
-    }
   }
   ptx::launch_dependents();
-  ptx::wait_prerequisites();
-  __syncthreads();
+  ptx::wait_prerequisites();  // R, P and the scratch belong to the previous kernel until now
+  ptx::cluster_wait();
+  __syncthreads();  // the mbarriers are initialised before any thread waits on them
 
-  if (!cta_wait(bar_n, 0, a.err, kErrDownNorm, flag)) {
-    drain(bar_w, 0);
-    return;
-  }
-
-  const int T = a.T;
-  bool weights_ready = false;
+  // A timed-out wait leaves garbage in shared memory but the CTA still runs
+  // to the end: it must take part in the cluster barrier below.
+  bool ok = true;
   for (int t0 = 0; t0 < T; t0 += TT) {
     const int tg = min(TT, T - t0);
 
-    // Commit the pending write, stage x = R' * w_norm, sum R'^2 (this slab).
+    // Issue every R and P load of the group, then commit the pending write,
+    // stage x = R' * w_norm and sum R'^2 over this slab.
+    float4 rv[TT][G::DN_F4_PER_THREAD];
+    float4 pv[TT][G::DN_F4_PER_THREAD];
+#pragma unroll
+    for (int t = 0; t < TT; ++t) {
+#pragma unroll
+      for (int m = 0; m < G::DN_F4_PER_THREAD; ++m) {
+        const int c4 = tid + m * kThreads;
+        rv[t][m] = make_float4(0.f, 0.f, 0.f, 0.f);
+        pv[t][m] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (t < tg && c4 < G::DN_F4) {
+          const size_t base = (size_t)(t0 + t) * G::N + col0;
+          rv[t][m] = __ldcg(reinterpret_cast<const float4*>(a.R + base) + c4);
+          if (a.P) pv[t][m] = __ldcg(reinterpret_cast<const float4*>(a.P + base) + c4);
+        }
+      }
+    }
+    if (t0 == 0) ok = wait_bar(bar_n, 0, a.err, kErrDownNorm) && ok;
     float ssl[TT];
 #pragma unroll
     for (int t = 0; t < TT; ++t) {
       ssl[t] = 0.f;
-      if (t < tg) {
-        const size_t base = (size_t)(t0 + t) * G::N + col0;
-        const float4* Rt = reinterpret_cast<const float4*>(a.R + base);
-        const float4* Pt = a.P ? reinterpret_cast<const float4*>(a.P + base) : nullptr;
-        for (int c4 = tid; c4 < G::SLAB / 4; c4 += kThreads) {
-          float4 r = __ldcg(Rt + c4);
-          const float4 p = Pt ? __ldcg(Pt + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int m = 0; m < G::DN_F4_PER_THREAD; ++m) {
+        const int c4 = tid + m * kThreads;
+        if (t < tg && c4 < G::DN_F4) {
+          float4 r = rv[t][m];
+          const float4 p = pv[t][m];
           r.x = __fadd_rn(r.x, p.x);
           r.y = __fadd_rn(r.y, p.y);
           r.z = __fadd_rn(r.z, p.z);
@@ -274,25 +317,23 @@ __global__ void __launch_bounds__(kThreads, 2) hc_down_kernel(const DownArgs a) 
       for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
       if (lane == 0) ssw_s[warp * TT + t] = v;
     }
-    if (!weights_ready) {
-      if (!cta_wait(bar_w, 0, a.err, kErrDownWeights, flag)) return;
-      weights_ready = true;
-    } else {
-      __syncthreads();
-    }
+    if (t0 == 0) ok = wait_bar(bar_w, 0, a.err, kErrDownWeights) && ok;
+    __syncthreads();  // x and the per-warp sums of squares are complete
     if (tid < tg) {
-      float s = 0.f;
+      float v = 0.f;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) s += ssw_s[w * TT + tid];
-      __stcg(a.ss_part + (size_t)(rg * G::SLABS + slab) * a.T_max + t0 + tid, s);
+      for (int w = 0; w < kWarps; ++w) v += ssw_s[w * TT + tid];
+      recv_ss[rank * T + t0 + tid] = v;  // into the leader's shared memory
     }
 
     // Partial dot products: lane = row, warp = column range of the slab.
+    // Two accumulation chains per token (elements 0-3 and 4-7 of each chunk),
+    // added at the end: a fixed order with half the dependent-FMA latency.
     const unsigned char* wrow = w_s + lane * G::DN_PITCH + warp * G::DN_CPW * 2;
     const float* xw = x_s + warp * G::DN_CPW;
-    float acc[TT];
+    float acc0[TT], acc1[TT];
 #pragma unroll
-    for (int t = 0; t < TT; ++t) acc[t] = 0.f;
+    for (int t = 0; t < TT; ++t) acc0[t] = acc1[t] = 0.f;
 #pragma unroll 2
     for (int j = 0; j < G::DN_CHUNKS; ++j) {
       float w[8];
@@ -301,69 +342,59 @@ __global__ void __launch_bounds__(kThreads, 2) hc_down_kernel(const DownArgs a) 
       for (int t = 0; t < TT; ++t) {
         const float4 xa = *reinterpret_cast<const float4*>(xw + t * G::SLAB + j * 8);
         const float4 xb = *reinterpret_cast<const float4*>(xw + t * G::SLAB + j * 8 + 4);
-        float s = acc[t];
-        s = __fmaf_rn(w[0], xa.x, s);
-        s = __fmaf_rn(w[1], xa.y, s);
-        s = __fmaf_rn(w[2], xa.z, s);
-        s = __fmaf_rn(w[3], xa.w, s);
-        s = __fmaf_rn(w[4], xb.x, s);
-        s = __fmaf_rn(w[5], xb.y, s);
-        s = __fmaf_rn(w[6], xb.z, s);
-        s = __fmaf_rn(w[7], xb.w, s);
-        acc[t] = s;
+        float v0 = acc0[t], v1 = acc1[t];
+        v0 = __fmaf_rn(w[0], xa.x, v0);
+        v1 = __fmaf_rn(w[4], xb.x, v1);
+        v0 = __fmaf_rn(w[1], xa.y, v0);
+        v1 = __fmaf_rn(w[5], xb.y, v1);
+        v0 = __fmaf_rn(w[2], xa.z, v0);
+        v1 = __fmaf_rn(w[6], xb.z, v1);
+        v0 = __fmaf_rn(w[3], xa.w, v0);
+        v1 = __fmaf_rn(w[7], xb.w, v1);
+        acc0[t] = v0;
+        acc1[t] = v1;
       }
     }
 #pragma unroll
-    for (int t = 0; t < TT; ++t) red_s[(warp * TT + t) * 32 + lane] = acc[t];
+    for (int t = 0; t < TT; ++t) red_s[(warp * TT + t) * 32 + lane] = __fadd_rn(acc0[t], acc1[t]);
     __syncthreads();
     for (int idx = tid; idx < tg * 32; idx += kThreads) {
       const int t = idx >> 5, r = idx & 31;
-      float s = 0.f;
+      float v = 0.f;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) s += red_s[(w * TT + t) * 32 + r];
-      __stcg(a.part + ((size_t)slab * a.T_max + t0 + t) * KD + row0 + r, s);
+      for (int w = 0; w < kWarps; ++w) v += red_s[(w * TT + t) * 32 + r];
+      recv_p[(rank * T + t0 + t) * 32 + r] = v;  // into the leader's shared memory
     }
     __syncthreads();
   }
 
-  // Arrival: the last CTA of this row group combines the slabs.
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const unsigned ticket = atomicAdd(a.counters + rg, 1u);
-    *flag = (ticket == (unsigned)(G::SLABS - 1)) ? 1 : 0;
+  if (!ok) {
+    drain(bar_n, 0);
+    drain(bar_w, 0);
   }
-  __syncthreads();
-  if (*flag == 0) return;
-  __threadfence();
+  // One cluster barrier: every slab's pushes are visible to the leader.
+  ptx::cluster_arrive_release();
+  ptx::cluster_wait();
+  if (rank != 0) return;
 
-  for (int idx = tid; idx < T * kStreams; idx += kThreads) {
-    const int t = idx >> 2, s = idx & 3;
+  // Leader: sum the four slabs in slab order, apply rs, write the partial.
+  for (int t = tid; t < T; t += kThreads) {
     float ss = 0.f;
 #pragma unroll
-    for (int q = 0; q < G::SLABS_PER_STREAM; ++q) {
-      ss += __ldcg(a.ss_part + (size_t)(rg * G::SLABS + s * G::SLABS_PER_STREAM + q) * a.T_max + t);
-    }
+    for (int q = 0; q < G::SLABS_PER_STREAM; ++q) ss += recv_ss[q * T + t];
     const float rs = 1.0f / sqrtf(ss / (float)D + a.eps);
-    rs_s[idx] = rs;
-    if (a.rs_out != nullptr && rg == 0) a.rs_out[idx] = rs;
+    rs_s[t] = rs;
+    if (rg == 0 && a.rs_out != nullptr) a.rs_out[t * kStreams + stream] = rs;
   }
   __syncthreads();
+  float* part = a.part + (size_t)stream * a.T_max * KD;
   for (int idx = tid; idx < T * G::DN_ROWS; idx += kThreads) {
     const int t = idx >> 5, r = idx & 31;
-    float l = 0.f;
+    float p = 0.f;
 #pragma unroll
-    for (int s = 0; s < kStreams; ++s) {
-      float ps = 0.f;
-#pragma unroll
-      for (int q = 0; q < G::SLABS_PER_STREAM; ++q) {
-        ps += __ldcg(a.part + ((size_t)(s * G::SLABS_PER_STREAM + q) * a.T_max + t) * KD + row0 + r);
-      }
-      l = __fmaf_rn(rs_s[t * kStreams + s], ps, l);
-    }
-    a.lo[(size_t)t * KD + row0 + r] = l;
+    for (int q = 0; q < G::SLABS_PER_STREAM; ++q) p += recv_p[(q * T + t) * 32 + r];
+    __stcg(part + (size_t)t * KD + row0 + r, __fmul_rn(rs_s[t], p));
   }
-  if (tid == 0) atomicExch(a.counters + rg, 0u);
 }
 
 // ------------------------------------------------------------------ kernel 2
@@ -371,16 +402,18 @@ template <int D, int KD, int TT>
 __global__ void __launch_bounds__(kThreads, 2) hc_up_kernel(const UpArgs a) {
   using G = Geo<D, KD>;
   using S = UpSmem<D, KD, TT>;
+  constexpr int EPI = (TT * G::UP_ROWS + kThreads - 1) / kThreads;  // epilogue items per thread
+  constexpr int LO4 = (TT * KD / 4 + kThreads - 1) / kThreads;       // lo float4 per thread
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* bar_w = reinterpret_cast<uint64_t*>(smem + S::BAR);
   uint64_t* bar_g = bar_w + 1;
-  volatile int* flag = reinterpret_cast<volatile int*>(smem + S::FLAG);
   unsigned char* w_s = smem + S::W;
   const float* g_s = reinterpret_cast<const float*>(smem + S::GATE);
   float* sig_s = reinterpret_cast<float*>(smem + S::SIG);
   float* lo_s = reinterpret_cast<float*>(smem + S::LO);
   float* red_s = reinterpret_cast<float*>(smem + S::RED);
   float* out_s = reinterpret_cast<float*>(smem + S::OUT);
+  float* rp_s = reinterpret_cast<float*>(smem + S::RP);
 
   const int c0 = blockIdx.x * G::UP_COLS;
   const int tid = threadIdx.x;
@@ -397,39 +430,83 @@ __global__ void __launch_bounds__(kThreads, 2) hc_up_kernel(const UpArgs a) {
     }
     __syncwarp();
     const uint64_t once = ptx::policy_evict_first();
+    if (lane < kStreams) {
+      ptx::bulk_g2s(smem + S::GATE + lane * G::UP_COLS * 4, a.gate + lane * D + c0,
+                    G::UP_COLS * 4, bar_g, once);
+    }
     // Local row r = s * 16 + j holds global row s * d + c0 + j.
     for (int r = lane; r < G::UP_ROWS; r += 32) {
       const int grow = (r / G::UP_COLS) * D + c0 + (r % G::UP_COLS);
       ptx::bulk_g2s(w_s + r * G::UP_PITCH, a.W_up + (size_t)grow * KD, KD * 2, bar_w, once);
     }
-    if (lane < kStreams) {
-      ptx::bulk_g2s(smem + S::GATE + lane * G::UP_COLS * 4, a.gate + lane * D + c0,
-                    G::UP_COLS * 4, bar_g, once);
-    }
   }
+  ptx::wait_prerequisites();  // the partials, R and P are ready from here on
+  // Only now may the next read's kernels launch: launching them earlier lets
+  // a cascade of waiting CTAs crowd the SMs that are computing this read.
   ptx::launch_dependents();
-  ptx::wait_prerequisites();
-  __syncthreads();
+  __syncthreads();  // the mbarriers are initialised before any thread waits on them
 
-  if (!cta_wait(bar_g, 0, a.err, kErrUpGate, flag)) {
-    drain(bar_w, 0);
-    return;
+  bool ok = true;
+  if (tid < G::UP_ROWS) {
+    ok = wait_bar(bar_g, 0, a.err, kErrUpGate);
+    sig_s[tid] = 1.0f / (1.0f + expf(-g_s[tid]));
   }
-  if (tid < G::UP_ROWS) sig_s[tid] = 1.0f / (1.0f + expf(-g_s[tid]));
 
   const int T = a.T;
-  bool weights_ready = false;
   for (int t0 = 0; t0 < T; t0 += TT) {
     const int tg = min(TT, T - t0);
-    const float4* lo_g = reinterpret_cast<const float4*>(a.lo + (size_t)t0 * KD);
-    for (int idx = tid; idx < tg * KD / 4; idx += kThreads) {
-      reinterpret_cast<float4*>(lo_s)[idx] = __ldcg(lo_g + idx);
+    // Issue every global load of the group before using any: the four
+    // per-stream partials of lo, and R and P of this CTA's rows.
+    float4 pv[LO4][kStreams];
+#pragma unroll
+    for (int m = 0; m < LO4; ++m) {
+      const int idx = tid + m * kThreads;
+#pragma unroll
+      for (int s = 0; s < kStreams; ++s) {
+        pv[m][s] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (idx < tg * KD / 4) {
+          pv[m][s] = __ldcg(reinterpret_cast<const float4*>(
+                                a.part + ((size_t)s * a.T_max + t0) * KD) + idx);
+        }
+      }
     }
-    if (!weights_ready) {
-      if (!cta_wait(bar_w, 0, a.err, kErrUpWeights, flag)) return;
-      weights_ready = true;
-    } else {
-      __syncthreads();
+    float rr[EPI], pp[EPI];
+#pragma unroll
+    for (int m = 0; m < EPI; ++m) {
+      const int idx = tid + m * kThreads;
+      const int t = idx / G::UP_ROWS, r = idx % G::UP_ROWS;
+      rr[m] = 0.f;
+      pp[m] = 0.f;
+      if (t < tg) {
+        const size_t off = (size_t)(t0 + t) * G::N + (r / G::UP_COLS) * D + c0 + (r % G::UP_COLS);
+        rr[m] = __ldcg(a.R + off);
+        if (a.P) pp[m] = __ldcg(a.P + off);
+      }
+    }
+    // lo: the four per-stream partials summed in stream order.
+#pragma unroll
+    for (int m = 0; m < LO4; ++m) {
+      const int idx = tid + m * kThreads;
+      if (idx < tg * KD / 4) {
+        float4 l;
+        l.x = ((pv[m][0].x + pv[m][1].x) + pv[m][2].x) + pv[m][3].x;
+        l.y = ((pv[m][0].y + pv[m][1].y) + pv[m][2].y) + pv[m][3].y;
+        l.z = ((pv[m][0].z + pv[m][1].z) + pv[m][2].z) + pv[m][3].z;
+        l.w = ((pv[m][0].w + pv[m][1].w) + pv[m][2].w) + pv[m][3].w;
+        reinterpret_cast<float4*>(lo_s)[idx] = l;
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < EPI; ++m) {
+      const int idx = tid + m * kThreads;
+      if (idx < tg * G::UP_ROWS) rp_s[idx] = __fadd_rn(rr[m], pp[m]);
+    }
+    if (t0 == 0) ok = wait_bar(bar_w, 0, a.err, kErrUpWeights) && ok;
+    __syncthreads();  // lo, R' and the gates are in shared memory
+    // This CTA's share of the lo output.
+    for (int idx = tid; idx < tg * G::LO_PER_CTA; idx += kThreads) {
+      const int t = idx / G::LO_PER_CTA, k = blockIdx.x * G::LO_PER_CTA + idx % G::LO_PER_CTA;
+      a.lo[(size_t)(t0 + t) * KD + k] = lo_s[t * KD + k];
     }
 
     // u for 64 rows: lane = row within a half, warp = (half, K quarter).
@@ -438,9 +515,9 @@ __global__ void __launch_bounds__(kThreads, 2) hc_up_kernel(const UpArgs a) {
     const int row = half * 32 + lane;
     const unsigned char* wrow = w_s + row * G::UP_PITCH + kq * G::UP_KQ * 2;
     const float* lw = lo_s + kq * G::UP_KQ;
-    float acc[TT];
+    float acc0[TT], acc1[TT];
 #pragma unroll
-    for (int t = 0; t < TT; ++t) acc[t] = 0.f;
+    for (int t = 0; t < TT; ++t) acc0[t] = acc1[t] = 0.f;
 #pragma unroll 2
     for (int j = 0; j < G::UP_CHUNKS; ++j) {
       float w[8];
@@ -449,20 +526,23 @@ __global__ void __launch_bounds__(kThreads, 2) hc_up_kernel(const UpArgs a) {
       for (int t = 0; t < TT; ++t) {
         const float4 la = *reinterpret_cast<const float4*>(lw + t * KD + j * 8);
         const float4 lb = *reinterpret_cast<const float4*>(lw + t * KD + j * 8 + 4);
-        float s = acc[t];
-        s = __fmaf_rn(w[0], la.x, s);
-        s = __fmaf_rn(w[1], la.y, s);
-        s = __fmaf_rn(w[2], la.z, s);
-        s = __fmaf_rn(w[3], la.w, s);
-        s = __fmaf_rn(w[4], lb.x, s);
-        s = __fmaf_rn(w[5], lb.y, s);
-        s = __fmaf_rn(w[6], lb.z, s);
-        s = __fmaf_rn(w[7], lb.w, s);
-        acc[t] = s;
+        float v0 = acc0[t], v1 = acc1[t];
+        v0 = __fmaf_rn(w[0], la.x, v0);
+        v1 = __fmaf_rn(w[4], lb.x, v1);
+        v0 = __fmaf_rn(w[1], la.y, v0);
+        v1 = __fmaf_rn(w[5], lb.y, v1);
+        v0 = __fmaf_rn(w[2], la.z, v0);
+        v1 = __fmaf_rn(w[6], lb.z, v1);
+        v0 = __fmaf_rn(w[3], la.w, v0);
+        v1 = __fmaf_rn(w[7], lb.w, v1);
+        acc0[t] = v0;
+        acc1[t] = v1;
       }
     }
 #pragma unroll
-    for (int t = 0; t < TT; ++t) red_s[(kq * TT + t) * G::UP_ROWS + row] = acc[t];
+    for (int t = 0; t < TT; ++t) {
+      red_s[(kq * TT + t) * G::UP_ROWS + row] = __fadd_rn(acc0[t], acc1[t]);
+    }
     __syncthreads();
 
     // Epilogue: pending write, gate, stream mean.
@@ -473,11 +553,11 @@ __global__ void __launch_bounds__(kThreads, 2) hc_up_kernel(const UpArgs a) {
                       red_s[(3 * TT + t) * G::UP_ROWS + r];
       const int i = (r / G::UP_COLS) * D + c0 + (r % G::UP_COLS);
       const size_t off = (size_t)(t0 + t) * G::N + i;
-      const float rp = __fadd_rn(__ldcg(a.R + off), a.P ? __ldcg(a.P + off) : 0.0f);
+      const float rp = rp_s[idx];
       const float o = __fmaf_rn(sig_s[r], u, rp);
       a.out[off] = o;
       if (a.r_out != nullptr) a.r_out[off] = rp;
-      out_s[t * G::UP_ROWS + r] = o;
+      out_s[idx] = o;
     }
     __syncthreads();
     for (int idx = tid; idx < tg * G::UP_COLS; idx += kThreads) {
@@ -487,6 +567,10 @@ __global__ void __launch_bounds__(kThreads, 2) hc_up_kernel(const UpArgs a) {
       a.mean[(size_t)(t0 + t) * D + c0 + j] = m;
     }
     __syncthreads();
+  }
+  if (!ok) {
+    drain(bar_g, 0);
+    drain(bar_w, 0);
   }
 }
 

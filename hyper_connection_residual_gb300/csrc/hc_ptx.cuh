@@ -84,5 +84,18 @@ __device__ __forceinline__ void wait_prerequisites() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Cluster barrier halves (all threads of every CTA in the cluster execute
+// both).  arrive.relaxed orders nothing; wait.acquire after arrive.release
+// publishes shared-memory writes made before the arrive to the whole cluster.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 }  // namespace ptx
 }  // namespace hc

@@ -18,11 +18,8 @@ struct hc_read_s {
   float eps;
   void* scratch;
   size_t scratch_bytes;
-  float* part;
-  float* ss_part;
-  unsigned* counters;
+  float* part;     // [4][T_max][K] rs-scaled per-stream partials
   unsigned* err;
-  int row_groups;
 };
 
 namespace {
@@ -34,7 +31,10 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-cudaLaunchConfig_t pdl_config(dim3 grid, size_t smem, cudaStream_t st, cudaLaunchAttribute* attr) {
+// Launch configuration with programmatic dependent launch and, when
+// cluster_x > 1, thread-block clusters of cluster_x CTAs along x.
+cudaLaunchConfig_t pdl_config(dim3 grid, size_t smem, cudaStream_t st, cudaLaunchAttribute* attr,
+                              unsigned cluster_x) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(hc::kThreads);
@@ -44,6 +44,13 @@ cudaLaunchConfig_t pdl_config(dim3 grid, size_t smem, cudaStream_t st, cudaLaunc
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (cluster_x > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster_x;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
   return cfg;
 }
 
@@ -51,11 +58,11 @@ template <int D, int KD, int TT>
 cudaError_t configure_one() {
   cudaError_t e = cudaFuncSetAttribute(hc::hc_down_kernel<D, KD, TT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       hc::DownSmem<D, KD, TT>::BYTES);
+                                       hc::DownSmem<D, KD, TT>::BYTES_MAX);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(hc::hc_up_kernel<D, KD, TT>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              hc::UpSmem<D, KD, TT>::BYTES);
+                              hc::UpSmem<D, KD, TT>::BYTES_MAX);
 }
 
 template <int D, int KD>
@@ -74,13 +81,15 @@ cudaError_t configure_geometry() {
 template <int D, int KD, int TT>
 cudaError_t launch_pair(const DownArgs& da, const UpArgs& ua, cudaStream_t st) {
   using G = hc::Geo<D, KD>;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t c1 = pdl_config(dim3(G::SLABS, G::ROW_GROUPS),
-                                      hc::DownSmem<D, KD, TT>::BYTES, st, attr);
+                                      hc::DownSmem<D, KD, TT>::bytes(da.T), st, attr,
+                                      G::SLABS_PER_STREAM);
   cudaError_t e = cudaLaunchKernelEx(&c1, hc::hc_down_kernel<D, KD, TT>, da);
   if (e != cudaSuccess) return e;
-  cudaLaunchAttribute attr2[1];
-  cudaLaunchConfig_t c2 = pdl_config(dim3(G::UP_CTAS), hc::UpSmem<D, KD, TT>::BYTES, st, attr2);
+  cudaLaunchAttribute attr2[2];
+  cudaLaunchConfig_t c2 = pdl_config(dim3(G::UP_CTAS), hc::UpSmem<D, KD, TT>::bytes(ua.T), st,
+                                      attr2, 1);
   return cudaLaunchKernelEx(&c2, hc::hc_up_kernel<D, KD, TT>, ua);
 }
 
@@ -122,27 +131,20 @@ HC_EXPORT int hc_read_create(hc_read_t* out, int n, int d, int K, int T_max, flo
       cudaSetDevice(prev);
       return HC_ERR_ARG;
     }
-    const int N = n * d;
-    const int slabs = N / (d / 4);
     h->n = n;
     h->d = d;
     h->K = K;
     h->T_max = T_max;
     h->device = device;
     h->eps = eps;
-    h->row_groups = K / 32;
-    const size_t part_b = round_up((size_t)slabs * T_max * K * sizeof(float), 256);
-    const size_t ss_b = round_up((size_t)h->row_groups * slabs * T_max * sizeof(float), 256);
-    const size_t cnt_b = round_up((size_t)h->row_groups * sizeof(unsigned), 256);
+    const size_t part_b = round_up((size_t)n * T_max * K * sizeof(float), 256);
     const size_t err_b = 256;
-    h->scratch_bytes = part_b + ss_b + cnt_b + err_b;
+    h->scratch_bytes = part_b + err_b;
     e = cudaMalloc(&h->scratch, h->scratch_bytes);
     if (e == cudaSuccess) {
       char* base = static_cast<char*>(h->scratch);
       h->part = reinterpret_cast<float*>(base);
-      h->ss_part = reinterpret_cast<float*>(base + part_b);
-      h->counters = reinterpret_cast<unsigned*>(base + part_b + ss_b);
-      h->err = reinterpret_cast<unsigned*>(base + part_b + ss_b + cnt_b);
+      h->err = reinterpret_cast<unsigned*>(base + part_b);
       e = cudaMemset(h->scratch, 0, h->scratch_bytes);
       if (e == cudaSuccess) e = cudaDeviceSynchronize();
     } else {
@@ -176,16 +178,15 @@ HC_EXPORT int hc_read_ex(hc_read_t h, const float* R, const float* w_norm, const
   if (cudaGetDevice(&cur) != cudaSuccess) return HC_ERR_CUDA;
   if (cur != h->device) return HC_ERR_ARG;
 
+  float* part = h->part;
+
   DownArgs da;
   da.R = R;
   da.P = pending;
   da.w_norm = w_norm;
   da.W_down = W_down;
-  da.part = h->part;
-  da.ss_part = h->ss_part;
-  da.counters = h->counters;
+  da.part = part;
   da.err = h->err;
-  da.lo = lo;
   da.rs_out = rs;
   da.T = T;
   da.T_max = h->T_max;
@@ -196,12 +197,14 @@ HC_EXPORT int hc_read_ex(hc_read_t h, const float* R, const float* w_norm, const
   ua.P = pending;
   ua.gate = gate;
   ua.W_up = W_up;
-  ua.lo = lo;
+  ua.part = part;
   ua.out = out;
   ua.mean = mean;
+  ua.lo = lo;
   ua.r_out = r_out;
   ua.err = h->err;
   ua.T = T;
+  ua.T_max = h->T_max;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = (h->d == 2560) ? launch_geometry<2560, 320>(T, da, ua, st)
@@ -239,9 +242,7 @@ HC_EXPORT int hc_read_reset(hc_read_t h, hc_stream_t stream) {
   if (cudaGetDevice(&cur) != cudaSuccess) return HC_ERR_CUDA;
   if (cur != h->device) return HC_ERR_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const size_t cnt_b = (size_t)h->row_groups * sizeof(unsigned);
-  cudaError_t e = cudaMemsetAsync(h->counters, 0, cnt_b, st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(h->err, 0, sizeof(unsigned), st);
+  cudaError_t e = cudaMemsetAsync(h->err, 0, sizeof(unsigned), st);
   return e == cudaSuccess ? HC_OK : HC_ERR_CUDA;
 }
 
@@ -305,17 +306,16 @@ HC_EXPORT void hc_graph_destroy(hc_graph_t exec) {
 
 // ---------------------------------------------------------------------------
 // No-allocation entry point.  Its scratch is one file-scope device array
-// (partials, per-slab sums of squares, arrival counters, error word), sized
-// for the largest supported geometry (d = 4096, K = 512: 16 row groups) at
-// T <= HC_NOALLOC_MAX_T.  Host code must not hand the array's name to a
-// kernel (on the host it only stands for the symbol); the device address is
-// looked up once per device with cudaGetSymbolAddress.
+// (one slot of rs-scaled per-stream partials and the error word), sized for
+// the largest supported geometry (K = 512) at T <= HC_NOALLOC_MAX_T.  Host
+// code must not hand the array's name to a kernel (on the host it only stands
+// for the symbol); the device address is looked up once per device with
+// cudaGetSymbolAddress.
 namespace {
 
-constexpr size_t kNoallocPartBytes = (size_t)16 * HC_NOALLOC_MAX_T * 512 * sizeof(float);
-constexpr size_t kNoallocSsBytes = (size_t)16 * 16 * HC_NOALLOC_MAX_T * sizeof(float);
-constexpr size_t kNoallocTailBytes = 256;  // 16 counters + the error word
-static_assert(kNoallocPartBytes + kNoallocSsBytes + kNoallocTailBytes == HC_NOALLOC_SCRATCH_BYTES,
+constexpr size_t kNoallocPartBytes = (size_t)4 * HC_NOALLOC_MAX_T * 512 * sizeof(float);
+constexpr size_t kNoallocTailBytes = 256;  // the error word
+static_assert(kNoallocPartBytes + kNoallocTailBytes == HC_NOALLOC_SCRATCH_BYTES,
               "scratch size in the header and here disagree");
 
 constexpr int kMaxDevices = 64;
@@ -364,23 +364,19 @@ HC_EXPORT int hc_read_noalloc(int n, int d, int K, float eps, const float* R, co
 
   char* b = static_cast<char*>(base);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  unsigned* counters = reinterpret_cast<unsigned*>(b + kNoallocPartBytes + kNoallocSsBytes);
-  // The arrival counters and the error word must start at zero.
-  if (cudaMemsetAsync(counters, 0, kNoallocTailBytes, st) != cudaSuccess) {
+  unsigned* err = reinterpret_cast<unsigned*>(b + kNoallocPartBytes);
+  // The error word must start at zero.
+  if (cudaMemsetAsync(err, 0, kNoallocTailBytes, st) != cudaSuccess) {
     cudaGetLastError();
     return HC_ERR_CUDA;
   }
-
   DownArgs da;
   da.R = R;
   da.P = pending;
   da.w_norm = w_norm;
   da.W_down = W_down;
   da.part = reinterpret_cast<float*>(b);
-  da.ss_part = reinterpret_cast<float*>(b + kNoallocPartBytes);
-  da.counters = counters;
-  da.err = counters + 16;
-  da.lo = lo;
+  da.err = err;
   da.rs_out = nullptr;
   da.T = T;
   da.T_max = HC_NOALLOC_MAX_T;
@@ -391,12 +387,14 @@ HC_EXPORT int hc_read_noalloc(int n, int d, int K, float eps, const float* R, co
   ua.P = pending;
   ua.gate = gate;
   ua.W_up = W_up;
-  ua.lo = lo;
+  ua.part = reinterpret_cast<float*>(b);
   ua.out = out;
   ua.mean = mean;
+  ua.lo = lo;
   ua.r_out = nullptr;
-  ua.err = counters + 16;
+  ua.err = err;
   ua.T = T;
+  ua.T_max = HC_NOALLOC_MAX_T;
 
   cudaError_t e = (d == 2560) ? launch_geometry<2560, 320>(T, da, ua, st)
                               : launch_geometry<4096, 512>(T, da, ua, st);

@@ -31,8 +31,8 @@
  *   rs                     : float  [T][n]
  *
  * Ownership: the caller owns every tensor.  A handle owns its scratch
- * (partial sums, per-slab sums of squares, arrival counters, an error word),
- * allocated and zeroed by hc_read_create and freed by hc_read_destroy.
+ * (per-stream partial sums and an error word), allocated and zeroed by
+ * hc_read_create and freed by hc_read_destroy.
  *
  * Aliasing: out may equal R (in-place update of the residual).  pending must
  * not overlap out; lo, mean, r_out and rs must not overlap any input.
@@ -43,15 +43,17 @@
  * CUDA graph; replays give the same bits as direct calls.  The kernels use
  * programmatic dependent launch: each kernel prefetches its BF16 weights,
  * w_norm and gate before it waits for the preceding kernel in the stream, so
- * those four arrays must not be written by a kernel that immediately precedes
- * the read on the stream and itself triggers its dependents early (kernels
- * that do not use programmatic completion are always waited for in full).
+ * those four arrays must not be written by a kernel that immediately
+ * precedes the read on the stream and itself triggers its dependents early
+ * (kernels that do not use programmatic completion, copies and memsets are
+ * always waited for in full).  Everything else (R, pending, the outputs, the
+ * scratch) is touched only after that wait.
  *
  * Errors: every entry point returns an hc_status (0 = HC_OK).  Argument errors
  * are detected on the host before anything is enqueued.  HC_ERR_CUDA reports
  * a CUDA runtime error at launch.  A kernel that gives up on a bounded wait
  * records it in the handle's error word; hc_read_check reports it as
- * HC_ERR_TIMEOUT, after which hc_read_reset must be called.
+ * HC_ERR_TIMEOUT until hc_read_reset clears it.
  */
 #ifndef HC_READ_H
 #define HC_READ_H
@@ -103,8 +105,7 @@ int hc_read_ex(hc_read_t h, const float* R, const float* w_norm, const uint16_t*
  * last hc_read_reset. */
 int hc_read_check(hc_read_t h);
 
-/* Re-zero the handle's arrival counters and error word on `stream` (needed
- * only after a read was aborted or reported HC_ERR_TIMEOUT). */
+/* Re-zero the handle's error word on `stream` (after HC_ERR_TIMEOUT). */
 int hc_read_reset(hc_read_t h, hc_stream_t stream);
 
 /* Free the handle's scratch.  Synchronises with the handle's device first.
@@ -138,7 +139,7 @@ int64_t hc_read_scratch_bytes(hc_read_t h);
  * give wrong results, so serialise them.  Each call clears the parts of the
  * scratch that must start at zero on `stream` before its kernels run. */
 #define HC_NOALLOC_MAX_T 8
-#define HC_NOALLOC_SCRATCH_BYTES (16 * HC_NOALLOC_MAX_T * 512 * 4 + 16 * 16 * HC_NOALLOC_MAX_T * 4 + 256)
+#define HC_NOALLOC_SCRATCH_BYTES (4 * HC_NOALLOC_MAX_T * 512 * 4 + 256)
 int hc_read_noalloc(int n, int d, int K, float eps, const float* R, const float* w_norm,
                     const uint16_t* W_down, const uint16_t* W_up, const float* gate,
                     const float* pending, int T, float* out, float* mean, float* lo,

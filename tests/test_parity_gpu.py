@@ -119,7 +119,7 @@ def test_repeat_and_graph_replay_bitwise(dev, g1, rd1):
     run(rd1, w, a, T, o1)
     torch.cuda.synchronize()
     ref = {k: bits(v) for k, v in o1.items()}
-    # a second direct call (counters must have been reset by the first)
+    # a second direct call on the same handle
     o2 = outputs(g, T, dev)
     run(rd1, w, a, T, o2)
     torch.cuda.synchronize()
@@ -204,3 +204,94 @@ def test_argument_errors(dev, g1, rd1):
     with pytest.raises(hc.HcError):
         hc.Read(4, 2560, 320, T_max=0)
     assert rd1.check() == hc.HC_OK
+
+
+def _oracle_from_gpu_inputs(orc, g, ws, R, P):
+    return orc.read(g.n, g.d, g.K, R=R, P=P, w_norm=ws.w_norm, W_down=ws.W_down,
+                    W_up=ws.W_up, gate=ws.gate, eps=EPS)
+
+
+@pytest.mark.parametrize("use_graph", [False, True], ids=["direct", "graph"])
+def test_chained_reads(dev, orc, rd1, use_graph):
+    """Read i's out is read i+1's R (the window's chaining): each read is
+    checked against the oracle fed with that read's GPU input."""
+    g = synth.G1
+    T, n_reads = 4, 5
+    sets = [synth.weight_set(g, 20 + i) for i in range(n_reads)]
+    w = [dev_weights(ws, dev) for ws in sets]
+    act = synth.activations(g, T, True, s0=31)
+    P = torch.from_numpy(act.P).to(dev)
+    bufs = [torch.from_numpy(act.R).to(dev)] + [torch.empty(T, g.N, device=dev) for _ in range(n_reads)]
+    outs = [outputs(g, T, dev) for _ in range(n_reads)]
+    s = torch.cuda.Stream()
+
+    def enqueue():
+        for i in range(n_reads):
+            rd1(bufs[i], w[i]["w_norm"], w[i]["W_down"], w[i]["W_up"], w[i]["gate"], P, T,
+                bufs[i + 1], outs[i]["mean"], outs[i]["lo"], r_out=outs[i]["r_out"],
+                rs=outs[i]["rs"], stream=s)
+
+    if use_graph:
+        with torch.cuda.stream(s):
+            hc.hc_graph_begin(s)
+            enqueue()
+            graph = hc.hc_graph_end(s)
+        try:
+            hc.hc_graph_launch(graph, s)
+            s.synchronize()
+        finally:
+            hc.hc_graph_destroy(graph)
+    else:
+        with torch.cuda.stream(s):
+            enqueue()
+        s.synchronize()
+    assert rd1.check() == hc.HC_OK
+    for i in range(n_reads):
+        R_in = bufs[i].cpu().numpy()
+        ref = _oracle_from_gpu_inputs(orc, g, sets[i], R_in, act.P)
+        o = dict(outs[i])
+        o["out"] = bufs[i + 1]
+        assert_parity(o, ref, T, f"chained read {i}")
+
+
+@pytest.mark.parametrize("same_out", [False, True], ids=["own_outputs", "shared_outputs"])
+def test_back_to_back_independent_reads(dev, orc, rd1, same_out):
+    """Reads that do not consume each other's outputs overlap on the GPU; each
+    still matches the oracle, and with shared output buffers the last read's
+    results are what remains."""
+    g = synth.G1
+    T, n_reads = 3, 6
+    sets = [synth.weight_set(g, 40 + i) for i in range(n_reads)]
+    w = [dev_weights(ws, dev) for ws in sets]
+    act = synth.activations(g, T, True, s0=51)
+    a = dev_act(act, dev)
+    shared = outputs(g, T, dev)
+    outs = [shared if same_out else outputs(g, T, dev) for _ in range(n_reads)]
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for i in range(n_reads):
+            run(rd1, w[i], a, T, outs[i], stream=s)
+    s.synchronize()
+    check = [n_reads - 1] if same_out else range(n_reads)
+    for i in check:
+        assert_parity(outs[i], oracle_read(orc, g, sets[i], act), T, f"read {i}")
+
+
+def test_in_place_chain(dev, orc, rd1):
+    """out = R in place, three times in a row: each read consumes the previous one."""
+    g = synth.G1
+    T = 2
+    sets = [synth.weight_set(g, 60 + i) for i in range(3)]
+    act = synth.activations(g, T, False, s0=61)
+    R = torch.from_numpy(act.R).to(dev)
+    o = outputs(g, T, dev)
+    R_host = act.R.copy()
+    for i in range(3):
+        w = dev_weights(sets[i], dev)
+        rd1(R, w["w_norm"], w["W_down"], w["W_up"], w["gate"], None, T, R, o["mean"], o["lo"])
+        ref = _oracle_from_gpu_inputs(orc, g, sets[i], R_host, None)
+        torch.cuda.synchronize()
+        got = R.double().cpu().numpy()
+        err = float(np.max(np.abs(got - ref.out)))
+        assert err <= 1e-4 * float(np.max(np.abs(ref.out))), f"in-place read {i}: {err}"
+        R_host = R.cpu().numpy()
