@@ -256,13 +256,14 @@ __global__ void __launch_bounds__(kThreads, 2) hc_down_kernel(const DownArgs a) 
                   G::SLAB * 2, bar_w, once);
   }
   ptx::launch_dependents();
+  __syncthreads();  // the mbarriers are initialised before any thread waits on them
+  // w_norm is a parameter: wait for it before the previous kernel finishes.
+  bool ok = wait_bar(bar_n, 0, a.err, kErrDownNorm);
   ptx::wait_prerequisites();  // R, P and the scratch belong to the previous kernel until now
   ptx::cluster_wait();
-  __syncthreads();  // the mbarriers are initialised before any thread waits on them
 
   // A timed-out wait leaves garbage in shared memory but the CTA still runs
   // to the end: it must take part in the cluster barrier below.
-  bool ok = true;
   for (int t0 = 0; t0 < T; t0 += TT) {
     const int tg = min(TT, T - t0);
 
@@ -284,7 +285,6 @@ __global__ void __launch_bounds__(kThreads, 2) hc_down_kernel(const DownArgs a) 
         }
       }
     }
-    if (t0 == 0) ok = wait_bar(bar_n, 0, a.err, kErrDownNorm) && ok;
     float ssl[TT];
 #pragma unroll
     for (int t = 0; t < TT; ++t) {
@@ -382,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 2) hc_down_kernel(const DownArgs a) 
     float ss = 0.f;
 #pragma unroll
     for (int q = 0; q < G::SLABS_PER_STREAM; ++q) ss += recv_ss[q * T + t];
-    const float rs = 1.0f / sqrtf(ss / (float)D + a.eps);
+    const float rs = rsqrtf(ss * (1.0f / (float)D) + a.eps);
     rs_s[t] = rs;
     if (rg == 0 && a.rs_out != nullptr) a.rs_out[t * kStreams + stream] = rs;
   }
@@ -440,17 +440,18 @@ __global__ void __launch_bounds__(kThreads, 2) hc_up_kernel(const UpArgs a) {
       ptx::bulk_g2s(w_s + r * G::UP_PITCH, a.W_up + (size_t)grow * KD, KD * 2, bar_w, once);
     }
   }
-  ptx::wait_prerequisites();  // the partials, R and P are ready from here on
-  // Only now may the next read's kernels launch: launching them earlier lets
-  // a cascade of waiting CTAs crowd the SMs that are computing this read.
-  ptx::launch_dependents();
   __syncthreads();  // the mbarriers are initialised before any thread waits on them
-
+  // The gates are parameters: their sigmoids are ready before the previous
+  // kernel finishes.
   bool ok = true;
   if (tid < G::UP_ROWS) {
     ok = wait_bar(bar_g, 0, a.err, kErrUpGate);
     sig_s[tid] = 1.0f / (1.0f + expf(-g_s[tid]));
   }
+  ptx::wait_prerequisites();  // the partials, R and P are ready from here on
+  // Only now may the next read's kernels launch: launching them earlier lets
+  // a cascade of waiting CTAs crowd the SMs that are computing this read.
+  ptx::launch_dependents();
 
   const int T = a.T;
   for (int t0 = 0; t0 < T; t0 += TT) {

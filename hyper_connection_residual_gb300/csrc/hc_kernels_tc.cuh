@@ -1,0 +1,454 @@
+// Tensor-core (warp-level mma.sync, BF16 in, FP32 accumulate) variants of the
+// two read kernels.
+//
+// The read is a skinny contraction: [T x N] x [N x K] for the down projection
+// and [T x K] x [K x N] for the up projection, with BF16 weights.  The FP32
+// activations (x = R' * w_norm for the down projection, lo for the up
+// projection) are split into two BF16 terms, hi = bf16(x) and
+// lo = bf16(x - hi) (x - hi is exact in FP32), so that hi + lo carries 16
+// significant bits and the products keep a relative error near 2^-17 instead
+// of the 2^-9 of a single BF16 term; both terms go through the MMA as separate
+// columns of the B operand (column 2t holds token t's hi, column 2t+1 its lo)
+// and are added in FP32 afterwards.  Accumulation is FP32 inside the MMA.
+//
+// Tiling, data movement, the cluster combine and the programmatic-launch
+// protocol are the ones of the CUDA-core kernels (hc_kernels.cuh): the down
+// kernel's CTA owns 32 rows of W_down x one d/4-column slab (two m16 tiles x
+// four K-parts over 8 warps), the up kernel's CTA owns 64 rows of W_up (four
+// m16 tiles x two K-halves).  Tokens are processed in groups of TG = 4 * NT
+// (N = 8 * NT MMA columns).
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "hc_kernels.cuh"
+
+namespace hc {
+
+// Split x into BF16 hi and lo parts packed as two bf16x2 words per pair.
+__device__ __forceinline__ uint32_t pack_bf16x2(__nv_bfloat16 a, __nv_bfloat16 b) {
+  return static_cast<uint32_t>(__bfloat16_as_ushort(a)) |
+         (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
+}
+
+__device__ __forceinline__ void split4(const float4 x, uint2& hi, uint2& lo) {
+  const __nv_bfloat16 h0 = __float2bfloat16_rn(x.x), h1 = __float2bfloat16_rn(x.y);
+  const __nv_bfloat16 h2 = __float2bfloat16_rn(x.z), h3 = __float2bfloat16_rn(x.w);
+  const __nv_bfloat16 l0 = __float2bfloat16_rn(__fsub_rn(x.x, __bfloat162float(h0)));
+  const __nv_bfloat16 l1 = __float2bfloat16_rn(__fsub_rn(x.y, __bfloat162float(h1)));
+  const __nv_bfloat16 l2 = __float2bfloat16_rn(__fsub_rn(x.z, __bfloat162float(h2)));
+  const __nv_bfloat16 l3 = __float2bfloat16_rn(__fsub_rn(x.w, __bfloat162float(h3)));
+  hi = make_uint2(pack_bf16x2(h0, h1), pack_bf16x2(h2, h3));
+  lo = make_uint2(pack_bf16x2(l0, l1), pack_bf16x2(l2, l3));
+}
+
+template <int D, int KD, int NT>
+struct DownTcSmem {
+  using G = Geo<D, KD>;
+  static constexpr int TG = 4 * NT;
+  static constexpr int NCOL = 8 * NT;
+  static constexpr int XS_PITCH = G::SLAB * 2 + 16;   // bytes; = 16 (mod 128)
+  static constexpr int BAR = 0;
+  static constexpr int W = 128;
+  static constexpr int WN = W + G::DN_ROWS * G::DN_PITCH;
+  static constexpr int XS = WN + G::SLAB * 4;         // [NCOL][SLAB] bf16: hi, lo rows
+  static constexpr int RED = XS + NCOL * XS_PITCH;    // [4 K-parts][TG][32] partials
+  static constexpr int SSW = RED + 4 * TG * 32 * 4;   // [8 warps][TG]
+  static constexpr int RS = SSW + kWarps * TG * 4;    // [kMaxT]
+  static constexpr int RECV = RS + kMaxT * 4;         // [4][T] ss, then [4][T][32] partials
+  static constexpr int bytes(int T) { return RECV + 4 * T * 4 + 4 * T * 32 * 4; }
+  static constexpr int BYTES_MAX = RECV + 4 * kMaxT * 4 + 4 * kMaxT * 32 * 4;
+  static_assert(XS_PITCH % 128 == 16, "x rows must be conflict-free for ldmatrix");
+};
+
+template <int D, int KD, int NT>
+struct UpTcSmem {
+  using G = Geo<D, KD>;
+  static constexpr int TG = 4 * NT;
+  static constexpr int NCOL = 8 * NT;
+  static constexpr int LS_PITCH = KD * 2 + 16;        // bytes; = 16 (mod 128)
+  static constexpr int BAR = 0;
+  static constexpr int W = 128;
+  static constexpr int GATE = W + G::UP_ROWS * G::UP_PITCH;
+  static constexpr int SIG = GATE + G::UP_ROWS * 4;
+  static constexpr int LS = SIG + G::UP_ROWS * 4;     // [NCOL][KD] bf16: hi, lo rows
+  static constexpr int RED = LS + NCOL * LS_PITCH;    // [2 K-halves][TG][64]
+  static constexpr int OUT = RED + 2 * TG * G::UP_ROWS * 4;
+  static constexpr int RP = OUT + TG * G::UP_ROWS * 4;
+  static constexpr int BYTES = RP + TG * G::UP_ROWS * 4;
+  static constexpr int bytes(int) { return BYTES; }
+  static constexpr int BYTES_MAX = BYTES;
+  static_assert(LS_PITCH % 128 == 16, "lo rows must be conflict-free for ldmatrix");
+};
+
+// ------------------------------------------------------------------ kernel 1
+// Grid (16 slabs, K/32 row groups), clusters of 4 along x (one stream).
+template <int D, int KD, int NT>
+__global__ void __launch_bounds__(kThreads, 2) hc_down_tc_kernel(const DownArgs a) {
+  using G = Geo<D, KD>;
+  using S = DownTcSmem<D, KD, NT>;
+  constexpr int TG = S::TG;
+  constexpr int KPART = G::SLAB / 4;   // columns per K-part
+  constexpr int KS = KPART / 16;       // k-steps per warp
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t* bar_w = reinterpret_cast<uint64_t*>(smem + S::BAR);
+  uint64_t* bar_n = bar_w + 1;
+  unsigned char* w_s = smem + S::W;
+  const float* wn_s = reinterpret_cast<const float*>(smem + S::WN);
+  unsigned char* xs = smem + S::XS;
+  float* red_s = reinterpret_cast<float*>(smem + S::RED);
+  float* ssw_s = reinterpret_cast<float*>(smem + S::SSW);
+  float* rs_s = reinterpret_cast<float*>(smem + S::RS);
+
+  const int slab = blockIdx.x;
+  const int stream = slab / G::SLABS_PER_STREAM;
+  const int rg = blockIdx.y;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int col0 = slab * G::SLAB;
+  const int row0 = rg * G::DN_ROWS;
+  const int T = a.T;
+  const int mt = warp & 1;    // m16 tile: rows 16 mt .. 16 mt + 15
+  const int kp = warp >> 1;   // K-part: columns kp * KPART .. + KPART
+
+  cg::cluster_group cluster = cg::this_cluster();
+  const unsigned rank = cluster.block_rank();
+  float* recv_ss = cluster.map_shared_rank(reinterpret_cast<float*>(smem + S::RECV), 0);
+  float* recv_p = recv_ss + 4 * T;
+
+  ptx::cluster_arrive_relaxed();
+  if (warp == 0) {
+    if (lane == 0) {
+      ptx::mbar_init(bar_w, 1);
+      ptx::mbar_init(bar_n, 1);
+      ptx::fence_barrier_init();
+      ptx::mbar_arrive_expect_tx(bar_n, G::SLAB * 4);
+      ptx::mbar_arrive_expect_tx(bar_w, G::DN_ROWS * G::SLAB * 2);
+      ptx::bulk_g2s(smem + S::WN, a.w_norm + col0, G::SLAB * 4, bar_n, ptx::policy_evict_last());
+    }
+    __syncwarp();
+    const uint64_t once = ptx::policy_evict_first();
+    ptx::bulk_g2s(w_s + lane * G::DN_PITCH, a.W_down + (size_t)(row0 + lane) * G::N + col0,
+                  G::SLAB * 2, bar_w, once);
+  }
+  ptx::launch_dependents();
+  __syncthreads();  // the mbarriers are initialised before any thread waits on them
+  bool ok = wait_bar(bar_n, 0, a.err, kErrDownNorm);
+  ptx::wait_prerequisites();  // R, P and the scratch belong to the previous kernel until now
+  ptx::cluster_wait();
+
+  // Lane address pattern of an ldmatrix.x4 on a 16x16 A tile.
+  const int a_row = mt * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+  const int a_col = kp * KPART + 8 * (lane >> 4);
+  const uint32_t a_base = ptx::smem_u32(w_s + a_row * G::DN_PITCH + a_col * 2);
+  // ... and of the B operand (rows = MMA columns).
+  const int b_row = (lane & 7) + 8 * (lane >> 4);
+  const int b_col = kp * KPART + 8 * ((lane >> 3) & 1);
+
+  for (int t0 = 0; t0 < T; t0 += TG) {
+    const int tg = min(TG, T - t0);
+    float4 rv[TG], pv[TG];
+    const int c4 = tid;  // one float4 of the slab per thread and token
+    static_assert(G::DN_F4 <= kThreads, "one float4 per thread and token");
+#pragma unroll
+    for (int t = 0; t < TG; ++t) {
+      rv[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+      pv[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (t < tg && c4 < G::DN_F4) {
+        const size_t base = (size_t)(t0 + t) * G::N + col0;
+        rv[t] = __ldcg(reinterpret_cast<const float4*>(a.R + base) + c4);
+        if (a.P) pv[t] = __ldcg(reinterpret_cast<const float4*>(a.P + base) + c4);
+      }
+    }
+    float ssl[TG];
+#pragma unroll
+    for (int t = 0; t < TG; ++t) {
+      ssl[t] = 0.f;
+      if (c4 < G::DN_F4) {
+        float4 r = rv[t];
+        r.x = __fadd_rn(r.x, pv[t].x);
+        r.y = __fadd_rn(r.y, pv[t].y);
+        r.z = __fadd_rn(r.z, pv[t].z);
+        r.w = __fadd_rn(r.w, pv[t].w);
+        const float4 w = reinterpret_cast<const float4*>(wn_s)[c4];
+        const float4 x = make_float4(__fmul_rn(r.x, w.x), __fmul_rn(r.y, w.y), __fmul_rn(r.z, w.z),
+                                     __fmul_rn(r.w, w.w));
+        uint2 hi, lo;
+        split4(x, hi, lo);  // tokens past tg carry zeros
+        *reinterpret_cast<uint2*>(xs + (2 * t) * S::XS_PITCH + c4 * 8) = hi;
+        *reinterpret_cast<uint2*>(xs + (2 * t + 1) * S::XS_PITCH + c4 * 8) = lo;
+        ssl[t] = __fmaf_rn(r.x, r.x, ssl[t]);
+        ssl[t] = __fmaf_rn(r.y, r.y, ssl[t]);
+        ssl[t] = __fmaf_rn(r.z, r.z, ssl[t]);
+        ssl[t] = __fmaf_rn(r.w, r.w, ssl[t]);
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < TG; ++t) {
+      float v = ssl[t];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0) ssw_s[warp * TG + t] = v;
+    }
+    if (t0 == 0) ok = wait_bar(bar_w, 0, a.err, kErrDownWeights) && ok;
+    __syncthreads();  // x (hi, lo) and the per-warp sums of squares are complete
+    if (tid < tg) {
+      float v = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) v += ssw_s[w * TG + tid];
+      recv_ss[rank * T + t0 + tid] = v;
+    }
+
+    float acc[NT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      uint32_t afrag[4];
+      ptx::ldsm_x4(a_base + ks * 32, afrag[0], afrag[1], afrag[2], afrag[3]);
+#pragma unroll
+      for (int n = 0; n < NT; n += 2) {
+        uint32_t b0, b1, b2, b3;
+        if (n + 1 < NT) {
+          ptx::ldsm_x4(ptx::smem_u32(xs + (n * 8 + b_row) * S::XS_PITCH + (b_col + ks * 16) * 2), b0, b1,
+                       b2, b3);
+          ptx::mma_bf16_16816(acc[n], afrag, b0, b1);
+          ptx::mma_bf16_16816(acc[n + 1], afrag, b2, b3);
+        } else {
+          ptx::ldsm_x2(ptx::smem_u32(xs + (n * 8 + (lane & 7)) * S::XS_PITCH + (b_col + ks * 16) * 2), b0,
+                       b1);
+          ptx::mma_bf16_16816(acc[n], afrag, b0, b1);
+        }
+      }
+    }
+    // Column 2t holds token t's hi part, 2t + 1 its lo part.
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      const int t = n * 4 + (lane & 3);
+      const int r = mt * 16 + (lane >> 2);
+      red_s[(kp * TG + t) * 32 + r] = __fadd_rn(acc[n][0], acc[n][1]);
+      red_s[(kp * TG + t) * 32 + r + 8] = __fadd_rn(acc[n][2], acc[n][3]);
+    }
+    __syncthreads();
+    for (int idx = tid; idx < tg * 32; idx += kThreads) {
+      const int t = idx >> 5, r = idx & 31;
+      const float v = ((red_s[(0 * TG + t) * 32 + r] + red_s[(1 * TG + t) * 32 + r]) +
+                       red_s[(2 * TG + t) * 32 + r]) +
+                      red_s[(3 * TG + t) * 32 + r];
+      recv_p[(rank * T + t0 + t) * 32 + r] = v;
+    }
+    __syncthreads();
+  }
+  if (!ok) {
+    drain(bar_n, 0);
+    drain(bar_w, 0);
+  }
+  ptx::cluster_arrive_release();
+  ptx::cluster_wait();
+  if (rank != 0) return;
+
+  for (int t = tid; t < T; t += kThreads) {
+    float ss = 0.f;
+#pragma unroll
+    for (int q = 0; q < G::SLABS_PER_STREAM; ++q) ss += recv_ss[q * T + t];
+    const float rs = rsqrtf(ss * (1.0f / (float)D) + a.eps);
+    rs_s[t] = rs;
+    if (rg == 0 && a.rs_out != nullptr) a.rs_out[t * kStreams + stream] = rs;
+  }
+  __syncthreads();
+  float* part = a.part + (size_t)stream * a.T_max * KD;
+  for (int idx = tid; idx < T * G::DN_ROWS; idx += kThreads) {
+    const int t = idx >> 5, r = idx & 31;
+    float p = 0.f;
+#pragma unroll
+    for (int q = 0; q < G::SLABS_PER_STREAM; ++q) p += recv_p[(q * T + t) * 32 + r];
+    __stcg(part + (size_t)t * KD + row0 + r, __fmul_rn(rs_s[t], p));
+  }
+}
+
+// ------------------------------------------------------------------ kernel 2
+template <int D, int KD, int NT>
+__global__ void __launch_bounds__(kThreads, 2) hc_up_tc_kernel(const UpArgs a) {
+  using G = Geo<D, KD>;
+  using S = UpTcSmem<D, KD, NT>;
+  constexpr int TG = S::TG;
+  constexpr int KHALF = KD / 2;
+  constexpr int KS = KHALF / 16;
+  constexpr int EPI = (TG * G::UP_ROWS + kThreads - 1) / kThreads;
+  constexpr int LO4 = (TG * KD / 4 + kThreads - 1) / kThreads;
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t* bar_w = reinterpret_cast<uint64_t*>(smem + S::BAR);
+  uint64_t* bar_g = bar_w + 1;
+  unsigned char* w_s = smem + S::W;
+  const float* g_s = reinterpret_cast<const float*>(smem + S::GATE);
+  float* sig_s = reinterpret_cast<float*>(smem + S::SIG);
+  unsigned char* ls = smem + S::LS;
+  float* red_s = reinterpret_cast<float*>(smem + S::RED);
+  float* out_s = reinterpret_cast<float*>(smem + S::OUT);
+  float* rp_s = reinterpret_cast<float*>(smem + S::RP);
+
+  const int c0 = blockIdx.x * G::UP_COLS;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int mt = warp & 3;   // m16 tile of the 64 rows
+  const int kh = warp >> 2;  // K half
+
+  if (warp == 0) {
+    if (lane == 0) {
+      ptx::mbar_init(bar_w, 1);
+      ptx::mbar_init(bar_g, 1);
+      ptx::fence_barrier_init();
+      ptx::mbar_arrive_expect_tx(bar_w, G::UP_ROWS * KD * 2);
+      ptx::mbar_arrive_expect_tx(bar_g, G::UP_ROWS * 4);
+    }
+    __syncwarp();
+    const uint64_t once = ptx::policy_evict_first();
+    if (lane < kStreams) {
+      ptx::bulk_g2s(smem + S::GATE + lane * G::UP_COLS * 4, a.gate + lane * D + c0,
+                    G::UP_COLS * 4, bar_g, once);
+    }
+    for (int r = lane; r < G::UP_ROWS; r += 32) {
+      const int grow = (r / G::UP_COLS) * D + c0 + (r % G::UP_COLS);
+      ptx::bulk_g2s(w_s + r * G::UP_PITCH, a.W_up + (size_t)grow * KD, KD * 2, bar_w, once);
+    }
+  }
+  __syncthreads();  // the mbarriers are initialised before any thread waits on them
+  bool ok = true;
+  if (tid < G::UP_ROWS) {
+    ok = wait_bar(bar_g, 0, a.err, kErrUpGate);
+    sig_s[tid] = 1.0f / (1.0f + expf(-g_s[tid]));
+  }
+  ptx::wait_prerequisites();  // the partials, R and P are ready from here on
+  ptx::launch_dependents();
+
+  const int a_row = mt * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+  const int a_col = kh * KHALF + 8 * (lane >> 4);
+  const uint32_t a_base = ptx::smem_u32(w_s + a_row * G::UP_PITCH + a_col * 2);
+  const int b_row = (lane & 7) + 8 * (lane >> 4);
+  const int b_col = kh * KHALF + 8 * ((lane >> 3) & 1);
+
+  const int T = a.T;
+  for (int t0 = 0; t0 < T; t0 += TG) {
+    const int tg = min(TG, T - t0);
+    // All global loads of the group first: the four per-stream partials of
+    // lo, then R and P of this CTA's rows.
+    float4 pv[LO4][kStreams];
+#pragma unroll
+    for (int m = 0; m < LO4; ++m) {
+      const int idx = tid + m * kThreads;
+#pragma unroll
+      for (int s = 0; s < kStreams; ++s) {
+        pv[m][s] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (idx < tg * KD / 4) {
+          pv[m][s] = __ldcg(reinterpret_cast<const float4*>(
+                                a.part + ((size_t)s * a.T_max + t0) * KD) + idx);
+        }
+      }
+    }
+    float rr[EPI], pp[EPI];
+#pragma unroll
+    for (int m = 0; m < EPI; ++m) {
+      const int idx = tid + m * kThreads;
+      const int t = idx / G::UP_ROWS, r = idx % G::UP_ROWS;
+      rr[m] = 0.f;
+      pp[m] = 0.f;
+      if (t < tg) {
+        const size_t off = (size_t)(t0 + t) * G::N + (r / G::UP_COLS) * D + c0 + (r % G::UP_COLS);
+        rr[m] = __ldcg(a.R + off);
+        if (a.P) pp[m] = __ldcg(a.P + off);
+      }
+    }
+    // lo (four partials in stream order), its hi/lo split, and this CTA's
+    // share of the lo output.
+#pragma unroll
+    for (int m = 0; m < LO4; ++m) {
+      const int idx = tid + m * kThreads;
+      if (idx < TG * KD / 4) {
+        float4 l;
+        l.x = ((pv[m][0].x + pv[m][1].x) + pv[m][2].x) + pv[m][3].x;
+        l.y = ((pv[m][0].y + pv[m][1].y) + pv[m][2].y) + pv[m][3].y;
+        l.z = ((pv[m][0].z + pv[m][1].z) + pv[m][2].z) + pv[m][3].z;
+        l.w = ((pv[m][0].w + pv[m][1].w) + pv[m][2].w) + pv[m][3].w;
+        const int t = idx / (KD / 4), k4 = idx % (KD / 4);
+        uint2 hi, lo;
+        split4(l, hi, lo);  // tokens past tg carry zeros
+        *reinterpret_cast<uint2*>(ls + (2 * t) * S::LS_PITCH + k4 * 8) = hi;
+        *reinterpret_cast<uint2*>(ls + (2 * t + 1) * S::LS_PITCH + k4 * 8) = lo;
+        const int k = k4 * 4;
+        const float lv[4] = {l.x, l.y, l.z, l.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int kk = k + e;
+          if (t < tg && kk / G::LO_PER_CTA == (int)blockIdx.x) a.lo[(size_t)(t0 + t) * KD + kk] = lv[e];
+        }
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < EPI; ++m) {
+      const int idx = tid + m * kThreads;
+      if (idx < tg * G::UP_ROWS) rp_s[idx] = __fadd_rn(rr[m], pp[m]);
+    }
+    if (t0 == 0) ok = wait_bar(bar_w, 0, a.err, kErrUpWeights) && ok;
+    __syncthreads();  // lo (hi, lo), R' and the gates are in shared memory
+
+    float acc[NT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      uint32_t afrag[4];
+      ptx::ldsm_x4(a_base + ks * 32, afrag[0], afrag[1], afrag[2], afrag[3]);
+#pragma unroll
+      for (int n = 0; n < NT; n += 2) {
+        uint32_t b0, b1, b2, b3;
+        if (n + 1 < NT) {
+          ptx::ldsm_x4(ptx::smem_u32(ls + (n * 8 + b_row) * S::LS_PITCH + (b_col + ks * 16) * 2), b0, b1,
+                       b2, b3);
+          ptx::mma_bf16_16816(acc[n], afrag, b0, b1);
+          ptx::mma_bf16_16816(acc[n + 1], afrag, b2, b3);
+        } else {
+          ptx::ldsm_x2(ptx::smem_u32(ls + (n * 8 + (lane & 7)) * S::LS_PITCH + (b_col + ks * 16) * 2), b0,
+                       b1);
+          ptx::mma_bf16_16816(acc[n], afrag, b0, b1);
+        }
+      }
+    }
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      const int t = n * 4 + (lane & 3);
+      const int r = mt * 16 + (lane >> 2);
+      red_s[(kh * TG + t) * G::UP_ROWS + r] = __fadd_rn(acc[n][0], acc[n][1]);
+      red_s[(kh * TG + t) * G::UP_ROWS + r + 8] = __fadd_rn(acc[n][2], acc[n][3]);
+    }
+    __syncthreads();
+
+    // Epilogue: pending write, gate, stream mean.
+    for (int idx = tid; idx < tg * G::UP_ROWS; idx += kThreads) {
+      const int t = idx / G::UP_ROWS, r = idx % G::UP_ROWS;
+      const float u = red_s[(0 * TG + t) * G::UP_ROWS + r] + red_s[(1 * TG + t) * G::UP_ROWS + r];
+      const int i = (r / G::UP_COLS) * D + c0 + (r % G::UP_COLS);
+      const size_t off = (size_t)(t0 + t) * G::N + i;
+      const float rp = rp_s[idx];
+      const float o = __fmaf_rn(sig_s[r], u, rp);
+      a.out[off] = o;
+      if (a.r_out != nullptr) a.r_out[off] = rp;
+      out_s[idx] = o;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < tg * G::UP_COLS; idx += kThreads) {
+      const int t = idx / G::UP_COLS, j = idx % G::UP_COLS;
+      const float* o = out_s + t * G::UP_ROWS + j;
+      const float m = (((o[0] + o[G::UP_COLS]) + o[2 * G::UP_COLS]) + o[3 * G::UP_COLS]) * 0.25f;
+      a.mean[(size_t)(t0 + t) * D + c0 + j] = m;
+    }
+    __syncthreads();
+  }
+  if (!ok) {
+    drain(bar_g, 0);
+    drain(bar_w, 0);
+  }
+}
+
+}  // namespace hc

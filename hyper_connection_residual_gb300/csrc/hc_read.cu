@@ -9,6 +9,7 @@
 #include <new>
 
 #include "hc_kernels.cuh"
+#include "hc_kernels_tc.cuh"
 #include "hc_read.h"
 
 #define HC_EXPORT extern "C" __attribute__((visibility("default")))
@@ -65,6 +66,17 @@ cudaError_t configure_one() {
                               hc::UpSmem<D, KD, TT>::BYTES_MAX);
 }
 
+template <int D, int KD, int NT>
+cudaError_t configure_tc() {
+  cudaError_t e = cudaFuncSetAttribute(hc::hc_down_tc_kernel<D, KD, NT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       hc::DownTcSmem<D, KD, NT>::BYTES_MAX);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(hc::hc_up_tc_kernel<D, KD, NT>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              hc::UpTcSmem<D, KD, NT>::BYTES_MAX);
+}
+
 template <int D, int KD>
 cudaError_t configure_geometry() {
   cudaError_t e;
@@ -75,7 +87,9 @@ cudaError_t configure_geometry() {
   if ((e = configure_one<D, KD, 5>()) != cudaSuccess) return e;
   if ((e = configure_one<D, KD, 6>()) != cudaSuccess) return e;
   if ((e = configure_one<D, KD, 7>()) != cudaSuccess) return e;
-  return configure_one<D, KD, 8>();
+  if ((e = configure_one<D, KD, 8>()) != cudaSuccess) return e;
+  if ((e = configure_tc<D, KD, 1>()) != cudaSuccess) return e;
+  return configure_tc<D, KD, 2>();
 }
 
 template <int D, int KD, int TT>
@@ -93,8 +107,31 @@ cudaError_t launch_pair(const DownArgs& da, const UpArgs& ua, cudaStream_t st) {
   return cudaLaunchKernelEx(&c2, hc::hc_up_kernel<D, KD, TT>, ua);
 }
 
+template <int D, int KD, int NT>
+cudaError_t launch_pair_tc(const DownArgs& da, const UpArgs& ua, cudaStream_t st) {
+  using G = hc::Geo<D, KD>;
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t c1 = pdl_config(dim3(G::SLABS, G::ROW_GROUPS),
+                                      hc::DownTcSmem<D, KD, NT>::bytes(da.T), st, attr,
+                                      G::SLABS_PER_STREAM);
+  cudaError_t e = cudaLaunchKernelEx(&c1, hc::hc_down_tc_kernel<D, KD, NT>, da);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr2[2];
+  cudaLaunchConfig_t c2 = pdl_config(dim3(G::UP_CTAS), hc::UpTcSmem<D, KD, NT>::bytes(ua.T), st,
+                                      attr2, 1);
+  return cudaLaunchKernelEx(&c2, hc::hc_up_tc_kernel<D, KD, NT>, ua);
+}
+
+// From T = 2 on the tensor-core kernels are faster on GB300 (measured: T=2
+// 6.1 vs 6.7 us, T=8 7.9 vs 11.1 us per read); at T = 1 the CUDA-core kernels
+// are (5.2 vs 6.0 us): the MMA path stages four tokens there.
+constexpr int kTcMinT = 2;
+
 template <int D, int KD>
 cudaError_t launch_geometry(int T, const DownArgs& da, const UpArgs& ua, cudaStream_t st) {
+  if (T >= kTcMinT) {
+    return T <= 4 ? launch_pair_tc<D, KD, 1>(da, ua, st) : launch_pair_tc<D, KD, 2>(da, ua, st);
+  }
   switch (T) {
     case 1: return launch_pair<D, KD, 1>(da, ua, st);
     case 2: return launch_pair<D, KD, 2>(da, ua, st);
