@@ -162,9 +162,11 @@ def test_in_place_update(dev, g1, rd1):
     assert np.array_equal(bits(o2["mean"]), bits(o["mean"]))
 
 
-def test_t1_is_row0_of_repeated_rows(dev, g1, rd1):
-    """A T=8 call whose 8 tokens are copies of one token gives, on every row,
-    the T=1 result bit for bit (tokens are independent)."""
+def test_repeated_rows_agree(dev, g1, rd1):
+    """A T=8 call whose 8 tokens are copies of one token gives the same bits on
+    every row (tokens are independent), and those rows agree with a T=1 call
+    within the parity bar (T=1 runs the CUDA-core kernels, T=8 the tensor-core
+    kernels, so the two summation orders differ); R' is bitwise in both."""
     g, ws, w = g1
     act1 = synth.activations(g, 1, True, s0=13)
     a1 = dev_act(act1, dev)
@@ -175,10 +177,13 @@ def test_t1_is_row0_of_repeated_rows(dev, g1, rd1):
     run(rd1, w, a8, 8, o8)
     torch.cuda.synchronize()
     for k in ("out", "mean", "lo", "r_out", "rs"):
-        b1 = bits(o1[k])
         b8 = bits(o8[k])
-        for t in range(8):
-            assert np.array_equal(b8[t], b1[0]), f"{k} row {t}"
+        for t in range(1, 8):
+            assert np.array_equal(b8[t], b8[0]), f"{k} row {t}"
+        one = o1[k][0].double().cpu().numpy()
+        eight = o8[k][0].double().cpu().numpy()
+        assert np.max(np.abs(one - eight)) <= 2e-4 * np.max(np.abs(one)), k
+    assert np.array_equal(bits(o8["r_out"])[0], bits(o1["r_out"])[0])
 
 
 def test_argument_errors(dev, g1, rd1):
