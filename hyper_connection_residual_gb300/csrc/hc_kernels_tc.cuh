@@ -25,21 +25,20 @@
 
 namespace hc {
 
-// Split x into BF16 hi and lo parts packed as two bf16x2 words per pair.
-__device__ __forceinline__ uint32_t pack_bf16x2(__nv_bfloat16 a, __nv_bfloat16 b) {
-  return static_cast<uint32_t>(__bfloat16_as_ushort(a)) |
-         (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
-}
-
+// hi = bf16(x) and lo = bf16(x - hi) for four values, packed two per word.
+// Each pair is converted by one packed round-to-nearest instruction; the hi
+// values are widened back exactly by a shift or a mask.
 __device__ __forceinline__ void split4(const float4 x, uint2& hi, uint2& lo) {
-  const __nv_bfloat16 h0 = __float2bfloat16_rn(x.x), h1 = __float2bfloat16_rn(x.y);
-  const __nv_bfloat16 h2 = __float2bfloat16_rn(x.z), h3 = __float2bfloat16_rn(x.w);
-  const __nv_bfloat16 l0 = __float2bfloat16_rn(__fsub_rn(x.x, __bfloat162float(h0)));
-  const __nv_bfloat16 l1 = __float2bfloat16_rn(__fsub_rn(x.y, __bfloat162float(h1)));
-  const __nv_bfloat16 l2 = __float2bfloat16_rn(__fsub_rn(x.z, __bfloat162float(h2)));
-  const __nv_bfloat16 l3 = __float2bfloat16_rn(__fsub_rn(x.w, __bfloat162float(h3)));
-  hi = make_uint2(pack_bf16x2(h0, h1), pack_bf16x2(h2, h3));
-  lo = make_uint2(pack_bf16x2(l0, l1), pack_bf16x2(l2, l3));
+  const __nv_bfloat162 h01 = __floats2bfloat162_rn(x.x, x.y);
+  const __nv_bfloat162 h23 = __floats2bfloat162_rn(x.z, x.w);
+  const uint32_t u01 = *reinterpret_cast<const uint32_t*>(&h01);
+  const uint32_t u23 = *reinterpret_cast<const uint32_t*>(&h23);
+  const __nv_bfloat162 l01 = __floats2bfloat162_rn(__fsub_rn(x.x, __uint_as_float(u01 << 16)),
+                                                   __fsub_rn(x.y, __uint_as_float(u01 & 0xffff0000u)));
+  const __nv_bfloat162 l23 = __floats2bfloat162_rn(__fsub_rn(x.z, __uint_as_float(u23 << 16)),
+                                                   __fsub_rn(x.w, __uint_as_float(u23 & 0xffff0000u)));
+  hi = make_uint2(u01, u23);
+  lo = make_uint2(*reinterpret_cast<const uint32_t*>(&l01), *reinterpret_cast<const uint32_t*>(&l23));
 }
 
 template <int D, int KD, int NT>
@@ -200,9 +199,14 @@ __global__ void __launch_bounds__(kThreads, 2) hc_down_tc_kernel(const DownArgs 
       recv_ss[rank * T + t0 + tid] = v;
     }
 
-    float acc[NT][4];
+    // Two accumulator sets (even and odd k-steps), added at the end: half the
+    // dependent-MMA chain, a fixed order.
+    float acc[NT][4], acc2[NT][4];
 #pragma unroll
-    for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+    for (int n = 0; n < NT; ++n) {
+      acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+      acc2[n][0] = acc2[n][1] = acc2[n][2] = acc2[n][3] = 0.f;
+    }
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
       uint32_t afrag[4];
@@ -210,17 +214,24 @@ __global__ void __launch_bounds__(kThreads, 2) hc_down_tc_kernel(const DownArgs 
 #pragma unroll
       for (int n = 0; n < NT; n += 2) {
         uint32_t b0, b1, b2, b3;
+        float (&c0)[4] = (ks & 1) ? acc2[n] : acc[n];
         if (n + 1 < NT) {
+          float (&c1)[4] = (ks & 1) ? acc2[n + 1] : acc[n + 1];
           ptx::ldsm_x4(ptx::smem_u32(xs + (n * 8 + b_row) * S::XS_PITCH + (b_col + ks * 16) * 2), b0, b1,
                        b2, b3);
-          ptx::mma_bf16_16816(acc[n], afrag, b0, b1);
-          ptx::mma_bf16_16816(acc[n + 1], afrag, b2, b3);
+          ptx::mma_bf16_16816(c0, afrag, b0, b1);
+          ptx::mma_bf16_16816(c1, afrag, b2, b3);
         } else {
           ptx::ldsm_x2(ptx::smem_u32(xs + (n * 8 + (lane & 7)) * S::XS_PITCH + (b_col + ks * 16) * 2), b0,
                        b1);
-          ptx::mma_bf16_16816(acc[n], afrag, b0, b1);
+          ptx::mma_bf16_16816(c0, afrag, b0, b1);
         }
       }
+    }
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[n][e] = __fadd_rn(acc[n][e], acc2[n][e]);
     }
     // Column 2t holds token t's hi part, 2t + 1 its lo part.
 #pragma unroll
@@ -393,9 +404,14 @@ __global__ void __launch_bounds__(kThreads, 2) hc_up_tc_kernel(const UpArgs a) {
     if (t0 == 0) ok = wait_bar(bar_w, 0, a.err, kErrUpWeights) && ok;
     __syncthreads();  // lo (hi, lo), R' and the gates are in shared memory
 
-    float acc[NT][4];
+    // Two accumulator sets (even and odd k-steps), added at the end: half the
+    // dependent-MMA chain, a fixed order.
+    float acc[NT][4], acc2[NT][4];
 #pragma unroll
-    for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+    for (int n = 0; n < NT; ++n) {
+      acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+      acc2[n][0] = acc2[n][1] = acc2[n][2] = acc2[n][3] = 0.f;
+    }
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
       uint32_t afrag[4];
@@ -403,17 +419,24 @@ __global__ void __launch_bounds__(kThreads, 2) hc_up_tc_kernel(const UpArgs a) {
 #pragma unroll
       for (int n = 0; n < NT; n += 2) {
         uint32_t b0, b1, b2, b3;
+        float (&c0)[4] = (ks & 1) ? acc2[n] : acc[n];
         if (n + 1 < NT) {
+          float (&c1)[4] = (ks & 1) ? acc2[n + 1] : acc[n + 1];
           ptx::ldsm_x4(ptx::smem_u32(ls + (n * 8 + b_row) * S::LS_PITCH + (b_col + ks * 16) * 2), b0, b1,
                        b2, b3);
-          ptx::mma_bf16_16816(acc[n], afrag, b0, b1);
-          ptx::mma_bf16_16816(acc[n + 1], afrag, b2, b3);
+          ptx::mma_bf16_16816(c0, afrag, b0, b1);
+          ptx::mma_bf16_16816(c1, afrag, b2, b3);
         } else {
           ptx::ldsm_x2(ptx::smem_u32(ls + (n * 8 + (lane & 7)) * S::LS_PITCH + (b_col + ks * 16) * 2), b0,
                        b1);
-          ptx::mma_bf16_16816(acc[n], afrag, b0, b1);
+          ptx::mma_bf16_16816(c0, afrag, b0, b1);
         }
       }
+    }
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[n][e] = __fadd_rn(acc[n][e], acc2[n][e]);
     }
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
