@@ -21,7 +21,16 @@
 //    applies rs and writes the stream's partial; no global atomics, no last
 //    arriver;
 //  * after its dependency wait, each kernel issues all of its global loads
-//    (R and P, or the partials and R and P) before using any of them.
+//    (R and P, or the partials and R and P) before using any of them;
+//  * independent mode: when the host has established that the read takes
+//    nothing the previous read on the stream writes (it compares address
+//    ranges), the down kernel reads R and P and computes before it waits and
+//    waits only at its end (so its read still completes after the previous
+//    one), and the up kernel fetches R and P before its wait.  Because every
+//    up kernel lets the next read launch only after its own wait has returned,
+//    a read's down kernel starts after the read before the previous one has
+//    completed: the previous read is the only one that can still be running.
+//    Its partial sums go to the other of two scratch slots.
 //
 // Kernel 1, hc_down_kernel (design ancestor: gr_fused_down_kernel in "#2812
 // sycl: STRATA_GR_FUSED=1, the two-kernel BF16 hyper-connection read
@@ -145,6 +154,7 @@ struct DownArgs {
   int T;
   int T_max;
   float eps;
+  int independent;         // 1: no read in flight writes R or P (see below)
 };
 
 struct UpArgs {
@@ -160,7 +170,28 @@ struct UpArgs {
   unsigned* err;
   int T;
   int T_max;
+  int independent;       // 1: no read in flight writes R or P (see below)
 };
+
+// R and P of one token group of this up CTA's rows (64 rows = 16 columns x
+// 4 streams), `EPI` entries per thread.
+template <int D, int EPI>
+__device__ __forceinline__ void load_rp(const UpArgs& a, int c0, int t0, int tg, float (&rr)[EPI],
+                                        float (&pp)[EPI]) {
+  constexpr int ROWS = 4 * 16;
+#pragma unroll
+  for (int m = 0; m < EPI; ++m) {
+    const int idx = threadIdx.x + m * 256;
+    const int t = idx / ROWS, r = idx % ROWS;
+    rr[m] = 0.f;
+    pp[m] = 0.f;
+    if (t < tg) {
+      const size_t off = (size_t)(t0 + t) * (4 * D) + (r / 16) * D + c0 + (r % 16);
+      rr[m] = __ldcg(a.R + off);
+      if (a.P) pp[m] = __ldcg(a.P + off);
+    }
+  }
+}
 
 // Eight BF16 values (one 16-byte chunk) widened to fp32: a BF16 is the upper
 // half of a binary32, so widening is a shift or a mask.
@@ -259,7 +290,10 @@ __global__ void __launch_bounds__(kThreads, 2) hc_down_kernel(const DownArgs a) 
   __syncthreads();  // the mbarriers are initialised before any thread waits on them
   // w_norm is a parameter: wait for it before the previous kernel finishes.
   bool ok = wait_bar(bar_n, 0, a.err, kErrDownNorm);
-  ptx::wait_prerequisites();  // R, P and the scratch belong to the previous kernel until now
+  // R, P and the scratch slot belong to the previous kernel until its end
+  // (in independent mode only the previous read's outputs do, and the down
+  // kernel waits at its end instead).
+  if (!a.independent) ptx::wait_prerequisites();
   ptx::cluster_wait();
 
   // A timed-out wait leaves garbage in shared memory but the CTA still runs
@@ -375,7 +409,10 @@ __global__ void __launch_bounds__(kThreads, 2) hc_down_kernel(const DownArgs a) 
   // One cluster barrier: every slab's pushes are visible to the leader.
   ptx::cluster_arrive_release();
   ptx::cluster_wait();
-  if (rank != 0) return;
+  if (rank != 0) {
+    if (a.independent) ptx::wait_prerequisites();
+    return;
+  }
 
   // Leader: sum the four slabs in slab order, apply rs, write the partial.
   for (int t = tid; t < T; t += kThreads) {
@@ -395,6 +432,7 @@ __global__ void __launch_bounds__(kThreads, 2) hc_down_kernel(const DownArgs a) 
     for (int q = 0; q < G::SLABS_PER_STREAM; ++q) p += recv_p[(q * T + t) * 32 + r];
     __stcg(part + (size_t)t * KD + row0 + r, __fmul_rn(rs_s[t], p));
   }
+  if (a.independent) ptx::wait_prerequisites();  // complete only after the previous read
 }
 
 // ------------------------------------------------------------------ kernel 2
@@ -448,6 +486,10 @@ __global__ void __launch_bounds__(kThreads, 2) hc_up_kernel(const UpArgs a) {
     ok = wait_bar(bar_g, 0, a.err, kErrUpGate);
     sig_s[tid] = 1.0f / (1.0f + expf(-g_s[tid]));
   }
+  // Independent mode: R and P of the first token group do not depend on the
+  // previous read; fetch them before waiting.
+  float rr0[EPI], pp0[EPI];
+  if (a.independent) load_rp<D, EPI>(a, c0, 0, min(TT, a.T), rr0, pp0);
   ptx::wait_prerequisites();  // the partials, R and P are ready from here on
   // Only now may the next read's kernels launch: launching them earlier lets
   // a cascade of waiting CTAs crowd the SMs that are computing this read.
@@ -472,17 +514,14 @@ __global__ void __launch_bounds__(kThreads, 2) hc_up_kernel(const UpArgs a) {
       }
     }
     float rr[EPI], pp[EPI];
+    if (t0 == 0 && a.independent) {
 #pragma unroll
-    for (int m = 0; m < EPI; ++m) {
-      const int idx = tid + m * kThreads;
-      const int t = idx / G::UP_ROWS, r = idx % G::UP_ROWS;
-      rr[m] = 0.f;
-      pp[m] = 0.f;
-      if (t < tg) {
-        const size_t off = (size_t)(t0 + t) * G::N + (r / G::UP_COLS) * D + c0 + (r % G::UP_COLS);
-        rr[m] = __ldcg(a.R + off);
-        if (a.P) pp[m] = __ldcg(a.P + off);
+      for (int m = 0; m < EPI; ++m) {
+        rr[m] = rr0[m];
+        pp[m] = pp0[m];
       }
+    } else {
+      load_rp<D, EPI>(a, c0, t0, tg, rr, pp);
     }
     // lo: the four per-stream partials summed in stream order.
 #pragma unroll

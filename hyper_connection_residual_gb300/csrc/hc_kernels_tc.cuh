@@ -134,7 +134,10 @@ __global__ void __launch_bounds__(kThreads, 2) hc_down_tc_kernel(const DownArgs 
   ptx::launch_dependents();
   __syncthreads();  // the mbarriers are initialised before any thread waits on them
   bool ok = wait_bar(bar_n, 0, a.err, kErrDownNorm);
-  ptx::wait_prerequisites();  // R, P and the scratch belong to the previous kernel until now
+  // R, P and the scratch slot belong to the previous kernel until its end
+  // (in independent mode only the previous read's outputs do, and the down
+  // kernel waits at its end instead).
+  if (!a.independent) ptx::wait_prerequisites();
   ptx::cluster_wait();
 
   // Lane address pattern of an ldmatrix.x4 on a 16x16 A tile.
@@ -257,7 +260,10 @@ __global__ void __launch_bounds__(kThreads, 2) hc_down_tc_kernel(const DownArgs 
   }
   ptx::cluster_arrive_release();
   ptx::cluster_wait();
-  if (rank != 0) return;
+  if (rank != 0) {
+    if (a.independent) ptx::wait_prerequisites();
+    return;
+  }
 
   for (int t = tid; t < T; t += kThreads) {
     float ss = 0.f;
@@ -276,6 +282,7 @@ __global__ void __launch_bounds__(kThreads, 2) hc_down_tc_kernel(const DownArgs 
     for (int q = 0; q < G::SLABS_PER_STREAM; ++q) p += recv_p[(q * T + t) * 32 + r];
     __stcg(part + (size_t)t * KD + row0 + r, __fmul_rn(rs_s[t], p));
   }
+  if (a.independent) ptx::wait_prerequisites();  // complete only after the previous read
 }
 
 // ------------------------------------------------------------------ kernel 2
@@ -331,6 +338,10 @@ __global__ void __launch_bounds__(kThreads, 2) hc_up_tc_kernel(const UpArgs a) {
     ok = wait_bar(bar_g, 0, a.err, kErrUpGate);
     sig_s[tid] = 1.0f / (1.0f + expf(-g_s[tid]));
   }
+  // Independent mode: R and P of the first token group do not depend on the
+  // previous read; fetch them before waiting.
+  float rr0[EPI], pp0[EPI];
+  if (a.independent) load_rp<D, EPI>(a, c0, 0, min(TG, a.T), rr0, pp0);
   ptx::wait_prerequisites();  // the partials, R and P are ready from here on
   ptx::launch_dependents();
 
@@ -359,17 +370,14 @@ __global__ void __launch_bounds__(kThreads, 2) hc_up_tc_kernel(const UpArgs a) {
       }
     }
     float rr[EPI], pp[EPI];
+    if (t0 == 0 && a.independent) {
 #pragma unroll
-    for (int m = 0; m < EPI; ++m) {
-      const int idx = tid + m * kThreads;
-      const int t = idx / G::UP_ROWS, r = idx % G::UP_ROWS;
-      rr[m] = 0.f;
-      pp[m] = 0.f;
-      if (t < tg) {
-        const size_t off = (size_t)(t0 + t) * G::N + (r / G::UP_COLS) * D + c0 + (r % G::UP_COLS);
-        rr[m] = __ldcg(a.R + off);
-        if (a.P) pp[m] = __ldcg(a.P + off);
+      for (int m = 0; m < EPI; ++m) {
+        rr[m] = rr0[m];
+        pp[m] = pp0[m];
       }
+    } else {
+      load_rp<D, EPI>(a, c0, t0, tg, rr, pp);
     }
     // lo (four partials in stream order), its hi/lo split, and this CTA's
     // share of the lo output.

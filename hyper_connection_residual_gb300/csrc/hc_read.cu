@@ -19,8 +19,9 @@ struct hc_read_s {
   float eps;
   void* scratch;
   size_t scratch_bytes;
-  float* part;     // [4][T_max][K] rs-scaled per-stream partials
+  float* part[2];  // two slots of [4][T_max][K] rs-scaled per-stream partials
   unsigned* err;
+  int parity;      // slot of the next read
 };
 
 namespace {
@@ -144,6 +145,63 @@ cudaError_t launch_geometry(int T, const DownArgs& da, const UpArgs& ua, cudaStr
   }
 }
 
+// ---- Which reads may overlap their predecessor.
+// For every (device, stream) the output ranges of the last read enqueued
+// there are kept.  A read whose inputs overlap none of them runs in
+// independent mode.  Work the caller enqueues between two reads is always
+// waited for in full (only kernels of this library trigger their dependents
+// early), so only the previous read matters.
+struct Range {
+  uintptr_t lo, hi;
+};
+
+struct LastRead {
+  int device;
+  void* stream;
+  bool valid;
+  Range outs[5];  // out, mean, lo, r_out, rs
+};
+
+constexpr int kTrackedStreams = 64;
+std::mutex g_track_mutex;
+LastRead g_track[kTrackedStreams];
+unsigned g_track_next;
+
+Range range_of(const void* p, size_t bytes) {
+  const uintptr_t b = reinterpret_cast<uintptr_t>(p);
+  return Range{b, p != nullptr ? b + bytes : b};
+}
+
+// Records this read's outputs for (device, stream); returns whether its inputs
+// are disjoint from the outputs of the previous read recorded there.
+bool record_and_check(int device, void* stream, const Range (&ins)[6], const Range (&outs)[5]) {
+  std::lock_guard<std::mutex> lock(g_track_mutex);
+  LastRead* slot = nullptr;
+  for (auto& e : g_track) {
+    if (e.valid && e.device == device && e.stream == stream) {
+      slot = &e;
+      break;
+    }
+  }
+  bool independent = false;
+  if (slot != nullptr) {
+    independent = true;
+    for (const Range& i : ins) {
+      if (i.lo == i.hi) continue;
+      for (const Range& o : slot->outs) {
+        if (o.lo != o.hi && i.lo < o.hi && o.lo < i.hi) independent = false;
+      }
+    }
+  } else {
+    slot = &g_track[g_track_next++ % kTrackedStreams];
+  }
+  slot->device = device;
+  slot->stream = stream;
+  slot->valid = true;
+  for (int k = 0; k < 5; ++k) slot->outs[k] = outs[k];
+  return independent;
+}
+
 bool geometry_supported(int n, int d, int K) {
   return n == hc::kStreams && ((d == 2560 && K == 320) || (d == 4096 && K == 512));
 }
@@ -176,12 +234,14 @@ HC_EXPORT int hc_read_create(hc_read_t* out, int n, int d, int K, int T_max, flo
     h->eps = eps;
     const size_t part_b = round_up((size_t)n * T_max * K * sizeof(float), 256);
     const size_t err_b = 256;
-    h->scratch_bytes = part_b + err_b;
+    h->scratch_bytes = 2 * part_b + err_b;
     e = cudaMalloc(&h->scratch, h->scratch_bytes);
     if (e == cudaSuccess) {
       char* base = static_cast<char*>(h->scratch);
-      h->part = reinterpret_cast<float*>(base);
-      h->err = reinterpret_cast<unsigned*>(base + part_b);
+      h->part[0] = reinterpret_cast<float*>(base);
+      h->part[1] = reinterpret_cast<float*>(base + part_b);
+      h->err = reinterpret_cast<unsigned*>(base + 2 * part_b);
+      h->parity = 0;
       e = cudaMemset(h->scratch, 0, h->scratch_bytes);
       if (e == cudaSuccess) e = cudaDeviceSynchronize();
     } else {
@@ -215,7 +275,16 @@ HC_EXPORT int hc_read_ex(hc_read_t h, const float* R, const float* w_norm, const
   if (cudaGetDevice(&cur) != cudaSuccess) return HC_ERR_CUDA;
   if (cur != h->device) return HC_ERR_ARG;
 
-  float* part = h->part;
+  const size_t N = (size_t)h->n * h->d;
+  const Range ins[6] = {range_of(R, T * N * 4),        range_of(pending, T * N * 4),
+                        range_of(w_norm, N * 4),        range_of(gate, N * 4),
+                        range_of(W_down, N * h->K * 2), range_of(W_up, N * h->K * 2)};
+  const Range outs[5] = {range_of(out, T * N * 4),  range_of(mean, (size_t)T * h->d * 4),
+                         range_of(lo, (size_t)T * h->K * 4), range_of(r_out, T * N * 4),
+                         range_of(rs, (size_t)T * h->n * 4)};
+  const int independent = record_and_check(cur, stream, ins, outs) ? 1 : 0;
+  float* part = h->part[h->parity];
+  h->parity ^= 1;
 
   DownArgs da;
   da.R = R;
@@ -227,6 +296,7 @@ HC_EXPORT int hc_read_ex(hc_read_t h, const float* R, const float* w_norm, const
   da.rs_out = rs;
   da.T = T;
   da.T_max = h->T_max;
+  da.independent = independent;
   da.eps = h->eps;
 
   UpArgs ua;
@@ -242,6 +312,7 @@ HC_EXPORT int hc_read_ex(hc_read_t h, const float* R, const float* w_norm, const
   ua.err = h->err;
   ua.T = T;
   ua.T_max = h->T_max;
+  ua.independent = independent;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = (h->d == 2560) ? launch_geometry<2560, 320>(T, da, ua, st)
@@ -407,6 +478,18 @@ HC_EXPORT int hc_read_noalloc(int n, int d, int K, float eps, const float* R, co
     cudaGetLastError();
     return HC_ERR_CUDA;
   }
+  // Keep this stream's record of the last read current, so that a later read
+  // that consumes these outputs waits for them.  (This path has one scratch
+  // slot and always waits for the previous kernel before it computes.)
+  const size_t N = (size_t)n * d;
+  const Range ins[6] = {range_of(R, T * N * 4),     range_of(pending, T * N * 4),
+                        range_of(w_norm, N * 4),     range_of(gate, N * 4),
+                        range_of(W_down, N * K * 2), range_of(W_up, N * K * 2)};
+  const Range outs[5] = {range_of(out, T * N * 4), range_of(mean, (size_t)T * d * 4),
+                         range_of(lo, (size_t)T * K * 4), range_of(nullptr, 0),
+                         range_of(nullptr, 0)};
+  record_and_check(dev, stream, ins, outs);
+
   DownArgs da;
   da.R = R;
   da.P = pending;
@@ -417,6 +500,7 @@ HC_EXPORT int hc_read_noalloc(int n, int d, int K, float eps, const float* R, co
   da.rs_out = nullptr;
   da.T = T;
   da.T_max = HC_NOALLOC_MAX_T;
+  da.independent = 0;
   da.eps = eps;
 
   UpArgs ua;
@@ -432,6 +516,7 @@ HC_EXPORT int hc_read_noalloc(int n, int d, int K, float eps, const float* R, co
   ua.err = err;
   ua.T = T;
   ua.T_max = HC_NOALLOC_MAX_T;
+  ua.independent = 0;
 
   cudaError_t e = (d == 2560) ? launch_geometry<2560, 320>(T, da, ua, st)
                               : launch_geometry<4096, 512>(T, da, ua, st);

@@ -30,9 +30,10 @@
  *   mean                   : float  [T][d]
  *   rs                     : float  [T][n]
  *
- * Ownership: the caller owns every tensor.  A handle owns its scratch
- * (per-stream partial sums and an error word), allocated and zeroed by
- * hc_read_create and freed by hc_read_destroy.
+ * Ownership: the caller owns every tensor.  A handle owns its scratch (two
+ * slots of per-stream partial sums, used by consecutive reads in turn, and an
+ * error word), allocated and zeroed by hc_read_create and freed by
+ * hc_read_destroy.
  *
  * Aliasing: out may equal R (in-place update of the residual).  pending must
  * not overlap out; lo, mean, r_out and rs must not overlap any input.
@@ -42,12 +43,15 @@
  * time (the scratch belongs to the handle).  The call can be captured into a
  * CUDA graph; replays give the same bits as direct calls.  The kernels use
  * programmatic dependent launch: each kernel prefetches its BF16 weights,
- * w_norm and gate before it waits for the preceding kernel in the stream, so
- * those four arrays must not be written by a kernel that immediately
- * precedes the read on the stream and itself triggers its dependents early
- * (kernels that do not use programmatic completion, copies and memsets are
- * always waited for in full).  Everything else (R, pending, the outputs, the
- * scratch) is touched only after that wait.
+ * w_norm and gate before it waits for the preceding kernel in the stream.
+ * When the read takes nothing that the previous read enqueued on the same
+ * stream by this library writes (the library compares address ranges), the
+ * read also reads R and pending and computes before that wait, so the two
+ * reads overlap on the GPU; its outputs are still written after the previous
+ * read's.  The inputs of a read must therefore not be written by a kernel
+ * that immediately precedes it on the stream and itself triggers its
+ * dependents early (kernels that do not use programmatic completion, copies
+ * and memsets are always waited for in full).
  *
  * Errors: every entry point returns an hc_status (0 = HC_OK).  Argument errors
  * are detected on the host before anything is enqueued.  HC_ERR_CUDA reports

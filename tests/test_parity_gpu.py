@@ -300,3 +300,47 @@ def test_in_place_chain(dev, orc, rd1):
         err = float(np.max(np.abs(got - ref.out)))
         assert err <= 1e-4 * float(np.max(np.abs(ref.out))), f"in-place read {i}: {err}"
         R_host = R.cpu().numpy()
+
+
+def test_mixed_dependent_and_independent_sequence(dev, orc, rd1):
+    """One stream, one handle: reads that consume the previous read's output
+    (which must wait for it) interleaved with reads that do not (which may
+    overlap it), different T on both kernel families, a shared output buffer.
+    Every read matches the oracle fed with that read's GPU inputs."""
+    g = synth.G1
+    sets = [synth.weight_set(g, 70 + i) for i in range(5)]
+    w = [dev_weights(ws, dev) for ws in sets]
+    act = synth.activations(g, 8, True, s0=71)
+    R0 = torch.from_numpy(act.R).to(dev)
+    P0 = torch.from_numpy(act.P).to(dev)
+    bufs = [torch.zeros(8, g.N, device=dev) for _ in range(4)]
+    # (weights, T, input, output, pending): B ignores A, C consumes B,
+    # D ignores C but rewrites A's output, E consumes D.
+    plan = [(0, 1, R0, bufs[0], None), (1, 4, R0, bufs[1], P0), (2, 4, bufs[1], bufs[2], None),
+            (3, 8, R0, bufs[0], P0), (4, 2, bufs[0], bufs[3], None)]
+    s = torch.cuda.Stream()
+    inputs, outs = [], []
+    with torch.cuda.stream(s):
+        for (j, T, rin, rout, p) in plan:
+            o = outputs(g, T, dev)
+            rd1(rin, w[j]["w_norm"], w[j]["W_down"], w[j]["W_up"], w[j]["gate"], p, T,
+                rout, o["mean"], o["lo"], r_out=o["r_out"], rs=o["rs"], stream=s)
+            outs.append(o)
+            inputs.append(rin)
+    s.synchronize()
+    host_in = {0: act.R, 1: act.R, 3: act.R}
+    host_in[2] = bufs[1].cpu().numpy()
+    host_in[4] = bufs[0].cpu().numpy()
+    for k, (j, T, rin, rout, p) in enumerate(plan):
+        Rk = host_in[k][:T]
+        Pk = act.P[:T] if p is not None else None
+        ref = orc.read(g.n, g.d, g.K, R=Rk, P=Pk, w_norm=sets[j].w_norm, W_down=sets[j].W_down,
+                       W_up=sets[j].W_up, gate=sets[j].gate, eps=EPS)
+        o = dict(outs[k])
+        if k in (1, 2, 4):
+            o["out"] = rout
+        if k == 3:
+            o["out"] = bufs[0]
+        if k == 0:
+            continue  # its output buffer was rewritten by read 3
+        assert_parity(o, ref, T, f"read {k} (T={T})")
