@@ -236,7 +236,7 @@ __device__ __forceinline__ void drain(uint64_t* bar, uint32_t parity) {
 // ------------------------------------------------------------------ kernel 1
 // Grid (16 slabs, K/32 row groups), clusters of 4 along x (one stream).
 template <int D, int KD, int TT>
-__global__ void __launch_bounds__(kThreads, 2) hc_down_kernel(const DownArgs a) {
+__global__ void __launch_bounds__(kThreads, D == 2560 ? 3 : 2) hc_down_kernel(const DownArgs a) {
   using G = Geo<D, KD>;
   using S = DownSmem<D, KD, TT>;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -289,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 2) hc_down_kernel(const DownArgs a) 
   ptx::launch_dependents();
   __syncthreads();  // the mbarriers are initialised before any thread waits on them
   // w_norm is a parameter: wait for it before the previous kernel finishes.
-  bool ok = wait_bar(bar_n, 0, a.err, kErrDownNorm);
+  bool ok = true;
   // R, P and the scratch slot belong to the previous kernel until its end
   // (in independent mode only the previous read's outputs do, and the down
   // kernel waits at its end instead).
@@ -319,6 +319,8 @@ __global__ void __launch_bounds__(kThreads, 2) hc_down_kernel(const DownArgs a) 
         }
       }
     }
+    // w_norm is waited for only now, with this group's R and P loads in flight.
+    if (t0 == 0) ok = wait_bar(bar_n, 0, a.err, kErrDownNorm) && ok;
     float ssl[TT];
 #pragma unroll
     for (int t = 0; t < TT; ++t) {
@@ -437,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 2) hc_down_kernel(const DownArgs a) 
 
 // ------------------------------------------------------------------ kernel 2
 template <int D, int KD, int TT>
-__global__ void __launch_bounds__(kThreads, 2) hc_up_kernel(const UpArgs a) {
+__global__ void __launch_bounds__(kThreads, D == 2560 ? 3 : 2) hc_up_kernel(const UpArgs a) {
   using G = Geo<D, KD>;
   using S = UpSmem<D, KD, TT>;
   constexpr int EPI = (TT * G::UP_ROWS + kThreads - 1) / kThreads;  // epilogue items per thread

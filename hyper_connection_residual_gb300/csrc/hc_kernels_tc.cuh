@@ -83,7 +83,7 @@ struct UpTcSmem {
 // ------------------------------------------------------------------ kernel 1
 // Grid (16 slabs, K/32 row groups), clusters of 4 along x (one stream).
 template <int D, int KD, int NT>
-__global__ void __launch_bounds__(kThreads, 2) hc_down_tc_kernel(const DownArgs a) {
+__global__ void __launch_bounds__(kThreads, D == 2560 ? 3 : 2) hc_down_tc_kernel(const DownArgs a) {
   using G = Geo<D, KD>;
   using S = DownTcSmem<D, KD, NT>;
   constexpr int TG = S::TG;
@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(kThreads, 2) hc_down_tc_kernel(const DownArgs 
   }
   ptx::launch_dependents();
   __syncthreads();  // the mbarriers are initialised before any thread waits on them
-  bool ok = wait_bar(bar_n, 0, a.err, kErrDownNorm);
+  bool ok = true;
   // R, P and the scratch slot belong to the previous kernel until its end
   // (in independent mode only the previous read's outputs do, and the down
   // kernel waits at its end instead).
@@ -163,6 +163,8 @@ __global__ void __launch_bounds__(kThreads, 2) hc_down_tc_kernel(const DownArgs 
         if (a.P) pv[t] = __ldcg(reinterpret_cast<const float4*>(a.P + base) + c4);
       }
     }
+    // w_norm is waited for only now, with this group's R and P loads in flight.
+    if (t0 == 0) ok = wait_bar(bar_n, 0, a.err, kErrDownNorm) && ok;
     float ssl[TG];
 #pragma unroll
     for (int t = 0; t < TG; ++t) {
@@ -287,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 2) hc_down_tc_kernel(const DownArgs 
 
 // ------------------------------------------------------------------ kernel 2
 template <int D, int KD, int NT>
-__global__ void __launch_bounds__(kThreads, 2) hc_up_tc_kernel(const UpArgs a) {
+__global__ void __launch_bounds__(kThreads, D == 2560 ? 3 : 2) hc_up_tc_kernel(const UpArgs a) {
   using G = Geo<D, KD>;
   using S = UpTcSmem<D, KD, NT>;
   constexpr int TG = S::TG;

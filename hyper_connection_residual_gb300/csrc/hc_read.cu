@@ -82,13 +82,6 @@ template <int D, int KD>
 cudaError_t configure_geometry() {
   cudaError_t e;
   if ((e = configure_one<D, KD, 1>()) != cudaSuccess) return e;
-  if ((e = configure_one<D, KD, 2>()) != cudaSuccess) return e;
-  if ((e = configure_one<D, KD, 3>()) != cudaSuccess) return e;
-  if ((e = configure_one<D, KD, 4>()) != cudaSuccess) return e;
-  if ((e = configure_one<D, KD, 5>()) != cudaSuccess) return e;
-  if ((e = configure_one<D, KD, 6>()) != cudaSuccess) return e;
-  if ((e = configure_one<D, KD, 7>()) != cudaSuccess) return e;
-  if ((e = configure_one<D, KD, 8>()) != cudaSuccess) return e;
   if ((e = configure_tc<D, KD, 1>()) != cudaSuccess) return e;
   return configure_tc<D, KD, 2>();
 }
@@ -126,23 +119,10 @@ cudaError_t launch_pair_tc(const DownArgs& da, const UpArgs& ua, cudaStream_t st
 // From T = 2 on the tensor-core kernels are faster on GB300 (measured: T=2
 // 6.1 vs 6.7 us, T=8 7.9 vs 11.1 us per read); at T = 1 the CUDA-core kernels
 // are (5.2 vs 6.0 us): the MMA path stages four tokens there.
-constexpr int kTcMinT = 2;
-
 template <int D, int KD>
 cudaError_t launch_geometry(int T, const DownArgs& da, const UpArgs& ua, cudaStream_t st) {
-  if (T >= kTcMinT) {
-    return T <= 4 ? launch_pair_tc<D, KD, 1>(da, ua, st) : launch_pair_tc<D, KD, 2>(da, ua, st);
-  }
-  switch (T) {
-    case 1: return launch_pair<D, KD, 1>(da, ua, st);
-    case 2: return launch_pair<D, KD, 2>(da, ua, st);
-    case 3: return launch_pair<D, KD, 3>(da, ua, st);
-    case 4: return launch_pair<D, KD, 4>(da, ua, st);
-    case 5: return launch_pair<D, KD, 5>(da, ua, st);
-    case 6: return launch_pair<D, KD, 6>(da, ua, st);
-    case 7: return launch_pair<D, KD, 7>(da, ua, st);
-    default: return launch_pair<D, KD, 8>(da, ua, st);  // groups of 8 tokens
-  }
+  if (T == 1) return launch_pair<D, KD, 1>(da, ua, st);
+  return T <= 4 ? launch_pair_tc<D, KD, 1>(da, ua, st) : launch_pair_tc<D, KD, 2>(da, ua, st);
 }
 
 // ---- Which reads may overlap their predecessor.
