@@ -22,8 +22,11 @@ from ._binding import (  # noqa: F401
     hc_graph_end,
     hc_graph_launch,
     hc_read,
+    hc_read_batch,
+    hc_read_batch_persistent,
     hc_read_check,
     hc_read_create,
+    hc_read_desc,
     hc_read_destroy,
     hc_read_ex,
     hc_read_noalloc,

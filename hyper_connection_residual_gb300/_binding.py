@@ -22,8 +22,14 @@ EXPORTS = (
     "hc_read_create", "hc_read", "hc_read_ex", "hc_read_check", "hc_read_reset",
     "hc_read_destroy", "hc_read_scratch_bytes", "hc_status_str",
     "hc_graph_begin", "hc_graph_end", "hc_graph_launch", "hc_graph_destroy",
-    "hc_read_noalloc",
+    "hc_read_noalloc", "hc_read_batch", "hc_read_batch_persistent",
 )
+
+
+class hc_read_desc(ctypes.Structure):
+    """One read of hc_read_batch (field order of the C struct)."""
+    _fields_ = [(name, ctypes.c_void_p) for name in (
+        "R", "w_norm", "W_down", "W_up", "gate", "pending", "out", "mean", "lo")]
 
 
 class HcError(RuntimeError):
@@ -79,6 +85,10 @@ def load(path: str | None = None):
     lib.hc_read_noalloc.restype = ctypes.c_int
     lib.hc_read_noalloc.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float] + \
         [_vp] * 6 + [ctypes.c_int] + [_vp] * 4
+    lib.hc_read_batch.restype = ctypes.c_int
+    lib.hc_read_batch.argtypes = [_vp, ctypes.POINTER(hc_read_desc), ctypes.c_int, ctypes.c_int, _vp]
+    lib.hc_read_batch_persistent.restype = ctypes.c_int
+    lib.hc_read_batch_persistent.argtypes = [_vp, ctypes.c_int]
     if path is None:
         _lib = lib
     return lib
@@ -190,6 +200,34 @@ def hc_read_noalloc(geometry, eps, R, w_norm, W_down, W_up, gate, pending, T: in
            "hc_read_noalloc")
 
 
+def hc_read_batch(h: int, geometry, reads, T: int, stream=None) -> None:
+    """Enqueue a list of reads in order (see include/hc_read.h).
+
+    ``reads``: sequence of dicts with keys R, w_norm, W_down, W_up, gate,
+    pending (or P; may be None), out, mean, lo.  A read whose R is the
+    previous read's out tensor is chained."""
+    n, d, K = geometry
+    N = n * d
+    arr = (hc_read_desc * len(reads))()
+    for i, r in enumerate(reads):
+        pend = r.get("pending", r.get("P"))
+        arr[i] = hc_read_desc(
+            _ptr(r["R"], "R", _F32, T * N), _ptr(r["w_norm"], "w_norm", _F32, N),
+            _ptr(r["W_down"], "W_down", _BF16, K * N), _ptr(r["W_up"], "W_up", _BF16, N * K),
+            _ptr(r["gate"], "gate", _F32, N), _ptr(pend, "pending", _F32, T * N),
+            _ptr(r["out"], "out", _F32, T * N), _ptr(r["mean"], "mean", _F32, T * d),
+            _ptr(r["lo"], "lo", _F32, T * K))
+    _check(load().hc_read_batch(h, arr, len(reads), T, _stream_ptr(stream)), "hc_read_batch")
+
+
+def hc_read_batch_persistent(h: int, T: int) -> bool:
+    """Whether batches of T-token reads run as the persistent kernel."""
+    st = load().hc_read_batch_persistent(h, T)
+    if st < 0:
+        _check(st, "hc_read_batch_persistent")
+    return st == 1
+
+
 def hc_read_check(h: int) -> int:
     """HC_OK or HC_ERR_TIMEOUT (synchronises the device)."""
     st = load().hc_read_check(h)
@@ -241,6 +279,13 @@ class Read:
                  r_out=None, rs=None, stream=None) -> None:
         hc_read_ex(self.h, self.geometry, R, w_norm, W_down, W_up, gate, pending, T,
                    out, mean, lo, r_out, rs, stream)
+
+    def batch(self, reads, T: int, stream=None) -> None:
+        """Enqueue a list of reads (dicts, see hc_read_batch) in order."""
+        hc_read_batch(self.h, self.geometry, reads, T, stream)
+
+    def batch_persistent(self, T: int) -> bool:
+        return hc_read_batch_persistent(self.h, T)
 
     def check(self) -> int:
         return hc_read_check(self.h)

@@ -11,6 +11,7 @@
 #include "hc_kernels.cuh"
 #include "hc_kernels_tc.cuh"
 #include "hc_read.h"
+#include "hc_window.cuh"
 
 #define HC_EXPORT extern "C" __attribute__((visibility("default")))
 
@@ -22,6 +23,15 @@ struct hc_read_s {
   float* part[2];  // two slots of [4][T_max][K] rs-scaled per-stream partials
   unsigned* err;
   int parity;      // slot of the next read
+  // Persistent multi-read kernel (d = 2560, K = 320 only): exchange packets,
+  // published output tiles, per-CTA epoch bases, abort word.
+  bool window;     // the kernel's 128 CTAs fit co-resident on this device
+  unsigned* xbuf;
+  unsigned* xss;
+  unsigned* mbuf;
+  unsigned* gen;
+  size_t window_bytes;  // xbuf, mbuf, gen, abort word: zeroed by hc_read_reset
+  unsigned* abort_flag;
 };
 
 namespace {
@@ -182,6 +192,56 @@ bool record_and_check(int device, void* stream, const Range (&ins)[6], const Ran
   return independent;
 }
 
+// ---- Persistent multi-read kernel (hc_window.cuh), d = 2560, K = 320, T <= 4.
+using WinG1 = hc::WinGeo<2560, 320, 1>;
+constexpr size_t kXbufWords = (size_t)2 * hc::kWinCluster * (hc::kWinCtas / hc::kWinCluster) *
+                              hc::kWinTmaxAlloc * WinG1::KQ;
+constexpr size_t kXssWords = (size_t)2 * hc::kWinTmaxAlloc * (hc::kWinCtas / hc::kWinCluster) * 2;
+constexpr size_t kMbufWords = (size_t)2 * hc::kStreams * hc::kWinTmaxAlloc * 2560;
+
+cudaLaunchConfig_t window_config(cudaStream_t st, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(hc::kWinCtas);
+  cfg.blockDim = dim3(WinG1::THREADS);
+  cfg.dynamicSmemBytes = WinG1::BYTES;
+  cfg.stream = st;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = hc::kWinCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  // The CTAs wait on one another: they must all be resident at once.
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
+  attr[2].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[2].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 3;
+  return cfg;
+}
+
+// Whether the current device can hold the window kernel's 32 clusters of
+// four CTAs (one CTA per SM) at once.
+bool window_fits() {
+  if (cudaFuncSetAttribute(hc::hc_window_kernel<2560, 320, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           WinG1::BYTES) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  cudaLaunchAttribute attr[3];
+  cudaLaunchConfig_t cfg = window_config(nullptr, attr);
+  cfg.numAttrs = 1;  // the cluster shape only
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, hc::hc_window_kernel<2560, 320, 1>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return clusters >= hc::kWinCtas / hc::kWinCluster;
+}
+
+bool overlaps(const Range& a, const Range& b) {
+  return a.lo != a.hi && b.lo != b.hi && a.lo < b.hi && b.lo < a.hi;
+}
+
 bool geometry_supported(int n, int d, int K) {
   return n == hc::kStreams && ((d == 2560 && K == 320) || (d == 4096 && K == 512));
 }
@@ -214,7 +274,12 @@ HC_EXPORT int hc_read_create(hc_read_t* out, int n, int d, int K, int T_max, flo
     h->eps = eps;
     const size_t part_b = round_up((size_t)n * T_max * K * sizeof(float), 256);
     const size_t err_b = 256;
-    h->scratch_bytes = 2 * part_b + err_b;
+    h->window = d == 2560 && window_fits();
+    const size_t xbuf_b = h->window ? round_up(kXbufWords * 4, 256) : 0;
+    const size_t xss_b = h->window ? round_up(kXssWords * 4, 256) : 0;
+    const size_t mbuf_b = h->window ? round_up(kMbufWords * 4, 256) : 0;
+    const size_t gen_b = h->window ? round_up(hc::kWinCtas * sizeof(unsigned), 256) + 256 : 0;
+    h->scratch_bytes = 2 * part_b + err_b + xbuf_b + xss_b + mbuf_b + gen_b;
     e = cudaMalloc(&h->scratch, h->scratch_bytes);
     if (e == cudaSuccess) {
       char* base = static_cast<char*>(h->scratch);
@@ -222,6 +287,15 @@ HC_EXPORT int hc_read_create(hc_read_t* out, int n, int d, int K, int T_max, flo
       h->part[1] = reinterpret_cast<float*>(base + part_b);
       h->err = reinterpret_cast<unsigned*>(base + 2 * part_b);
       h->parity = 0;
+      // Window state, contiguous (hc_read_reset zeroes it in one go):
+      // xbuf | xss | mbuf | gen[128] | abort word.
+      char* wb = base + 2 * part_b + err_b;
+      h->window_bytes = xbuf_b + xss_b + mbuf_b + gen_b;
+      h->xbuf = h->window ? reinterpret_cast<unsigned*>(wb) : nullptr;
+      h->xss = h->window ? reinterpret_cast<unsigned*>(wb + xbuf_b) : nullptr;
+      h->mbuf = h->window ? reinterpret_cast<unsigned*>(wb + xbuf_b + xss_b) : nullptr;
+      h->gen = h->window ? reinterpret_cast<unsigned*>(wb + xbuf_b + xss_b + mbuf_b) : nullptr;
+      h->abort_flag = h->window ? reinterpret_cast<unsigned*>(wb + h->window_bytes - 256) : nullptr;
       e = cudaMemset(h->scratch, 0, h->scratch_bytes);
       if (e == cudaSuccess) e = cudaDeviceSynchronize();
     } else {
@@ -311,6 +385,100 @@ HC_EXPORT int hc_read(hc_read_t h, const float* R, const float* w_norm, const ui
                     stream);
 }
 
+namespace {
+
+// One launch of the persistent kernel over descs[0..count) (count <= kWinMaxReads).
+int launch_window(hc_read_t h, const hc_read_desc* descs, int count, int T, cudaStream_t st) {
+  hc::WinArgs* a = new (std::nothrow) hc::WinArgs();
+  if (a == nullptr) return HC_ERR_ARG;
+  a->xbuf = h->xbuf;
+  a->xss = h->xss;
+  a->mbuf = h->mbuf;
+  a->gen = h->gen;
+  a->abort_flag = h->abort_flag;
+  a->err = h->err;
+  a->count = count;
+  a->T = T;
+  a->eps = h->eps;
+  for (int j = 0; j < count; ++j) {
+    const hc_read_desc& d = descs[j];
+    a->rd[j] = hc::WinRead{d.R, d.pending, d.w_norm, d.W_down, d.W_up, d.gate, d.out, d.mean, d.lo};
+    a->chained[j] = (j > 0 && d.R == descs[j - 1].out) ? 1 : 0;
+  }
+  cudaLaunchAttribute attr[3];
+  cudaLaunchConfig_t cfg = window_config(st, attr);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, hc::hc_window_kernel<2560, 320, 1>, *a);
+  delete a;
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return HC_ERR_CUDA;
+  }
+  return HC_OK;
+}
+
+}  // namespace
+
+HC_EXPORT int hc_read_batch_persistent(hc_read_t h, int T) {
+  if (h == nullptr || T < 1 || T > h->T_max) return HC_ERR_ARG;
+  return (h->window && T <= 4) ? 1 : 0;
+}
+
+HC_EXPORT int hc_read_batch(hc_read_t h, const hc_read_desc* descs, int count, int T, hc_stream_t stream) {
+  if (h == nullptr || descs == nullptr || count < 1) return HC_ERR_ARG;
+  if (T < 1 || T > h->T_max) return HC_ERR_ARG;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return HC_ERR_CUDA;
+  if (cur != h->device) return HC_ERR_ARG;
+  const size_t N = (size_t)h->n * h->d;
+  for (int j = 0; j < count; ++j) {
+    const hc_read_desc& d = descs[j];
+    if (!d.R || !d.w_norm || !d.W_down || !d.W_up || !d.gate || !d.out || !d.mean || !d.lo) return HC_ERR_ARG;
+    const void* ptrs[] = {d.R, d.w_norm, d.W_down, d.W_up, d.gate, d.pending, d.out, d.mean, d.lo};
+    for (const void* p : ptrs) {
+      if (p != nullptr && !aligned16(p)) return HC_ERR_ALIGN;
+    }
+    const Range p_in = range_of(d.pending, T * N * 4);
+    if (overlaps(p_in, range_of(d.out, T * N * 4))) return HC_ERR_ARG;
+    // Inputs may not depend on earlier reads of the batch, except R taking
+    // the previous read's out exactly (a chained read, whose R is never
+    // loaded: it is the previous read's output tile, still on chip).
+    const bool chained = j > 0 && d.R == descs[j - 1].out;
+    const Range r_in = chained ? range_of(nullptr, 0) : range_of(d.R, T * N * 4);
+    for (int i = 0; i < j; ++i) {
+      const hc_read_desc& o = descs[i];
+      const Range outs[3] = {range_of(o.out, T * N * 4), range_of(o.mean, (size_t)T * h->d * 4),
+                             range_of(o.lo, (size_t)T * h->K * 4)};
+      for (int k = 0; k < 3; ++k) {
+        if (overlaps(r_in, outs[k]) || overlaps(p_in, outs[k])) return HC_ERR_ARG;
+      }
+    }
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (hc_read_batch_persistent(h, T) != 1) {
+    // Shapes the persistent kernel does not cover: the reads one by one.
+    for (int j = 0; j < count; ++j) {
+      const hc_read_desc& d = descs[j];
+      const int r = hc_read_ex(h, d.R, d.w_norm, d.W_down, d.W_up, d.gate, d.pending, T, d.out, d.mean, d.lo,
+                               nullptr, nullptr, stream);
+      if (r != HC_OK) return r;
+    }
+    return HC_OK;
+  }
+  for (int j0 = 0; j0 < count; j0 += hc::kWinMaxReads) {
+    const int r = launch_window(h, descs + j0, count - j0 < hc::kWinMaxReads ? count - j0 : hc::kWinMaxReads, T, st);
+    if (r != HC_OK) return r;
+  }
+  // A later hc_read that consumes the last read's outputs must wait for them.
+  const hc_read_desc& last = descs[count - 1];
+  const Range ins[6] = {range_of(last.R, T * N * 4),         range_of(last.pending, T * N * 4),
+                        range_of(last.w_norm, N * 4),         range_of(last.gate, N * 4),
+                        range_of(last.W_down, N * h->K * 2), range_of(last.W_up, N * h->K * 2)};
+  const Range outs[5] = {range_of(last.out, T * N * 4), range_of(last.mean, (size_t)T * h->d * 4),
+                         range_of(last.lo, (size_t)T * h->K * 4), range_of(nullptr, 0), range_of(nullptr, 0)};
+  record_and_check(cur, stream, ins, outs);
+  return HC_OK;
+}
+
 HC_EXPORT int hc_read_check(hc_read_t h) {
   if (h == nullptr) return HC_ERR_ARG;
   int prev = -1;
@@ -331,6 +499,8 @@ HC_EXPORT int hc_read_reset(hc_read_t h, hc_stream_t stream) {
   if (cur != h->device) return HC_ERR_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(h->err, 0, sizeof(unsigned), st);
+  // The persistent kernel's exchange words, epoch bases and abort word start over.
+  if (e == cudaSuccess && h->xbuf != nullptr) e = cudaMemsetAsync(h->xbuf, 0, h->window_bytes, st);
   return e == cudaSuccess ? HC_OK : HC_ERR_CUDA;
 }
 

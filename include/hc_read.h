@@ -104,6 +104,46 @@ int hc_read_ex(hc_read_t h, const float* R, const float* w_norm, const uint16_t*
                float* out, float* mean, float* lo, float* r_out, float* rs,
                hc_stream_t stream);
 
+/* One read of a batch: the arguments of hc_read, same meaning and layouts. */
+typedef struct {
+  const float* R;
+  const float* w_norm;
+  const uint16_t* W_down;
+  const uint16_t* W_up;
+  const float* gate;
+  const float* pending;  /* NULL = no pending write */
+  float* out;
+  float* mean;
+  float* lo;
+} hc_read_desc;
+
+/* Enqueue `count` reads of T tokens each on `stream`, in order: the reads of a
+ * verify window (the pages' engine runs 96 per window, one per layer; Strata
+ * pull request #2070, first paragraph), or any list of reads.
+ *
+ * Read j may take as R the previous read's out (the same pointer): a chained
+ * read, whose input then never leaves the chip.  Otherwise R and pending of
+ * read j must not overlap an output (out, mean, lo) of an earlier read of the
+ * batch, and pending must not overlap the read's own out (HC_ERR_ARG).  Each
+ * read's outputs are those of hc_read with the same arguments; reads may
+ * reuse one set of output buffers.  `descs` is host memory, read during the
+ * call only.
+ *
+ * For (d, K) = (2560, 320) and T <= 4 on a device that can hold it, the batch
+ * runs as one persistent kernel per 224 reads: 128 CTAs, one per SM, that
+ * must all be resident at once (a cooperative launch).  Do not run two such
+ * batches at the same time on one device (two streams or two threads): a
+ * kernel that cannot get its 128 SMs gives up after its bounded waits and
+ * reports HC_ERR_TIMEOUT through hc_read_check.  Other shapes run read by
+ * read as hc_read does.  hc_read_reset also clears the persistent kernel's
+ * abort word; its exchange state needs no reset. */
+int hc_read_batch(hc_read_t h, const hc_read_desc* descs, int count, int T, hc_stream_t stream);
+
+/* 1 if hc_read_batch on this handle runs batches of T-token reads as the
+ * persistent kernel, 0 if it runs them read by read; HC_ERR_ARG for a NULL
+ * handle or T outside 1..T_max. */
+int hc_read_batch_persistent(hc_read_t h, int T);
+
 /* Synchronise with the handle's device and report the kernels' error word:
  * HC_OK, or HC_ERR_TIMEOUT if any kernel gave up on a bounded wait since the
  * last hc_read_reset. */
