@@ -28,6 +28,7 @@ from ._binding import (  # noqa: F401
     hc_read_create,
     hc_read_desc,
     hc_read_destroy,
+    hc_read_error_word,
     hc_read_ex,
     hc_read_noalloc,
     hc_read_reset,

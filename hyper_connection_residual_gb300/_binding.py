@@ -22,7 +22,7 @@ EXPORTS = (
     "hc_read_create", "hc_read", "hc_read_ex", "hc_read_check", "hc_read_reset",
     "hc_read_destroy", "hc_read_scratch_bytes", "hc_status_str",
     "hc_graph_begin", "hc_graph_end", "hc_graph_launch", "hc_graph_destroy",
-    "hc_read_noalloc", "hc_read_batch", "hc_read_batch_persistent",
+    "hc_read_noalloc", "hc_read_batch", "hc_read_batch_persistent", "hc_read_error_word",
 )
 
 
@@ -87,6 +87,8 @@ def load(path: str | None = None):
         [_vp] * 6 + [ctypes.c_int] + [_vp] * 4
     lib.hc_read_batch.restype = ctypes.c_int
     lib.hc_read_batch.argtypes = [_vp, ctypes.POINTER(hc_read_desc), ctypes.c_int, ctypes.c_int, _vp]
+    lib.hc_read_error_word.restype = ctypes.c_int64
+    lib.hc_read_error_word.argtypes = [_vp]
     lib.hc_read_batch_persistent.restype = ctypes.c_int
     lib.hc_read_batch_persistent.argtypes = [_vp, ctypes.c_int]
     if path is None:
@@ -236,6 +238,14 @@ def hc_read_check(h: int) -> int:
     return st
 
 
+def hc_read_error_word(h: int) -> int:
+    """The raw error word (synchronises the device); bits in include/hc_read.h."""
+    w = int(load().hc_read_error_word(h))
+    if w < 0:
+        _check(w, "hc_read_error_word")
+    return w
+
+
 def hc_read_reset(h: int, stream=None) -> None:
     _check(load().hc_read_reset(h, _stream_ptr(stream)), "hc_read_reset")
 
@@ -289,6 +299,9 @@ class Read:
 
     def check(self) -> int:
         return hc_read_check(self.h)
+
+    def error_word(self) -> int:
+        return hc_read_error_word(self.h)
 
     def reset(self, stream=None) -> None:
         hc_read_reset(self.h, stream)

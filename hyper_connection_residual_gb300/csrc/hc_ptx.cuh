@@ -97,6 +97,16 @@ __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// The same cluster barrier halves without .aligned: threads of a warp may
+// arrive after divergent code (the .aligned forms need the whole warp to
+// execute the instruction together, which no CTA-wide barrier guarantees).
+__device__ __forceinline__ void cluster_arrive_release_any() {
+  asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_any() {
+  asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+
 // ldmatrix: four (or two) 8x8 b16 matrices from shared memory; lane i
 // supplies the row address of matrix i/8.
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,

@@ -194,10 +194,10 @@ bool record_and_check(int device, void* stream, const Range (&ins)[6], const Ran
 
 // ---- Persistent multi-read kernel (hc_window.cuh), d = 2560, K = 320, T <= 4.
 using WinG1 = hc::WinGeo<2560, 320, 1>;
-constexpr size_t kXbufWords = (size_t)2 * hc::kWinCluster * (hc::kWinCtas / hc::kWinCluster) *
+constexpr size_t kXbufWords = (size_t)hc::kWinXSlots * hc::kWinCluster * (hc::kWinCtas / hc::kWinCluster) *
                               hc::kWinTmaxAlloc * WinG1::KQ;
-constexpr size_t kXssWords = (size_t)2 * hc::kWinTmaxAlloc * (hc::kWinCtas / hc::kWinCluster) * 2;
-constexpr size_t kMbufWords = (size_t)2 * hc::kStreams * hc::kWinTmaxAlloc * 2560;
+constexpr size_t kXssWords = (size_t)hc::kWinXSlots * hc::kWinTmaxAlloc * (hc::kWinCtas / hc::kWinCluster) * 2;
+constexpr size_t kMbufWords = (size_t)hc::kWinXSlots * hc::kStreams * hc::kWinTmaxAlloc * 2560;
 
 cudaLaunchConfig_t window_config(cudaStream_t st, cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
@@ -490,6 +490,19 @@ HC_EXPORT int hc_read_check(hc_read_t h) {
   cudaSetDevice(prev);
   if (e != cudaSuccess) return HC_ERR_CUDA;
   return word == 0 ? HC_OK : HC_ERR_TIMEOUT;
+}
+
+HC_EXPORT int64_t hc_read_error_word(hc_read_t h) {
+  if (h == nullptr) return HC_ERR_ARG;
+  int prev = -1;
+  if (cudaGetDevice(&prev) != cudaSuccess) return HC_ERR_CUDA;
+  if (cudaSetDevice(h->device) != cudaSuccess) return HC_ERR_CUDA;
+  unsigned word = 0;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(&word, h->err, sizeof word, cudaMemcpyDeviceToHost);
+  cudaSetDevice(prev);
+  if (e != cudaSuccess) return HC_ERR_CUDA;
+  return static_cast<int64_t>(word);
 }
 
 HC_EXPORT int hc_read_reset(hc_read_t h, hc_stream_t stream) {

@@ -18,28 +18,32 @@
 //   * cluster reduce-scatter over distributed shared memory (st.async with
 //     mbarrier transaction counts): rank r of the cluster receives the four
 //     CTAs' partials for k in its quarter of K and sums them;
-//   * global exchange through L2 with self-tagged words: the two low mantissa
-//     bits of every exchanged fp32 value carry the read's epoch modulo 4 (a
-//     relative change below 2^-21), so a reader polls the data itself, 16 bytes
-//     at a time, and needs no separate flag, fence or second round trip.  An
-//     aligned 4-byte access is single-copy atomic, so a word is either old or
-//     new, never torn.  Rank r of every cluster reads its quarter of K from all
-//     32 clusters, sums the 8 clusters of each stream, forms rs per stream from
-//     the exchanged sums of squares and lo = sum_s rs_s * S_s;
+//   * global exchange through L2 with self-tagged words: the three low
+//     mantissa bits of every exchanged fp32 value carry the read's epoch
+//     modulo 8 (a relative change below 2^-20), so a reader polls the data
+//     itself, 16 bytes at a time, and needs no separate flag, fence or second
+//     round trip.  Words are written by 8-byte strong stores, which are
+//     single-copy atomic, so a word is either old or new, never torn.  Rank r
+//     of every cluster reads its quarter of K from all 32 clusters, sums the 8
+//     clusters of each stream, forms rs per stream from the exchanged sums of
+//     squares and lo = sum_s rs_s * S_s;
 //   * cluster all-gather of lo (split into BF16 hi/lo terms) over distributed
-//     shared memory, then the up projection and the epilogue on tensor cores;
+//     shared memory, then the up projection (one warp per 16 rows of W_up
+//     over the whole K) on tensor cores, with the epilogue taken straight
+//     from the accumulators;
 //   * the stream mean needs the four streams of a column, which live in four
 //     clusters: each CTA publishes its output tile as tagged words and
 //     computes the mean of its quarter of the columns one read later; those
 //     loads are issued with the next read's exchange loads and are long
 //     written by then.
 //
-// Tag safety: every read rewrites every slot of its parity, all 8 token rows
-// whatever T is (rows of tokens >= T carry zeros), so a stale word is always
-// from the read two earlier (epoch - 2, a different tag); all CTAs are within
-// one read of each other.  Buffers start zeroed and epochs at 1, so the first
-// use of each slot (epochs 1 and 2) cannot match a zero tag.  hc_read_reset
-// zeroes the buffers and the epoch bases again.
+// Tag safety: exchange buffers have four slots (epoch mod 4), and every read
+// rewrites all 8 token rows of its slot whatever T is (rows of tokens >= T
+// carry zeros), so a stale word is from epoch - 4 at the oldest, which carries
+// another tag; all CTAs are within one read of each other.  Buffers start
+// zeroed and epochs at 1, so the first use of each slot (epochs 1..4) cannot
+// match a zero tag.  hc_read_reset zeroes the buffers and the epoch bases
+// again.
 //
 // Every sum runs in a fixed order, so repeated launches and graph replays give
 // identical bits.  All waits are bounded (kWaitNs) and also give up once any
@@ -63,6 +67,7 @@ constexpr int kWinMaxReads = 224;  // reads per launch (kernel parameter space)
 constexpr int kWinCtas = 128;
 constexpr int kWinCluster = 4;
 constexpr int kWinTmaxAlloc = 8;   // exchange buffers are sized for T <= 8
+constexpr int kWinXSlots = 4;      // exchange slots (epoch mod 4)
 
 // Error bits of the window kernel.
 constexpr unsigned kErrWinFull = 16u;      // weight tiles did not land
@@ -130,8 +135,6 @@ struct WinGeo {
   static constexpr int DN_KS = W / 16;                      // down k-steps
   static constexpr int MT_PER_Q = KQ / 16;                  // down m16 tiles per rank quarter
   static constexpr int UP_MT = W / 16;                      // up m16 tiles (rows of W_up)
-  static constexpr int UP_KSPLIT = NCW / UP_MT;
-  static constexpr int UP_KS = KD / 16 / UP_KSPLIT;         // up k-steps per warp
   // One ring entry: everything a read takes from HBM.
   static constexpr int E_WD = 0;
   static constexpr int E_WU = E_WD + KD * WD_ROWB;
@@ -146,22 +149,20 @@ struct WinGeo {
   static constexpr int XS = ENT + 2 * ENT_BYTES;             // [8 NT][W] bf16: x hi/lo rows
   static constexpr int LS = XS + 8 * NT * XS_PITCH;          // [8 NT][K] bf16: lo hi/lo rows
   static constexpr int RP = LS + 8 * NT * LS_PITCH;          // [TMAX][W] R', then out
-  static constexpr int SIG = RP + TMAX * W * 4;              // [W] sigmoid(gate)
-  static constexpr int RECV = SIG + W * 4;                   // see RECV_BYTES
+  static constexpr int RECV = RP + TMAX * W * 4;             // see RECV_BYTES
   static constexpr int RECV_PART = CL * TMAX * KQ * 4;       // [CL src][TMAX][KQ] partials
   static constexpr int RECV_SS = RECV_PART;                  // then [CL src][TMAX] ss
   static constexpr int SUMS_BYTES = kStreams * TMAX * XW * 4;  // exchange sums [4][TMAX][XW]
   static constexpr int RECV_BYTES =
       (RECV_PART + CL * TMAX * 4) > SUMS_BYTES ? (RECV_PART + CL * TMAX * 4) : SUMS_BYTES;
-  static constexpr int RED = RECV + RECV_BYTES;              // [UP_KSPLIT][TMAX][W]
-  static constexpr int BYTES = RED + UP_KSPLIT * TMAX * W * 4;
+  static constexpr int BYTES = RECV + RECV_BYTES;
   // Transaction bytes per read at each cluster rank.
   __host__ __device__ static constexpr int rs_bytes(int T) { return CL * (T * KQ * 4 + T * 4); }
   __host__ __device__ static constexpr int lo_bytes(int T) { return CL * T * KQ * 4; }
 
   static_assert(kWinCtas % (kStreams * CL) == 0, "clusters must not straddle streams");
   static_assert(DN_MT % NCW == 0 && KQ % 16 == 0, "down tiles must split over warps and ranks");
-  static_assert(NCW % UP_MT == 0 && (KD / 16) % UP_KSPLIT == 0, "up tiles must split over warps");
+  static_assert(UP_MT <= NCW, "one warp per up m16 tile");
   static_assert(W % 16 == 0 && W / 4 <= 32, "column slab must be whole k-steps, one warp per token");
   static_assert(WD_CH % 4 == 2, "W_down swizzle assumes a row of 2 (mod 4) chunks");
   static_assert(WU_CH % 8 == 0, "W_up swizzle assumes a row of a multiple of 8 chunks");
@@ -231,14 +232,14 @@ __device__ __forceinline__ void st_async(uint32_t addr, uint32_t v, uint32_t bar
 }
 
 // Self-tagged exchange words: fp32 bits with the two low mantissa bits
-// replaced by the epoch modulo 4.
+// replaced by the epoch modulo 8.
 __device__ __forceinline__ uint32_t tag_word(float v, uint32_t epoch) {
-  return (__float_as_uint(v) & ~3u) | (epoch & 3u);
+  return (__float_as_uint(v) & ~7u) | (epoch & 7u);
 }
-__device__ __forceinline__ float tag_val(uint32_t w) { return __uint_as_float(w & ~3u); }
+__device__ __forceinline__ float tag_val(uint32_t w) { return __uint_as_float(w & ~7u); }
 __device__ __forceinline__ bool tags_ok(const uint4& w, uint32_t epoch) {
-  const uint32_t e = epoch & 3u;
-  return ((w.x & 3u) == e) & ((w.y & 3u) == e) & ((w.z & 3u) == e) & ((w.w & 3u) == e);
+  const uint32_t e = epoch & 7u;
+  return ((w.x & 7u) == e) & ((w.y & 7u) == e) & ((w.z & 7u) == e) & ((w.w & 7u) == e);
 }
 // Stores are 8-byte relaxed (strong) stores, loads 16-byte relaxed loads of
 // two 8-byte elements; a word is never torn.
@@ -320,7 +321,7 @@ __device__ __forceinline__ bool poll_all(uint4 (&v)[MI][MC], const unsigned* con
 // Named barrier of the compute warps (the producer warps never take part).
 template <int COUNT>
 __device__ __forceinline__ void compute_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(COUNT) : "memory");
+  asm volatile("barrier.sync 1, %0;" ::"n"(COUNT) : "memory");
 }
 
 // hi = bf16(v), lo = bf16(v - hi) for a pair, packed two per word.
@@ -351,7 +352,7 @@ struct WinMean {
     n = tid < a.T * QV ? 1 : 0;
     t = n ? tid / QV : 0;
     c = j * G::W + s * (G::W / kStreams) + (tid % QV) * 4;
-    base[0] = a.mbuf + ((size_t)(epoch & 1) * kStreams * G::XT + t) * D + c;
+    base[0] = a.mbuf + ((size_t)(epoch % kWinXSlots) * kStreams * G::XT + t) * D + c;
     if (n) {
 #pragma unroll
       for (int s2 = 0; s2 < kStreams; ++s2) v[0][s2] = win::ld_tag4(base[0] + (size_t)s2 * G::XT * D);
@@ -386,11 +387,9 @@ __global__ void __launch_bounds__(WinGeo<D, KD, NT>::THREADS, 1)
   unsigned char* xs = smem + G::XS;
   unsigned char* ls = smem + G::LS;
   float* rp = reinterpret_cast<float*>(smem + G::RP);
-  float* sig = reinterpret_cast<float*>(smem + G::SIG);
   float* recv = reinterpret_cast<float*>(smem + G::RECV);
   float* recv_ss = reinterpret_cast<float*>(smem + G::RECV + G::RECV_SS);
   float* sums = reinterpret_cast<float*>(smem + G::RECV);  // reuses the receive area
-  float* red = reinterpret_cast<float*>(smem + G::RED);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -493,7 +492,7 @@ __global__ void __launch_bounds__(WinGeo<D, KD, NT>::THREADS, 1)
       const uint32_t xp = i & 1;          // exchange barrier phase
       const WinRead& rd = a.rd[i];
       const uint32_t epoch = base + 1u + (uint32_t)i;
-      const int p = epoch & 1;
+      const int p = epoch % kWinXSlots;  // exchange slot
       unsigned char* ent = smem + G::ENT + e * G::ENT_BYTES;
 
       // (1) down part of the entry: W_down tile, w_norm, R, P.
@@ -722,82 +721,79 @@ __global__ void __launch_bounds__(WinGeo<D, KD, NT>::THREADS, 1)
         if (q == 0) *reinterpret_cast<float2*>(rd.lo + (size_t)t * KD + k) = make_float2(l0, l1);
       }
 
-      // (7) up part of the entry; sigmoid of the gate.
+      // (7) up part of the entry.
       ok = win::wait_phase<false>(&full_u[e], ph, a.abort_flag, a.err, kErrWinFull) && ok;
-      if (tid < G::W) {
-        const float gv = reinterpret_cast<const float*>(ent + G::E_GATE)[tid];
-        sig[tid] = 1.0f / (1.0f + expf(-gv));
-      }
       {
         const bool got = win::wait_phase<true>(bar_lo, xp, a.abort_flag, a.err, kErrWinCluster);
         ok = got && ok;
         if (tid == 0 && got) ptx::mbar_arrive_expect_tx(bar_lo, G::lo_bytes(T));  // arm the next read
       }
 
-      // (8) up projection: warp w owns W_up rows 16 (w % UP_MT) .. + 15 and
-      // k-steps of its K part.
+      // (8) up projection, one warp per m16 tile of W_up rows over the whole
+      // K, and the epilogue from the accumulators.
       {
-        const int mt = warp % G::UP_MT;
-        const int h = warp / G::UP_MT;
-        const unsigned char* wu = ent + G::E_WU;
-        const int row = mt * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
-        float acc[NT][4], acc2[NT][4];
-#pragma unroll
-        for (int n = 0; n < NT; ++n) {
-          acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-          acc2[n][0] = acc2[n][1] = acc2[n][2] = acc2[n][3] = 0.f;
-        }
-#pragma unroll
-        for (int kk = 0; kk < G::UP_KS; ++kk) {
-          const int ks = h * G::UP_KS + kk;
-          uint32_t af[4];
-          ptx::ldsm_x4(ptx::smem_u32(wu + win::wu_off(row, 2 * ks + (lane >> 4), G::WU_ROWB)), af[0], af[1], af[2], af[3]);
+        __syncwarp();
+        unsigned* mrow = a.mbuf + (((size_t)p * kStreams + s) * G::XT) * D + j * G::W;
+        constexpr int UPW = G::UP_MT;
+        if (warp < UPW) {
+          const int mt = warp;
+          const unsigned char* wu = ent + G::E_WU;
+          const int row = mt * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+          float acc[NT][4], acc2[NT][4];
 #pragma unroll
           for (int n = 0; n < NT; ++n) {
-            uint32_t b0, b1;
-            ptx::ldsm_x2(ls_a + (n * 8 + (lane & 7)) * G::LS_PITCH + (2 * ks + ((lane >> 3) & 1)) * 16, b0, b1);
-            ptx::mma_bf16_16816((kk & 1) ? acc2[n] : acc[n], af, b0, b1);
+            acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+            acc2[n][0] = acc2[n][1] = acc2[n][2] = acc2[n][3] = 0.f;
           }
-        }
-        __syncwarp();
-        if (lane == 0) win::mbar_arrive(&empty_u[e]);
 #pragma unroll
-        for (int n = 0; n < NT; ++n) {
-          const int t = n * 4 + qd;
-          const int r = mt * 16 + g;
-          const float u0 = __fadd_rn(__fadd_rn(acc[n][0], acc2[n][0]), __fadd_rn(acc[n][1], acc2[n][1]));
-          const float u1 = __fadd_rn(__fadd_rn(acc[n][2], acc2[n][2]), __fadd_rn(acc[n][3], acc2[n][3]));
-          red[(h * G::TMAX + t) * G::W + r] = u0;
-          red[(h * G::TMAX + t) * G::W + r + 8] = u1;
-        }
-      }
-      win::compute_sync<G::CT>();
-
-      // (9) epilogue: out = R' + sigmoid(g) * u, kept on chip for a chained
-      // next read and published for the stream mean.
-      {
-        unsigned* mrow = a.mbuf + (((size_t)p * kStreams + s) * G::XT) * D + j * G::W;
-        for (int idx = tid; idx < G::XT * (G::W / 2); idx += G::CT) {
-          const int t = idx / (G::W / 2), c = (idx % (G::W / 2)) * 2;
-          if (t >= T) {  // keeps every slot of this parity fresh (see the tag rule above)
+          for (int ks = 0; ks < KD / 16; ++ks) {
+            uint32_t af[4];
+            ptx::ldsm_x4(ptx::smem_u32(wu + win::wu_off(row, 2 * ks + (lane >> 4), G::WU_ROWB)), af[0], af[1], af[2],
+                         af[3]);
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+              uint32_t b0, b1;
+              ptx::ldsm_x2(ls_a + (n * 8 + (lane & 7)) * G::LS_PITCH + (2 * ks + ((lane >> 3) & 1)) * 16, b0, b1);
+              ptx::mma_bf16_16816((ks & 1) ? acc2[n] : acc[n], af, b0, b1);
+            }
+          }
+          const float* gate = reinterpret_cast<const float*>(ent + G::E_GATE);
+          const int r0 = mt * 16 + g;
+          const float sg0 = 1.0f / (1.0f + expf(-gate[r0]));
+          const float sg1 = 1.0f / (1.0f + expf(-gate[r0 + 8]));
+          __syncwarp();
+          if (lane == 0) win::mbar_arrive(&empty_u[e]);
+#pragma unroll
+          for (int n = 0; n < NT; ++n) {
+            const int t = n * 4 + qd;
+            const float u0 = __fadd_rn(__fadd_rn(acc[n][0], acc2[n][0]), __fadd_rn(acc[n][1], acc2[n][1]));
+            const float u1 = __fadd_rn(__fadd_rn(acc[n][2], acc2[n][2]), __fadd_rn(acc[n][3], acc2[n][3]));
+            float o0 = 0.f, o1 = 0.f;
+            if (t < T) {
+              o0 = __fmaf_rn(sg0, u0, rp[t * G::W + r0]);
+              o1 = __fmaf_rn(sg1, u1, rp[t * G::W + r0 + 8]);
+              rd.out[(size_t)t * G::N + col0 + r0] = o0;
+              rd.out[(size_t)t * G::N + col0 + r0 + 8] = o1;
+              rp[t * G::W + r0] = o0;
+              rp[t * G::W + r0 + 8] = o1;
+            }
+            const float n0 = __shfl_down_sync(0xffffffffu, o0, 4);
+            const float n1 = __shfl_down_sync(0xffffffffu, o1, 4);
+            if ((g & 1) == 0) {
+              win::st_tag2(mrow + (size_t)t * D + r0, win::tag_word(o0, epoch), win::tag_word(n0, epoch));
+              win::st_tag2(mrow + (size_t)t * D + r0 + 8, win::tag_word(o1, epoch), win::tag_word(n1, epoch));
+            }
+          }
+        } else {
+          __syncwarp();
+          if (lane == 0) win::mbar_arrive(&empty_u[e]);
+          for (int idx = tid - 32 * UPW; idx < (G::XT - G::TMAX) * (G::W / 2); idx += G::CT - 32 * UPW) {
+            const int t = G::TMAX + idx / (G::W / 2), c = (idx % (G::W / 2)) * 2;
             win::st_tag2(mrow + (size_t)t * D + c, win::tag_word(0.f, epoch), win::tag_word(0.f, epoch));
-            continue;
           }
-          float2 u = *reinterpret_cast<const float2*>(red + t * G::W + c);
-#pragma unroll
-          for (int h = 1; h < G::UP_KSPLIT; ++h) {
-            const float2 u2 = *reinterpret_cast<const float2*>(red + (h * G::TMAX + t) * G::W + c);
-            u.x = __fadd_rn(u.x, u2.x);
-            u.y = __fadd_rn(u.y, u2.y);
-          }
-          const float2 r = *reinterpret_cast<const float2*>(rp + t * G::W + c);
-          const float2 o = make_float2(__fmaf_rn(sig[c], u.x, r.x), __fmaf_rn(sig[c + 1], u.y, r.y));
-          *reinterpret_cast<float2*>(rd.out + (size_t)t * G::N + col0 + c) = o;
-          *reinterpret_cast<float2*>(rp + t * G::W + c) = o;
-          win::st_tag2(mrow + (size_t)t * D + c, win::tag_word(o.x, epoch), win::tag_word(o.y, epoch));
         }
       }
-      win::compute_sync<G::CT>();  // out tile, red and sig are complete before the next read
+      win::compute_sync<G::CT>();  // the out tile is complete before the next read
     }
     // The last read's stream mean.
     {
@@ -808,10 +804,25 @@ __global__ void __launch_bounds__(WinGeo<D, KD, NT>::THREADS, 1)
     win::compute_sync<G::CT>();
     if (tid == 0) a.gen[b] = base + (uint32_t)a.count;
   }
+  __syncwarp();
   __syncthreads();
-  // No CTA leaves while a peer may still write into its shared memory.
+  // No CTA leaves while a peer may still write into its shared memory.  After
+  // an abort the receivers stop waiting for their bytes: let stores a peer
+  // issued before it saw the abort land first (decision taken once per CTA).
+  __shared__ unsigned aborted;
+  if (tid == 0) aborted = win::load_abort(a.abort_flag);
   ptx::cluster_arrive_release();
   ptx::cluster_wait();
+  if (aborted != 0u) {
+    if (tid == 0) {
+      const uint64_t t0 = ptx::globaltimer_ns();
+      while (ptx::globaltimer_ns() - t0 < 50000u) {
+      }
+    }
+    __syncthreads();
+    ptx::cluster_arrive_release();
+    ptx::cluster_wait();
+  }
 }
 
 }  // namespace hc

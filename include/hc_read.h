@@ -149,6 +149,14 @@ int hc_read_batch_persistent(hc_read_t h, int T);
  * last hc_read_reset. */
 int hc_read_check(hc_read_t h);
 
+/* The error word itself (synchronises the device), or a negative hc_status.
+ * Bits: 1 and 2 the down kernel's w_norm and W_down copies, 4 and 8 the up
+ * kernel's gate and W_up copies, 16 a ring slot of hc_read_batch's persistent
+ * kernel that did not land, 32 a ring slot its producer could not reuse, 64 a
+ * cluster exchange (partial sums or lo) and 128 the global exchange that did
+ * not complete in time. */
+int64_t hc_read_error_word(hc_read_t h);
+
 /* Re-zero the handle's error word on `stream` (after HC_ERR_TIMEOUT). */
 int hc_read_reset(hc_read_t h, hc_stream_t stream);
 
