@@ -23,7 +23,9 @@ from ._binding import (  # noqa: F401
     hc_graph_launch,
     hc_read,
     hc_read_batch,
+    hc_read_batch_groups,
     hc_read_batch_persistent,
+    hc_read_batch_plan,
     hc_read_check,
     hc_read_create,
     hc_read_desc,

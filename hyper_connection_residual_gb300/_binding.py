@@ -23,6 +23,7 @@ EXPORTS = (
     "hc_read_destroy", "hc_read_scratch_bytes", "hc_status_str",
     "hc_graph_begin", "hc_graph_end", "hc_graph_launch", "hc_graph_destroy",
     "hc_read_noalloc", "hc_read_batch", "hc_read_batch_persistent", "hc_read_error_word",
+    "hc_read_batch_plan", "hc_read_batch_groups", "hc_read_set_batch_lanes",
 )
 
 
@@ -87,6 +88,14 @@ def load(path: str | None = None):
         [_vp] * 6 + [ctypes.c_int] + [_vp] * 4
     lib.hc_read_batch.restype = ctypes.c_int
     lib.hc_read_batch.argtypes = [_vp, ctypes.POINTER(hc_read_desc), ctypes.c_int, ctypes.c_int, _vp]
+    lib.hc_read_batch_plan.restype = ctypes.c_int
+    lib.hc_read_batch_plan.argtypes = [_vp, ctypes.POINTER(hc_read_desc), ctypes.c_int, ctypes.c_int]
+    lib.hc_read_set_batch_lanes.restype = ctypes.c_int
+    lib.hc_read_set_batch_lanes.argtypes = [_vp, ctypes.c_int]
+    lib.hc_read_batch_groups.restype = ctypes.c_int
+    lib.hc_read_batch_groups.argtypes = [ctypes.POINTER(hc_read_desc), ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.POINTER(ctypes.c_int)]
     lib.hc_read_error_word.restype = ctypes.c_int64
     lib.hc_read_error_word.argtypes = [_vp]
     lib.hc_read_batch_persistent.restype = ctypes.c_int
@@ -202,12 +211,8 @@ def hc_read_noalloc(geometry, eps, R, w_norm, W_down, W_up, gate, pending, T: in
            "hc_read_noalloc")
 
 
-def hc_read_batch(h: int, geometry, reads, T: int, stream=None) -> None:
-    """Enqueue a list of reads in order (see include/hc_read.h).
-
-    ``reads``: sequence of dicts with keys R, w_norm, W_down, W_up, gate,
-    pending (or P; may be None), out, mean, lo.  A read whose R is the
-    previous read's out tensor is chained."""
+def _descs(geometry, reads, T: int):
+    """hc_read_desc array of a list of reads (tensors checked; ints pass as addresses)."""
     n, d, K = geometry
     N = n * d
     arr = (hc_read_desc * len(reads))()
@@ -219,7 +224,36 @@ def hc_read_batch(h: int, geometry, reads, T: int, stream=None) -> None:
             _ptr(r["gate"], "gate", _F32, N), _ptr(pend, "pending", _F32, T * N),
             _ptr(r["out"], "out", _F32, T * N), _ptr(r["mean"], "mean", _F32, T * d),
             _ptr(r["lo"], "lo", _F32, T * K))
+    return arr
+
+
+def hc_read_batch(h: int, geometry, reads, T: int, stream=None) -> None:
+    """Enqueue a list of reads in order (see include/hc_read.h).
+
+    ``reads``: sequence of dicts with keys R, w_norm, W_down, W_up, gate,
+    pending (or P; may be None), out, mean, lo.  A read whose R is the
+    previous read's out tensor is chained."""
+    arr = _descs(geometry, reads, T)
     _check(load().hc_read_batch(h, arr, len(reads), T, _stream_ptr(stream)), "hc_read_batch")
+
+
+def hc_read_batch_plan(h: int, geometry, reads, T: int) -> int:
+    """0: read by read on the caller's stream, 1: the persistent kernel,
+    L >= 2: read by read on L internal streams."""
+    st = load().hc_read_batch_plan(h, _descs(geometry, reads, T), len(reads), T)
+    if st < 0:
+        _check(st, "hc_read_batch_plan")
+    return st
+
+
+def hc_read_batch_groups(geometry, reads, T: int) -> list[int]:
+    """Group index of every read (host logic; reads may give int addresses)."""
+    n, d, K = geometry
+    group = (ctypes.c_int * len(reads))()
+    st = load().hc_read_batch_groups(_descs(geometry, reads, T), len(reads), n, d, K, T, group)
+    if st < 0:
+        _check(st, "hc_read_batch_groups")
+    return list(group)
 
 
 def hc_read_batch_persistent(h: int, T: int) -> bool:
@@ -296,6 +330,16 @@ class Read:
 
     def batch_persistent(self, T: int) -> bool:
         return hc_read_batch_persistent(self.h, T)
+
+    def batch_plan(self, reads, T: int) -> int:
+        return hc_read_batch_plan(self.h, self.geometry, reads, T)
+
+    def set_batch_lanes(self, lanes: int) -> int:
+        """Most internal streams a batch may use (0/1: the caller's stream only)."""
+        st = load().hc_read_set_batch_lanes(self.h, lanes)
+        if st < 0:
+            _check(st, "hc_read_set_batch_lanes")
+        return st
 
     def check(self) -> int:
         return hc_read_check(self.h)

@@ -5,8 +5,11 @@
 
 #include <cstdint>
 #include <cstdlib>
+#include <algorithm>
 #include <mutex>
 #include <new>
+#include <numeric>
+#include <vector>
 
 #include "hc_kernels.cuh"
 #include "hc_kernels_tc.cuh"
@@ -14,6 +17,11 @@
 #include "hc_window.cuh"
 
 #define HC_EXPORT extern "C" __attribute__((visibility("default")))
+
+// Streams hc_read_batch spreads independent reads over.  Measured on GB300
+// (cold reads, d = 2560): one stream 5.2 us per read at T = 1; 4 / 6 / 8
+// streams 2.60 / 2.52 / 2.51 us; at T = 8 6.9 -> 3.88 / 3.79 / 3.82 us.
+constexpr int kBatchLanes = 6;
 
 struct hc_read_s {
   int n, d, K, T_max, device;
@@ -32,6 +40,18 @@ struct hc_read_s {
   unsigned* gen;
   size_t window_bytes;  // xbuf, mbuf, gen, abort word: zeroed by hc_read_reset
   unsigned* abort_flag;
+  // Internal streams on which hc_read_batch runs groups of reads that share
+  // no memory side by side (each with its own partial-sum slots), forked from
+  // and joined back into the caller's stream with events.
+  struct Lane {
+    cudaStream_t st;
+    cudaEvent_t done;
+    float* part[2];
+    int parity;
+  } lanes[kBatchLanes];
+  int nlanes;         // lanes created (0: batches run on the caller's stream only)
+  int batch_lanes;    // most lanes a batch may use (hc_read_set_batch_lanes)
+  cudaEvent_t fork;
 };
 
 namespace {
@@ -42,6 +62,34 @@ using hc::UpArgs;
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// The batch lanes' streams and events (on the current device).
+cudaError_t create_lanes(hc_read_s* h) {
+  cudaError_t e = cudaEventCreateWithFlags(&h->fork, cudaEventDisableTiming);
+  if (e != cudaSuccess) return e;
+  for (int l = 0; l < kBatchLanes; ++l) {
+    e = cudaStreamCreateWithFlags(&h->lanes[l].st, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return e;
+    e = cudaEventCreateWithFlags(&h->lanes[l].done, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      cudaStreamDestroy(h->lanes[l].st);
+      return e;
+    }
+    h->nlanes = l + 1;
+  }
+  h->batch_lanes = h->nlanes;
+  return cudaSuccess;
+}
+
+void destroy_lanes(hc_read_s* h) {
+  for (int l = 0; l < h->nlanes; ++l) {
+    cudaEventDestroy(h->lanes[l].done);
+    cudaStreamDestroy(h->lanes[l].st);
+  }
+  if (h->fork != nullptr) cudaEventDestroy(h->fork);
+  h->nlanes = 0;
+  h->fork = nullptr;
+}
 
 // Launch configuration with programmatic dependent launch and, when
 // cluster_x > 1, thread-block clusters of cluster_x CTAs along x.
@@ -192,6 +240,15 @@ bool record_and_check(int device, void* stream, const Range (&ins)[6], const Ran
   return independent;
 }
 
+// Drops what is kept for (device, stream): the next read there waits for
+// everything before it in full.
+void forget_stream(int device, void* stream) {
+  std::lock_guard<std::mutex> lock(g_track_mutex);
+  for (auto& e : g_track) {
+    if (e.valid && e.device == device && e.stream == stream) e.valid = false;
+  }
+}
+
 // ---- Persistent multi-read kernel (hc_window.cuh), d = 2560, K = 320, T <= 4.
 using WinG1 = hc::WinGeo<2560, 320, 1>;
 constexpr size_t kXbufWords = (size_t)hc::kWinXSlots * hc::kWinCluster * (hc::kWinCtas / hc::kWinCluster) *
@@ -279,7 +336,8 @@ HC_EXPORT int hc_read_create(hc_read_t* out, int n, int d, int K, int T_max, flo
     const size_t xss_b = h->window ? round_up(kXssWords * 4, 256) : 0;
     const size_t mbuf_b = h->window ? round_up(kMbufWords * 4, 256) : 0;
     const size_t gen_b = h->window ? round_up(hc::kWinCtas * sizeof(unsigned), 256) + 256 : 0;
-    h->scratch_bytes = 2 * part_b + err_b + xbuf_b + xss_b + mbuf_b + gen_b;
+    const size_t lanes_b = kBatchLanes * 2 * part_b;
+    h->scratch_bytes = 2 * part_b + err_b + xbuf_b + xss_b + mbuf_b + gen_b + lanes_b;
     e = cudaMalloc(&h->scratch, h->scratch_bytes);
     if (e == cudaSuccess) {
       char* base = static_cast<char*>(h->scratch);
@@ -296,8 +354,15 @@ HC_EXPORT int hc_read_create(hc_read_t* out, int n, int d, int K, int T_max, flo
       h->mbuf = h->window ? reinterpret_cast<unsigned*>(wb + xbuf_b + xss_b) : nullptr;
       h->gen = h->window ? reinterpret_cast<unsigned*>(wb + xbuf_b + xss_b + mbuf_b) : nullptr;
       h->abort_flag = h->window ? reinterpret_cast<unsigned*>(wb + h->window_bytes - 256) : nullptr;
+      char* lb = wb + h->window_bytes;
+      for (int l = 0; l < kBatchLanes; ++l) {
+        h->lanes[l].part[0] = reinterpret_cast<float*>(lb + (2 * l) * part_b);
+        h->lanes[l].part[1] = reinterpret_cast<float*>(lb + (2 * l + 1) * part_b);
+        h->lanes[l].parity = 0;
+      }
       e = cudaMemset(h->scratch, 0, h->scratch_bytes);
       if (e == cudaSuccess) e = cudaDeviceSynchronize();
+      if (e == cudaSuccess) e = create_lanes(h);
     } else {
       h->scratch = nullptr;
     }
@@ -305,7 +370,11 @@ HC_EXPORT int hc_read_create(hc_read_t* out, int n, int d, int K, int T_max, flo
   cudaSetDevice(prev);
   if (e != cudaSuccess) {
     if (h != nullptr) {
-      if (h->scratch != nullptr) cudaFree(h->scratch);
+      if (cudaSetDevice(h->device) == cudaSuccess) {
+        destroy_lanes(h);
+        if (h->scratch != nullptr) cudaFree(h->scratch);
+        cudaSetDevice(prev);
+      }
       delete h;
     }
     return HC_ERR_CUDA;
@@ -314,21 +383,13 @@ HC_EXPORT int hc_read_create(hc_read_t* out, int n, int d, int K, int T_max, flo
   return HC_OK;
 }
 
-HC_EXPORT int hc_read_ex(hc_read_t h, const float* R, const float* w_norm, const uint16_t* W_down,
-                         const uint16_t* W_up, const float* gate, const float* pending, int T,
-                         float* out, float* mean, float* lo, float* r_out, float* rs,
-                         hc_stream_t stream) {
-  if (h == nullptr) return HC_ERR_ARG;
-  if (T < 1 || T > h->T_max) return HC_ERR_ARG;
-  if (!R || !w_norm || !W_down || !W_up || !gate || !out || !mean || !lo) return HC_ERR_ARG;
-  const void* ptrs[] = {R, w_norm, W_down, W_up, gate, pending, out, mean, lo, r_out, rs};
-  for (const void* p : ptrs) {
-    if (p != nullptr && !aligned16(p)) return HC_ERR_ALIGN;
-  }
-  int cur = -1;
-  if (cudaGetDevice(&cur) != cudaSuccess) return HC_ERR_CUDA;
-  if (cur != h->device) return HC_ERR_ARG;
+namespace {
 
+// Enqueues one validated read on `st` with partial-sum slot `part` (the two
+// kernels of the read; the caller alternates between its two slots).
+int enqueue_read(hc_read_t h, float* part, int device, const float* R, const float* w_norm,
+                 const uint16_t* W_down, const uint16_t* W_up, const float* gate, const float* pending,
+                 int T, float* out, float* mean, float* lo, float* r_out, float* rs, cudaStream_t st) {
   const size_t N = (size_t)h->n * h->d;
   const Range ins[6] = {range_of(R, T * N * 4),        range_of(pending, T * N * 4),
                         range_of(w_norm, N * 4),        range_of(gate, N * 4),
@@ -336,9 +397,7 @@ HC_EXPORT int hc_read_ex(hc_read_t h, const float* R, const float* w_norm, const
   const Range outs[5] = {range_of(out, T * N * 4),  range_of(mean, (size_t)T * h->d * 4),
                          range_of(lo, (size_t)T * h->K * 4), range_of(r_out, T * N * 4),
                          range_of(rs, (size_t)T * h->n * 4)};
-  const int independent = record_and_check(cur, stream, ins, outs) ? 1 : 0;
-  float* part = h->part[h->parity];
-  h->parity ^= 1;
+  const int independent = record_and_check(device, st, ins, outs) ? 1 : 0;
 
   DownArgs da;
   da.R = R;
@@ -368,7 +427,6 @@ HC_EXPORT int hc_read_ex(hc_read_t h, const float* R, const float* w_norm, const
   ua.T_max = h->T_max;
   ua.independent = independent;
 
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = (h->d == 2560) ? launch_geometry<2560, 320>(T, da, ua, st)
                                  : launch_geometry<4096, 512>(T, da, ua, st);
   if (e != cudaSuccess) {
@@ -376,6 +434,29 @@ HC_EXPORT int hc_read_ex(hc_read_t h, const float* R, const float* w_norm, const
     return HC_ERR_CUDA;
   }
   return HC_OK;
+}
+
+}  // namespace
+
+HC_EXPORT int hc_read_ex(hc_read_t h, const float* R, const float* w_norm, const uint16_t* W_down,
+                         const uint16_t* W_up, const float* gate, const float* pending, int T,
+                         float* out, float* mean, float* lo, float* r_out, float* rs,
+                         hc_stream_t stream) {
+  if (h == nullptr) return HC_ERR_ARG;
+  if (T < 1 || T > h->T_max) return HC_ERR_ARG;
+  if (!R || !w_norm || !W_down || !W_up || !gate || !out || !mean || !lo) return HC_ERR_ARG;
+  const void* ptrs[] = {R, w_norm, W_down, W_up, gate, pending, out, mean, lo, r_out, rs};
+  for (const void* p : ptrs) {
+    if (p != nullptr && !aligned16(p)) return HC_ERR_ALIGN;
+  }
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return HC_ERR_CUDA;
+  if (cur != h->device) return HC_ERR_ARG;
+
+  float* part = h->part[h->parity];
+  h->parity ^= 1;
+  return enqueue_read(h, part, cur, R, w_norm, W_down, W_up, gate, pending, T, out, mean, lo, r_out, rs,
+                      static_cast<cudaStream_t>(stream));
 }
 
 HC_EXPORT int hc_read(hc_read_t h, const float* R, const float* w_norm, const uint16_t* W_down,
@@ -386,6 +467,112 @@ HC_EXPORT int hc_read(hc_read_t h, const float* R, const float* w_norm, const ui
 }
 
 namespace {
+
+int find_root(std::vector<int>& parent, int x) {
+  while (parent[x] != x) {
+    parent[x] = parent[parent[x]];
+    x = parent[x];
+  }
+  return x;
+}
+
+// Groups of a batch's reads that must run in order: two reads share a group
+// when an output of one overlaps an input or an output of the other, directly
+// or through other reads.  group[j] numbers the groups in order of first
+// appearance; returns how many there are.
+int group_reads(const hc_read_desc* descs, int count, int n, int d, int K, int T, int* group) {
+  const size_t N = (size_t)n * d;
+  struct Out {
+    Range r;
+    int read;
+  };
+  std::vector<Out> outs;
+  outs.reserve(3 * (size_t)count);
+  for (int j = 0; j < count; ++j) {
+    const hc_read_desc& q = descs[j];
+    const Range rs[3] = {range_of(q.out, T * N * 4), range_of(q.mean, (size_t)T * d * 4),
+                         range_of(q.lo, (size_t)T * K * 4)};
+    for (const Range& r : rs) {
+      if (r.lo != r.hi) outs.push_back({r, j});
+    }
+  }
+  std::sort(outs.begin(), outs.end(), [](const Out& a, const Out& b) { return a.r.lo < b.r.lo; });
+  std::vector<uintptr_t> hi_max(outs.size());
+  for (size_t i = 0; i < outs.size(); ++i) hi_max[i] = std::max(i ? hi_max[i - 1] : 0, outs[i].r.hi);
+  std::vector<int> parent(count);
+  std::iota(parent.begin(), parent.end(), 0);
+  for (int j = 0; j < count; ++j) {
+    const hc_read_desc& q = descs[j];
+    const Range mine[9] = {range_of(q.R, T * N * 4),         range_of(q.pending, T * N * 4),
+                           range_of(q.w_norm, N * 4),         range_of(q.gate, N * 4),
+                           range_of(q.W_down, N * K * 2),     range_of(q.W_up, N * K * 2),
+                           range_of(q.out, T * N * 4),        range_of(q.mean, (size_t)T * d * 4),
+                           range_of(q.lo, (size_t)T * K * 4)};
+    for (const Range& m : mine) {
+      if (m.lo == m.hi) continue;
+      // Outputs starting below m.hi, walked down while one of them may still
+      // reach above m.lo.
+      const auto first_after = std::lower_bound(outs.begin(), outs.end(), m.hi,
+                                                [](const Out& o, uintptr_t v) { return o.r.lo < v; });
+      for (ptrdiff_t i = (first_after - outs.begin()) - 1; i >= 0 && hi_max[i] > m.lo; --i) {
+        if (outs[i].r.hi > m.lo && outs[i].read != j) {
+          parent[find_root(parent, outs[i].read)] = find_root(parent, j);
+        }
+      }
+    }
+  }
+  std::vector<int> id(count, -1);
+  int groups = 0;
+  for (int j = 0; j < count; ++j) {
+    const int r = find_root(parent, j);
+    if (id[r] < 0) id[r] = groups++;
+    group[j] = id[r];
+  }
+  return groups;
+}
+
+// Runs the reads of a batch on the handle's lanes, group g on lane g mod L,
+// each lane in the batch's order; forks from and joins back into `caller`.
+int run_lanes(hc_read_t h, const hc_read_desc* descs, int count, int T, const int* group, int lanes,
+              int device, cudaStream_t caller) {
+  if (cudaEventRecord(h->fork, caller) != cudaSuccess) {
+    cudaGetLastError();
+    return HC_ERR_CUDA;
+  }
+  int forked = 0;
+  for (; forked < lanes; ++forked) {
+    // A lane's first read waits in full for whatever preceded the batch.
+    forget_stream(device, h->lanes[forked].st);
+    if (cudaStreamWaitEvent(h->lanes[forked].st, h->fork, 0) != cudaSuccess) break;
+  }
+  int status = forked == lanes ? HC_OK : HC_ERR_CUDA;
+  for (int j = 0; j < count && status == HC_OK; ++j) {
+    hc_read_s::Lane& ln = h->lanes[group[j] % lanes];
+    const hc_read_desc& q = descs[j];
+    float* part = ln.part[ln.parity];
+    ln.parity ^= 1;
+    status = enqueue_read(h, part, device, q.R, q.w_norm, q.W_down, q.W_up, q.gate, q.pending, T, q.out,
+                          q.mean, q.lo, nullptr, nullptr, ln.st);
+  }
+  // Every forked lane joins, also after a failure: a capture must not end
+  // with work left on a lane.
+  for (int l = 0; l < forked; ++l) {
+    if (cudaEventRecord(h->lanes[l].done, h->lanes[l].st) != cudaSuccess ||
+        cudaStreamWaitEvent(caller, h->lanes[l].done, 0) != cudaSuccess) {
+      status = HC_ERR_CUDA;
+    }
+  }
+  if (status != HC_OK) cudaGetLastError();
+  // The caller's next read waits for the whole batch.
+  forget_stream(device, caller);
+  return status;
+}
+
+// How many lanes a batch with `groups` groups runs on (0: not on lanes).
+int lanes_for(hc_read_t h, int groups) {
+  const int most = std::min(h->nlanes, h->batch_lanes);
+  return (groups >= 2 && most >= 2) ? std::min(groups, most) : 0;
+}
 
 // One launch of the persistent kernel over descs[0..count) (count <= kWinMaxReads).
 int launch_window(hc_read_t h, const hc_read_desc* descs, int count, int T, cudaStream_t st) {
@@ -454,6 +641,11 @@ HC_EXPORT int hc_read_batch(hc_read_t h, const hc_read_desc* descs, int count, i
     }
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (count >= 2 && lanes_for(h, count) >= 2) {
+    std::vector<int> group(count);
+    const int lanes = lanes_for(h, group_reads(descs, count, h->n, h->d, h->K, T, group.data()));
+    if (lanes >= 2) return run_lanes(h, descs, count, T, group.data(), lanes, cur, st);
+  }
   if (hc_read_batch_persistent(h, T) != 1) {
     // Shapes the persistent kernel does not cover: the reads one by one.
     for (int j = 0; j < count; ++j) {
@@ -477,6 +669,29 @@ HC_EXPORT int hc_read_batch(hc_read_t h, const hc_read_desc* descs, int count, i
                          range_of(last.lo, (size_t)T * h->K * 4), range_of(nullptr, 0), range_of(nullptr, 0)};
   record_and_check(cur, stream, ins, outs);
   return HC_OK;
+}
+
+HC_EXPORT int hc_read_batch_plan(hc_read_t h, const hc_read_desc* descs, int count, int T) {
+  if (h == nullptr || descs == nullptr || count < 1 || T < 1 || T > h->T_max) return HC_ERR_ARG;
+  if (count >= 2) {
+    std::vector<int> group(count);
+    const int lanes = lanes_for(h, group_reads(descs, count, h->n, h->d, h->K, T, group.data()));
+    if (lanes >= 2) return lanes;
+  }
+  return hc_read_batch_persistent(h, T) == 1 ? 1 : 0;
+}
+
+HC_EXPORT int hc_read_set_batch_lanes(hc_read_t h, int lanes) {
+  if (h == nullptr || lanes < 0) return HC_ERR_ARG;
+  const int prev = h->batch_lanes;
+  h->batch_lanes = std::min(lanes, kBatchLanes);
+  return prev;
+}
+
+HC_EXPORT int hc_read_batch_groups(const hc_read_desc* descs, int count, int n, int d, int K, int T,
+                                   int* group) {
+  if (descs == nullptr || group == nullptr || count < 1 || T < 1 || n < 1 || d < 1 || K < 1) return HC_ERR_ARG;
+  return group_reads(descs, count, n, d, K, T, group);
 }
 
 HC_EXPORT int hc_read_check(hc_read_t h) {
@@ -522,6 +737,7 @@ HC_EXPORT void hc_read_destroy(hc_read_t h) {
   int prev = -1;
   if (cudaGetDevice(&prev) == cudaSuccess && cudaSetDevice(h->device) == cudaSuccess) {
     cudaDeviceSynchronize();
+    destroy_lanes(h);
     cudaFree(h->scratch);
     cudaSetDevice(prev);
   }

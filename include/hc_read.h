@@ -129,15 +129,49 @@ typedef struct {
  * reuse one set of output buffers.  `descs` is host memory, read during the
  * call only.
  *
- * For (d, K) = (2560, 320) and T <= 4 on a device that can hold it, the batch
- * runs as one persistent kernel per 224 reads: 128 CTAs, one per SM, that
- * must all be resident at once (a cooperative launch).  Do not run two such
- * batches at the same time on one device (two streams or two threads): a
- * kernel that cannot get its 128 SMs gives up after its bounded waits and
- * reports HC_ERR_TIMEOUT through hc_read_check.  Other shapes run read by
- * read as hc_read does.  hc_read_reset also clears the persistent kernel's
- * abort word; its exchange state needs no reset. */
+ * The reads fall into groups (hc_read_batch_groups): two reads share a group
+ * when an output of one overlaps an input or output of the other, directly or
+ * through other reads.  With two or more groups the batch runs read by read
+ * on up to 6 internal streams of the handle, each group on one of them in
+ * the batch's order, forked from `stream` and joined back into it with
+ * events (graph capture included); every read's bits are those of hc_read.
+ * Reads sharing nothing then overlap on the device, which is what the
+ * hardware needs: one read is a chain of dependent steps (about 5 us) that
+ * keeps HBM busy for only 2 us of it.
+ *
+ * A batch that is one group (a chain, or reads reusing one set of outputs),
+ * for (d, K) = (2560, 320) and T <= 4 on a device that can hold it, runs as
+ * one persistent kernel per 224 reads: 128 CTAs, one per SM, that must all
+ * be resident at once (a cooperative launch).  Do not run two such batches
+ * at the same time on one device (two streams or two threads): a kernel that
+ * cannot get its 128 SMs gives up after its bounded waits and reports
+ * HC_ERR_TIMEOUT through hc_read_check.  Other one-group batches run read by
+ * read on `stream` as hc_read does.  hc_read_reset also clears the
+ * persistent kernel's abort word; its exchange state needs no reset. */
 int hc_read_batch(hc_read_t h, const hc_read_desc* descs, int count, int T, hc_stream_t stream);
+
+/* How hc_read_batch would run this batch (same arguments): 0 read by read on
+ * the caller's stream, 1 as the persistent kernel, L >= 2 on L internal
+ * streams; HC_ERR_ARG for a NULL handle or descs, no reads or T outside
+ * 1..T_max.  Enqueues nothing. */
+int hc_read_batch_plan(hc_read_t h, const hc_read_desc* descs, int count, int T);
+
+/* Most internal streams hc_read_batch may use on this handle (default and
+ * upper bound 6; 0 or 1: every batch stays on the caller's stream, as one
+ * persistent kernel or read by read).  Returns the previous setting, or
+ * HC_ERR_ARG for a NULL handle or lanes < 0.  Not thread-safe against a
+ * concurrent hc_read_batch on the same handle. */
+int hc_read_set_batch_lanes(hc_read_t h, int lanes);
+
+/* The groups of a batch of `count` T-token reads of geometry (n, d, K): writes
+ * group[j] (groups numbered 0, 1, ... in order of first appearance) and
+ * returns the number of groups, or HC_ERR_ARG.  Reads j and k share a group
+ * when a byte range of one's outputs (out [T][n d] fp32, mean [T][d] fp32,
+ * lo [T][K] fp32) overlaps one of the other's inputs (R, pending, w_norm,
+ * gate, W_down, W_up) or outputs, or through a chain of such overlaps.
+ * Host logic only: the pointers are compared, never dereferenced, and no
+ * device is needed. */
+int hc_read_batch_groups(const hc_read_desc* descs, int count, int n, int d, int K, int T, int* group);
 
 /* 1 if hc_read_batch on this handle runs batches of T-token reads as the
  * persistent kernel, 0 if it runs them read by read; HC_ERR_ARG for a NULL

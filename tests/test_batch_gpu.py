@@ -46,6 +46,9 @@ def sets(dev):
 @pytest.fixture(scope="module")
 def rd(dev):
     r = hc.Read(4, 2560, 320, T_max=8, eps=EPS)
+    # Batches stay on the caller's stream: these tests are about the
+    # persistent kernel (the internal streams: test_lanes_gpu.py).
+    r.set_batch_lanes(1)
     yield r
     r.close()
 
@@ -55,6 +58,11 @@ def test_persistent_kernel_is_used(dev, rd):
     persistent kernel (the other tests would also pass read by read)."""
     assert all(rd.batch_persistent(T) for T in (1, 2, 3, 4))
     assert not any(rd.batch_persistent(T) for T in (5, 8))
+    g = synth.G1
+    o = [_outs(g, 2, dev) for _ in range(3)]
+    w = dev_weights(synth.weight_set(g, 0), dev)
+    R = torch.zeros(2, g.N, device=dev)
+    assert rd.batch_plan([_desc(w, R, None, o[j]) for j in range(3)], 2) == 1
 
 
 def _outs(g, T, dev):
