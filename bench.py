@@ -3,15 +3,18 @@
 Metric: microseconds per hyper-connection read and achieved HBM GB/s with cold
 weights at T = 1..8.  One step is the cold read sweep at n=4, d=2560, K=320:
 for every T in (1, 2, 3, 4, 5, 6, 8) with the pending write off and on, 300
-reads rotated over 16 weight sets (16 x 13.1 MB > the 129 MB L2), each case
-captured once as a CUDA graph and replayed.  `value` is the algorithmic bytes
-of every read of the step divided by the step time (GB/s, higher is better);
-`us_per_read` gives the per-case times.
+independent reads rotated over 16 weight sets (16 x 13.1 MB > the 129 MB L2),
+each with its own output buffers, enqueued as one hc_read_batch (the library
+runs reads that share no memory side by side on its internal streams), each
+case captured once as a CUDA graph and replayed.  `value` is the algorithmic
+bytes of every read of the step divided by the step time (GB/s, higher is
+better); `us_per_read` gives the per-case times.
 
-Also reported on the same line: the 96-read chained window graph (T=4), the
-scaled-up width (d=4096, K=512) and the T=16/32/64 batches, the roofline of the
-read, an end-to-end figure through host buffers, and the FP64 oracle timed on
-one host core (a baseline only).
+Also reported on the same line: the same sweep as 300 hc_read calls on one
+stream, the 96-read chained window graph (T=4; hc_read_batch, the persistent
+window kernel, and 96 hc_read calls), the scaled-up width (d=4096, K=512) and
+the T=16/32/64 batches, the roofline of the read, an end-to-end figure through
+host buffers, and the FP64 oracle timed on one host core (a baseline only).
 
 `--impl reference` times the FP64 oracle as the reference arm (host cores, a
 bounded sample of the same workload per step).
@@ -242,11 +245,15 @@ def run_reference(args):
 # --------------------------------------------------------------------- GPU arm
 
 class Sweep:
-    """Device-resident inputs and one captured graph per case."""
+    """Device-resident inputs and one captured graph per case.
+
+    batch=True: the case's reads are one hc_read_batch, every read with its
+    own out, mean and lo.  batch=False: one hc_read call per read on the
+    stream, all into one set of output buffers."""
 
     def __init__(self, hc, torch, dev, g: synth.Geometry, Ts, pendings, sets: int, calls: int,
-                 stream):
-        self.g, self.calls = g, calls
+                 stream, batch: bool = True):
+        self.g, self.calls, self.batch = g, calls, batch
         self.torch, self.hc, self.dev, self.stream = torch, hc, dev, stream
         Tmax = max(Ts)
         self.ws = []
@@ -259,27 +266,39 @@ class Sweep:
         act = synth.activations(g, Tmax, True)
         self.R = torch.from_numpy(act.R).to(dev)
         self.P = torch.from_numpy(act.P).to(dev)
-        self.out = torch.empty(Tmax, g.N, device=dev)
-        self.mean = torch.empty(Tmax, g.d, device=dev)
-        self.lo = torch.empty(Tmax, g.K, device=dev)
+        self.outs = [dict(out=torch.empty(Tmax, g.N, device=dev), mean=torch.empty(Tmax, g.d, device=dev),
+                          lo=torch.empty(Tmax, g.K, device=dev)) for _ in range(calls if batch else 1)]
         self.rd = hc.Read(g.n, g.d, g.K, T_max=max(8, Tmax), eps=EPS)
         self.cases = [(T, p) for T in Ts for p in pendings]
         self.graphs = {}
         for case in self.cases:
             self.graphs[case] = self._capture(*case)
 
-    def _launch(self, T, pending, j):
-        w = self.ws[j % len(self.ws)]
-        self.rd(self.R, w["w_norm"], w["W_down"], w["W_up"], w["gate"],
-                self.P if pending else None, T, self.out, self.mean, self.lo, stream=self.stream)
+    def _desc(self, T, pending, j):
+        o = self.outs[j if self.batch else 0]
+        return dict(R=self.R, P=self.P if pending else None, out=o["out"][:T], mean=o["mean"][:T],
+                    lo=o["lo"][:T], **self.ws[j % len(self.ws)])
 
     def _capture(self, T, pending):
         hc = self.hc
+        descs = [self._desc(T, pending, j) for j in range(self.calls)]
         with self.torch.cuda.stream(self.stream):
             hc.hc_graph_begin(self.stream)
-            for j in range(self.calls):
-                self._launch(T, pending, j)
+            if self.batch:
+                self.rd.batch(descs, T, stream=self.stream)
+            else:
+                for d in descs:
+                    self.rd(d["R"], d["w_norm"], d["W_down"], d["W_up"], d["gate"], d["P"], T,
+                            d["out"], d["mean"], d["lo"], stream=self.stream)
             return hc.hc_graph_end(self.stream)
+
+    def plan(self, case):
+        T, pending = case
+        return self.rd.batch_plan([self._desc(T, pending, j) for j in range(self.calls)], T)
+
+    def result(self):
+        """The output buffers of the last read of a case."""
+        return self.outs[-1]
 
     def replay(self, case):
         self.hc.hc_graph_launch(self.graphs[case], self.stream)
@@ -319,9 +338,10 @@ def time_cases(torch, sweep: Sweep, steps: int, warmup: int, stream):
     return start.elapsed_time(stop) / 1e3, per_case
 
 
-def run_window(torch, hc, dev, stream, replays: int):
+def run_window(torch, hc, dev, stream, replays: int, batch: bool):
     """96 chained reads (out_i is R_{i+1}) with distinct weight sets, T=4,
-    captured once and replayed."""
+    captured once and replayed: one hc_read_batch (batch=True: the persistent
+    window kernel) or 96 hc_read calls."""
     g = synth.G1
     T = WINDOW_T
     ws = []
@@ -336,12 +356,16 @@ def run_window(torch, hc, dev, stream, replays: int):
     mean = torch.empty(T, g.d, device=dev)
     lo = torch.empty(T, g.K, device=dev)
     rd = hc.Read(g.n, g.d, g.K, T_max=8, eps=EPS)
+    descs = [dict(R=bufs[i], P=None, out=bufs[i + 1], mean=mean, lo=lo, **ws[i]) for i in range(WINDOW_READS)]
+    plan = rd.batch_plan(descs, T)
     with torch.cuda.stream(stream):
         hc.hc_graph_begin(stream)
-        for i in range(WINDOW_READS):
-            w = ws[i]
-            rd(bufs[i], w["w_norm"], w["W_down"], w["W_up"], w["gate"], None, T,
-               bufs[i + 1], mean, lo, stream=stream)
+        if batch:
+            rd.batch(descs, T, stream=stream)
+        else:
+            for d in descs:
+                rd(d["R"], d["w_norm"], d["W_down"], d["W_up"], d["gate"], None, T,
+                   d["out"], d["mean"], d["lo"], stream=stream)
         graph = hc.hc_graph_end(stream)
     bufs[0].copy_(R0)
     torch.cuda.synchronize()
@@ -357,11 +381,14 @@ def run_window(torch, hc, dev, stream, replays: int):
     b.synchronize()
     sec = a.elapsed_time(b) / 1e3 / replays
     hc.hc_graph_destroy(graph)
+    ok = rd.check() == hc.HC_OK
     rd.close()
     nbytes = WINDOW_READS * read_bytes(g, T, False)
     return {"reads": WINDOW_READS, "T": T, "replays": replays,
+            "path": ("persistent window kernel" if plan == 1 else f"batch plan {plan}") if batch
+            else "one hc_read call per read",
             "us_per_replay": sec * 1e6, "us_per_read": sec * 1e6 / WINDOW_READS,
-            "GBps": nbytes / sec / 1e9, "bytes_per_replay": nbytes}
+            "GBps": nbytes / sec / 1e9, "bytes_per_replay": nbytes, "status_ok": ok}
 
 
 def run_profile_case():
@@ -417,6 +444,7 @@ def run_gpu(args):
     calls = args.calls
     sweep = Sweep(hc, torch, dev, g, SWEEP_T, (False, True), SETS, calls, stream)
     step_bytes = sum(sweep.bytes_per_replay(c) for c in sweep.cases)
+    plans = {sweep.plan(c) for c in sweep.cases}
 
     # ---- timed region (device-resident inputs)
     if pg:
@@ -459,8 +487,8 @@ def run_gpu(args):
                     sweep.P[:T].copy_(pin_P[:T], non_blocking=True)
             sweep.replay((T, p))
             with torch.cuda.stream(stream):
-                host_out[:T].copy_(sweep.out[:T], non_blocking=True)
-                host_mean[:T].copy_(sweep.mean[:T], non_blocking=True)
+                host_out[:T].copy_(sweep.result()["out"][:T], non_blocking=True)
+                host_mean[:T].copy_(sweep.result()["mean"][:T], non_blocking=True)
     eb.record(stream)
     eb.synchronize()
     e2e_sec = ea.elapsed_time(eb) / 1e3
@@ -473,7 +501,16 @@ def run_gpu(args):
 
     extra = {}
     if not args.quick:
-        extra["window_96_reads_T4"] = run_window(torch, hc, dev, stream, replays=100)
+        single = Sweep(hc, torch, dev, g, SWEEP_T, (False, True), SETS, calls, stream, batch=False)
+        ts, pc = time_cases(torch, single, 5, 3, stream)
+        extra["sweep_one_stream_per_call"] = {
+            "note": "the same 300 reads per case as hc_read calls on one stream, one set of outputs",
+            "us_per_read": {f"T{T}_{'pend' if p else 'nopend'}": 1e6 * pc[(T, p)] / (5 * calls)
+                            for (T, p) in single.cases},
+            "GBps": sum(single.bytes_per_replay(c) for c in single.cases) * 5 / ts / 1e9}
+        single.close()
+        extra["window_96_reads_T4"] = run_window(torch, hc, dev, stream, replays=100, batch=True)
+        extra["window_96_reads_T4_per_call"] = run_window(torch, hc, dev, stream, replays=20, batch=False)
         big = Sweep(hc, torch, dev, g, (16, 32, 64), (False,), SETS, CALLS, stream)
         tb, pc = time_cases(torch, big, 5, 3, stream)
         extra["batch_T16_32_64"] = {f"T{T}": {"us_per_read": 1e6 * pc[(T, p)] / (5 * CALLS),
@@ -495,15 +532,17 @@ def run_gpu(args):
         return 0
 
     peaks = measured_peaks()
-    # the read (down kernel + up kernel) is the unit: its average duration is
-    # the sweep's per-read time at T=1 with the pending write off
+    # the read (down kernel + up kernel) is the unit; reads of the batch
+    # overlap, so its time is the case's time over its reads (T=1, pending off)
     t1 = per_case[(1, False)] / (args.steps * calls)
     achieved = read_bytes(g, 1, False) / t1 / 1e9
     traffic = profiled_traffic()
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"],
                 "traffic": traffic["dram_bytes_per_read_T1"] if traffic else None,
-                "unit_of_work": "one read (down + up kernel) at T=1, pending off",
+                "unit_of_work": "one read (down + up kernel) at T=1, pending off: algorithmic bytes "
+                                "over the 300-read batch's time per read (reads overlap on the "
+                                "library's streams)",
                 "peak_source": peaks["source"]}
 
     cpu = None
@@ -519,8 +558,10 @@ def run_gpu(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32 (bf16 weights)", "data": "synthetic",
         "config": {"workload": "cold read sweep: n=4 streams, d=2560, K=320, T in (1,2,3,4,5,6,8), "
-                               "pending write off and on, 300 reads per case rotated over 16 weight "
-                               "sets, CUDA-graph replay",
+                               "pending write off and on, 300 independent reads per case rotated over "
+                               "16 weight sets, own outputs per read, one hc_read_batch per case, "
+                               "CUDA-graph replay",
+                   "batch_plan": sorted(plans),
                    "l2": "inputs larger than L2 (16 x 13.1 MB weight sets rotated)",
                    "parallelism": f"replicas x{world}"},
         "us_per_read": us_per_read, "GBps_per_case": gbs_per_case,
