@@ -267,6 +267,46 @@ __device__ __forceinline__ void raise_abort(unsigned* f, unsigned* err, unsigned
   atomicExch(f, 1u);
 }
 
+// Exit of a CTA of a CL-CTA cluster whose CTAs store into one another's
+// shared memory (st.async), called by every thread after the CTA's last
+// store was issued.  Normally every byte sent was waited for by its
+// receiver, so nothing is in flight.  After an abort, receivers stop waiting:
+// stores a peer issued earlier may still be on their way, and no CTA may
+// leave before they land.  The CTAs first meet (nobody sends any more), then
+// each posts its reading of the abort word to every peer; all see the same
+// CL readings, so all take the same decision: if any saw the abort, all wait
+// 50 us and meet once more before leaving.
+template <int CL>
+__device__ __forceinline__ void leave_cluster(const unsigned* abort_flag, uint32_t rank, int tid) {
+  __shared__ unsigned votes[CL];
+  ptx::cluster_arrive_release();
+  ptx::cluster_wait();
+  if (tid == 0) {
+    const unsigned mine = load_abort(abort_flag);
+    const uint32_t at = ptx::smem_u32(&votes[rank]);
+    for (uint32_t peer = 0; peer < (uint32_t)CL; ++peer) {
+      asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(mapa(at, peer)), "r"(mine) : "memory");
+    }
+  }
+  __syncwarp();
+  ptx::cluster_arrive_release();
+  ptx::cluster_wait();
+  unsigned any = 0u;
+#pragma unroll
+  for (int r = 0; r < CL; ++r) any |= votes[r];
+  if (any != 0u) {
+    if (tid == 0) {
+      const uint64_t t0 = ptx::globaltimer_ns();
+      while (ptx::globaltimer_ns() - t0 < 50000u) {
+      }
+    }
+    __syncwarp();
+    __syncthreads();
+    ptx::cluster_arrive_release();
+    ptx::cluster_wait();
+  }
+}
+
 // Bounded mbarrier wait; gives up after kWaitNs or once the launch is aborted.
 template <bool kCluster>
 __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, unsigned* abort_flag,
@@ -806,23 +846,7 @@ __global__ void __launch_bounds__(WinGeo<D, KD, NT>::THREADS, 1)
   }
   __syncwarp();
   __syncthreads();
-  // No CTA leaves while a peer may still write into its shared memory.  After
-  // an abort the receivers stop waiting for their bytes: let stores a peer
-  // issued before it saw the abort land first (decision taken once per CTA).
-  __shared__ unsigned aborted;
-  if (tid == 0) aborted = win::load_abort(a.abort_flag);
-  ptx::cluster_arrive_release();
-  ptx::cluster_wait();
-  if (aborted != 0u) {
-    if (tid == 0) {
-      const uint64_t t0 = ptx::globaltimer_ns();
-      while (ptx::globaltimer_ns() - t0 < 50000u) {
-      }
-    }
-    __syncthreads();
-    ptx::cluster_arrive_release();
-    ptx::cluster_wait();
-  }
+  win::leave_cluster<G::CL>(a.abort_flag, rank, tid);
 }
 
 }  // namespace hc
