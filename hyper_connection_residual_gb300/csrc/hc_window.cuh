@@ -48,7 +48,7 @@
 // Every sum runs in a fixed order, so repeated launches and graph replays give
 // identical bits.  All waits are bounded (kWaitNs) and also give up once any
 // CTA has raised the launch's abort word; a CTA that gives up records an error
-// bit, stops issuing work and meets its cluster at the final barrier.  The
+// bit, stops issuing work and leaves with its cluster (leave_cluster).  The
 // 128 CTAs must be co-resident (the host launches cooperatively).
 //
 // Design ancestors: the down and up kernels of "#2812 sycl: STRATA_GR_FUSED=1,
@@ -117,9 +117,9 @@ struct WinGeo {
   static constexpr int XT = kWinTmaxAlloc;                  // token stride of the buffers
   static constexpr int NCW = 10;                            // compute warps
   // Producer warps: 128 threads keep each thread's cp.async copies in flight
-  // near 100 (two ring entries of ~52).  With 64 producer threads (~210 in
-  // flight per thread) the kernel raised an illegal-instruction fault on
-  // GB300; 14 warps cap the kernel at 128 registers a thread.
+  // near 100 (two ring entries of ~52).  A variant with 64 producer threads
+  // raised an illegal-instruction fault on GB300 (cause not established);
+  // 14 warps cap the kernel at 128 registers a thread.
   static constexpr int NPW = 4;
   static constexpr int CT = 32 * NCW;
   static constexpr int PT = 32 * NPW;
