@@ -49,15 +49,19 @@ struct DownTcSmem {
   static constexpr int XS_PITCH = G::SLAB * 2 + 16;   // bytes; = 16 (mod 128)
   static constexpr int BAR = 0;
   static constexpr int W = 128;
-  static constexpr int WN = W + G::DN_ROWS * G::DN_PITCH;
-  static constexpr int XS = WN + G::SLAB * 4;         // [NCOL][SLAB] bf16: hi, lo rows
-  static constexpr int RED = XS + NCOL * XS_PITCH;    // [4 K-parts][TG][32] partials
-  static constexpr int SSW = RED + 4 * TG * 32 * 4;   // [8 warps][TG]
-  static constexpr int RS = SSW + kWarps * TG * 4;    // [kMaxT]
-  static constexpr int RECV = RS + kMaxT * 4;         // [4][T] ss, then [4][T][32] partials
+  static constexpr int XS = W + G::DN_ROWS * G::DN_PITCH;  // [NCOL][SLAB] bf16: hi, lo rows
+  // [4 K-parts][TG][32] partials, over the x rows: written only once every
+  // warp is past its MMAs (a CTA barrier), read before the next group's x.
+  static constexpr int RED = XS;
+  // [kMaxT] rs of the cluster leader, over the partials: used only after the
+  // cluster barrier, when this CTA's own sums are done.
+  static constexpr int RS = RED;
+  static constexpr int SSW = XS + NCOL * XS_PITCH;    // [8 warps][TG]
+  static constexpr int RECV = SSW + kWarps * TG * 4;  // [4][T] ss, then [4][T][32] partials
   static constexpr int bytes(int T) { return RECV + 4 * T * 4 + 4 * T * 32 * 4; }
   static constexpr int BYTES_MAX = RECV + 4 * kMaxT * 4 + 4 * kMaxT * 32 * 4;
   static_assert(XS_PITCH % 128 == 16, "x rows must be conflict-free for ldmatrix");
+  static_assert(4 * TG * 32 * 4 <= NCOL * XS_PITCH && kMaxT <= 4 * TG * 32, "aliased regions fit");
 };
 
 template <int D, int KD, int NT>
@@ -80,10 +84,20 @@ struct UpTcSmem {
   static_assert(LS_PITCH % 128 == 16, "lo rows must be conflict-free for ldmatrix");
 };
 
+// CTAs per SM the register budget is cut for: at d = 2560 four for one token
+// group (no spills at 64 registers; reads of a batch overlap better, measured
+// 3.06 -> 2.71 us per read at T = 2 and 3.15 -> 2.82 at T = 4 on six
+// streams), three for two groups (64 registers would spill: 3.67 -> 4.78 us
+// at T = 6).
+template <int D, int NT>
+constexpr int tc_min_blocks() {
+  return D == 2560 ? (NT == 1 ? 4 : 3) : 2;
+}
+
 // ------------------------------------------------------------------ kernel 1
 // Grid (16 slabs, K/32 row groups), clusters of 4 along x (one stream).
 template <int D, int KD, int NT>
-__global__ void __launch_bounds__(kThreads, D == 2560 ? 3 : 2) hc_down_tc_kernel(const DownArgs a) {
+__global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_down_tc_kernel(const DownArgs a) {
   using G = Geo<D, KD>;
   using S = DownTcSmem<D, KD, NT>;
   constexpr int TG = S::TG;
@@ -91,9 +105,7 @@ __global__ void __launch_bounds__(kThreads, D == 2560 ? 3 : 2) hc_down_tc_kernel
   constexpr int KS = KPART / 16;       // k-steps per warp
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* bar_w = reinterpret_cast<uint64_t*>(smem + S::BAR);
-  uint64_t* bar_n = bar_w + 1;
   unsigned char* w_s = smem + S::W;
-  const float* wn_s = reinterpret_cast<const float*>(smem + S::WN);
   unsigned char* xs = smem + S::XS;
   float* red_s = reinterpret_cast<float*>(smem + S::RED);
   float* ssw_s = reinterpret_cast<float*>(smem + S::SSW);
@@ -120,17 +132,20 @@ __global__ void __launch_bounds__(kThreads, D == 2560 ? 3 : 2) hc_down_tc_kernel
   if (warp == 0) {
     if (lane == 0) {
       ptx::mbar_init(bar_w, 1);
-      ptx::mbar_init(bar_n, 1);
       ptx::fence_barrier_init();
-      ptx::mbar_arrive_expect_tx(bar_n, G::SLAB * 4);
       ptx::mbar_arrive_expect_tx(bar_w, G::DN_ROWS * G::SLAB * 2);
-      ptx::bulk_g2s(smem + S::WN, a.w_norm + col0, G::SLAB * 4, bar_n, ptx::policy_evict_last());
     }
     __syncwarp();
     const uint64_t once = ptx::policy_evict_first();
     ptx::bulk_g2s(w_s + lane * G::DN_PITCH, a.W_down + (size_t)(row0 + lane) * G::N + col0,
                   G::SLAB * 2, bar_w, once);
   }
+  // This thread's float4 of the w_norm slab goes straight to registers (it is
+  // not written by the previous kernel): no shared copy, no barrier.
+  const int c4 = tid;  // one float4 of the slab per thread and token
+  static_assert(G::DN_F4 <= kThreads, "one float4 per thread and token");
+  const float4 wn = c4 < G::DN_F4 ? __ldg(reinterpret_cast<const float4*>(a.w_norm + col0) + c4)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
   ptx::launch_dependents();
   __syncthreads();  // the mbarriers are initialised before any thread waits on them
   bool ok = true;
@@ -151,8 +166,6 @@ __global__ void __launch_bounds__(kThreads, D == 2560 ? 3 : 2) hc_down_tc_kernel
   for (int t0 = 0; t0 < T; t0 += TG) {
     const int tg = min(TG, T - t0);
     float4 rv[TG], pv[TG];
-    const int c4 = tid;  // one float4 of the slab per thread and token
-    static_assert(G::DN_F4 <= kThreads, "one float4 per thread and token");
 #pragma unroll
     for (int t = 0; t < TG; ++t) {
       rv[t] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -163,8 +176,6 @@ __global__ void __launch_bounds__(kThreads, D == 2560 ? 3 : 2) hc_down_tc_kernel
         if (a.P) pv[t] = __ldcg(reinterpret_cast<const float4*>(a.P + base) + c4);
       }
     }
-    // w_norm is waited for only now, with this group's R and P loads in flight.
-    if (t0 == 0) ok = wait_bar(bar_n, 0, a.err, kErrDownNorm) && ok;
     float ssl[TG];
 #pragma unroll
     for (int t = 0; t < TG; ++t) {
@@ -175,9 +186,8 @@ __global__ void __launch_bounds__(kThreads, D == 2560 ? 3 : 2) hc_down_tc_kernel
         r.y = __fadd_rn(r.y, pv[t].y);
         r.z = __fadd_rn(r.z, pv[t].z);
         r.w = __fadd_rn(r.w, pv[t].w);
-        const float4 w = reinterpret_cast<const float4*>(wn_s)[c4];
-        const float4 x = make_float4(__fmul_rn(r.x, w.x), __fmul_rn(r.y, w.y), __fmul_rn(r.z, w.z),
-                                     __fmul_rn(r.w, w.w));
+        const float4 x = make_float4(__fmul_rn(r.x, wn.x), __fmul_rn(r.y, wn.y), __fmul_rn(r.z, wn.z),
+                                     __fmul_rn(r.w, wn.w));
         uint2 hi, lo;
         split4(x, hi, lo);  // tokens past tg carry zeros
         *reinterpret_cast<uint2*>(xs + (2 * t) * S::XS_PITCH + c4 * 8) = hi;
@@ -238,6 +248,7 @@ __global__ void __launch_bounds__(kThreads, D == 2560 ? 3 : 2) hc_down_tc_kernel
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[n][e] = __fadd_rn(acc[n][e], acc2[n][e]);
     }
+    __syncthreads();  // every warp is done with the x rows the partials overwrite
     // Column 2t holds token t's hi part, 2t + 1 its lo part.
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
@@ -256,10 +267,7 @@ __global__ void __launch_bounds__(kThreads, D == 2560 ? 3 : 2) hc_down_tc_kernel
     }
     __syncthreads();
   }
-  if (!ok) {
-    drain(bar_n, 0);
-    drain(bar_w, 0);
-  }
+  if (!ok) drain(bar_w, 0);
   ptx::cluster_arrive_release();
   ptx::cluster_wait();
   if (rank != 0) {
@@ -289,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, D == 2560 ? 3 : 2) hc_down_tc_kernel
 
 // ------------------------------------------------------------------ kernel 2
 template <int D, int KD, int NT>
-__global__ void __launch_bounds__(kThreads, D == 2560 ? 3 : 2) hc_up_tc_kernel(const UpArgs a) {
+__global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_up_tc_kernel(const UpArgs a) {
   using G = Geo<D, KD>;
   using S = UpTcSmem<D, KD, NT>;
   constexpr int TG = S::TG;

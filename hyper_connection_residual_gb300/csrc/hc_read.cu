@@ -176,11 +176,17 @@ cudaError_t launch_pair_tc(const DownArgs& da, const UpArgs& ua, cudaStream_t st
 
 // From T = 2 on the tensor-core kernels are faster on GB300 (measured: T=2
 // 6.1 vs 6.7 us, T=8 7.9 vs 11.1 us per read); at T = 1 the CUDA-core kernels
-// are (5.2 vs 6.0 us): the MMA path stages four tokens there.
+// are (5.2 vs 6.0 us): the MMA path stages four tokens there.  At d = 2560,
+// up to T = 8, the kernels of one 4-token group run the tokens in one or two
+// groups: they fit four CTAs per SM, and reads of a batch overlap better
+// (measured on six streams at T = 6: 3.50 us per read against 3.83 with
+// 8-token groups).  At d = 4096 (two CTAs per SM either way) 8-token groups
+// stay faster from T = 5 (8.5 against 9.0 us).
 template <int D, int KD>
 cudaError_t launch_geometry(int T, const DownArgs& da, const UpArgs& ua, cudaStream_t st) {
   if (T == 1) return launch_pair<D, KD, 1>(da, ua, st);
-  return T <= 4 ? launch_pair_tc<D, KD, 1>(da, ua, st) : launch_pair_tc<D, KD, 2>(da, ua, st);
+  constexpr int kOneGroupMaxT = D == 2560 ? 8 : 4;
+  return T <= kOneGroupMaxT ? launch_pair_tc<D, KD, 1>(da, ua, st) : launch_pair_tc<D, KD, 2>(da, ua, st);
 }
 
 // ---- Which reads may overlap their predecessor.
