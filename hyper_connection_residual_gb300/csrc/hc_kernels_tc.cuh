@@ -163,19 +163,28 @@ __global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_down_tc_k
   const int b_row = (lane & 7) + 8 * (lane >> 4);
   const int b_col = kp * KPART + 8 * ((lane >> 3) & 1);
 
-  for (int t0 = 0; t0 < T; t0 += TG) {
-    const int tg = min(TG, T - t0);
-    float4 rv[TG], pv[TG];
+  // R and P of one token group, this thread's float4 of the slab.
+  float4 rv[TG], pv[TG];
+  auto load_group = [&](int g0) {
+    const int gn = min(TG, T - g0);
 #pragma unroll
     for (int t = 0; t < TG; ++t) {
       rv[t] = make_float4(0.f, 0.f, 0.f, 0.f);
       pv[t] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (t < tg && c4 < G::DN_F4) {
-        const size_t base = (size_t)(t0 + t) * G::N + col0;
+      if (t < gn && c4 < G::DN_F4) {
+        const size_t base = (size_t)(g0 + t) * G::N + col0;
         rv[t] = __ldcg(reinterpret_cast<const float4*>(a.R + base) + c4);
         if (a.P) pv[t] = __ldcg(reinterpret_cast<const float4*>(a.P + base) + c4);
       }
     }
+  };
+  // The next group's loads go out while this group's MMAs run, except where
+  // the 8-token kernel at d = 2560 (80 registers) would spill them.
+  constexpr bool kEarly = !(D == 2560 && NT == 2);
+  if (kEarly) load_group(0);
+  for (int t0 = 0; t0 < T; t0 += TG) {
+    const int tg = min(TG, T - t0);
+    if (!kEarly) load_group(t0);
     float ssl[TG];
 #pragma unroll
     for (int t = 0; t < TG; ++t) {
@@ -198,6 +207,7 @@ __global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_down_tc_k
         ssl[t] = __fmaf_rn(r.w, r.w, ssl[t]);
       }
     }
+    if (kEarly && t0 + TG < T) load_group(t0 + TG);
 #pragma unroll
     for (int t = 0; t < TG; ++t) {
       float v = ssl[t];
@@ -362,33 +372,41 @@ __global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_up_tc_ker
   const int b_col = kh * KHALF + 8 * ((lane >> 3) & 1);
 
   const int T = a.T;
-  for (int t0 = 0; t0 < T; t0 += TG) {
-    const int tg = min(TG, T - t0);
-    // All global loads of the group first: the four per-stream partials of
-    // lo, then R and P of this CTA's rows.
-    float4 pv[LO4][kStreams];
+  // All global loads of a token group: the four per-stream partials of lo,
+  // then R and P of this CTA's rows.
+  float4 pv[LO4][kStreams];
+  float rr[EPI], pp[EPI];
+  auto load_group = [&](int g0) {
+    const int gn = min(TG, T - g0);
 #pragma unroll
     for (int m = 0; m < LO4; ++m) {
       const int idx = tid + m * kThreads;
 #pragma unroll
       for (int s = 0; s < kStreams; ++s) {
         pv[m][s] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (idx < tg * KD / 4) {
+        if (idx < gn * KD / 4) {
           pv[m][s] = __ldcg(reinterpret_cast<const float4*>(
-                                a.part + ((size_t)s * a.T_max + t0) * KD) + idx);
+                                a.part + ((size_t)s * a.T_max + g0) * KD) + idx);
         }
       }
     }
-    float rr[EPI], pp[EPI];
-    if (t0 == 0 && a.independent) {
+    if (g0 == 0 && a.independent) {
 #pragma unroll
       for (int m = 0; m < EPI; ++m) {
         rr[m] = rr0[m];
         pp[m] = pp0[m];
       }
     } else {
-      load_rp<D, EPI>(a, c0, t0, tg, rr, pp);
+      load_rp<D, EPI>(a, c0, g0, gn, rr, pp);
     }
+  };
+  // The next group's loads go out while this group's MMAs run, except where
+  // the 8-token kernel at d = 2560 (80 registers) would spill them.
+  constexpr bool kEarly = !(D == 2560 && NT == 2);
+  if (kEarly) load_group(0);
+  for (int t0 = 0; t0 < T; t0 += TG) {
+    const int tg = min(TG, T - t0);
+    if (!kEarly) load_group(t0);
     // lo (four partials in stream order), its hi/lo split, and this CTA's
     // share of the lo output.
 #pragma unroll
@@ -419,6 +437,7 @@ __global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_up_tc_ker
       const int idx = tid + m * kThreads;
       if (idx < tg * G::UP_ROWS) rp_s[idx] = __fadd_rn(rr[m], pp[m]);
     }
+    if (kEarly && t0 + TG < T) load_group(t0 + TG);
     if (t0 == 0) ok = wait_bar(bar_w, 0, a.err, kErrUpWeights) && ok;
     __syncthreads();  // lo (hi, lo), R' and the gates are in shared memory
 
