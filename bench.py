@@ -75,6 +75,23 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(dist, seconds: float, device=None) -> float:
+    """The largest of the ranks' values (a time), by one all-reduce (MAX);
+    `dist` is torch.distributed with a process group, or None on one rank."""
+    if dist is None:
+        return seconds
+    import torch
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(world: int, bytes_per_step: int, steps: int, seconds: float) -> float:
+    """Whole-job throughput: every rank moved bytes_per_step per step (weak
+    scaling, replicas), over the slowest rank's time."""
+    return world * bytes_per_step * steps / seconds / 1e9
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "hyper_connection_residual_gb300", "csrc")
@@ -453,12 +470,10 @@ def run_gpu(args):
     with ClockSampler(gpu_uuid(dev) if rank == 0 else None) as clocks:
         total, per_case = time_cases(torch, sweep, args.steps, args.warmup, stream)
     torch.cuda.synchronize()
+    total = max_over_ranks(pg, total, dev)
     if pg:
-        t = torch.tensor([total], device=dev, dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total = float(t.item())
         pg.barrier()
-    value = world * step_bytes * args.steps / total / 1e9
+    value = whole_job_gbs(world, step_bytes, args.steps, total)
     us_per_read = {f"T{T}_{'pend' if p else 'nopend'}": 1e6 * per_case[(T, p)] / (args.steps * calls)
                    for (T, p) in sweep.cases}
     gbs_per_case = {f"T{T}_{'pend' if p else 'nopend'}":
@@ -492,11 +507,8 @@ def run_gpu(args):
     eb.record(stream)
     eb.synchronize()
     e2e_sec = ea.elapsed_time(eb) / 1e3
-    if pg:
-        t = torch.tensor([e2e_sec], device=dev, dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_sec = float(t.item())
-    e2e_value = world * step_bytes * e2e_steps / e2e_sec / 1e9
+    e2e_sec = max_over_ranks(pg, e2e_sec, dev)
+    e2e_value = whole_job_gbs(world, step_bytes, e2e_steps, e2e_sec)
     sweep.close()
 
     extra = {}
