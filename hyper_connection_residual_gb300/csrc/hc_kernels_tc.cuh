@@ -178,9 +178,10 @@ __global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_down_tc_k
       }
     }
   };
-  // The next group's loads go out while this group's MMAs run, except where
-  // the 8-token kernel at d = 2560 (80 registers) would spill them.
-  constexpr bool kEarly = !(D == 2560 && NT == 2);
+  // The next group's loads go out while this group's MMAs run, in the
+  // 4-token kernels (the 8-token ones would spill them at d = 2560 and
+  // measured slower with them at d = 4096).
+  constexpr bool kEarly = NT == 1;
   if (kEarly) load_group(0);
   for (int t0 = 0; t0 < T; t0 += TG) {
     const int tg = min(TG, T - t0);
@@ -400,9 +401,10 @@ __global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_up_tc_ker
       load_rp<D, EPI>(a, c0, g0, gn, rr, pp);
     }
   };
-  // The next group's loads go out while this group's MMAs run, except where
-  // the 8-token kernel at d = 2560 (80 registers) would spill them.
-  constexpr bool kEarly = !(D == 2560 && NT == 2);
+  // The next group's loads go out while this group's MMAs run, in the
+  // 4-token kernels (the 8-token ones would spill them at d = 2560 and
+  // measured slower with them at d = 4096).
+  constexpr bool kEarly = NT == 1;
   if (kEarly) load_group(0);
   for (int t0 = 0; t0 < T; t0 += TG) {
     const int tg = min(TG, T - t0);
