@@ -266,3 +266,30 @@ def test_lane_limit(dev, sets, rd):
     finally:
         rd.set_batch_lanes(prev)
     assert rd.batch_plan(descs, T) == 6
+
+
+def test_bench_sized_batch(dev, orc, sets, rd, ref):
+    """The timed configuration of the benchmark: 300 independent reads at T=4
+    with the pending write, own outputs each, one batch on the six streams;
+    every read bit for bit against a direct read, three against the oracle."""
+    g, host, w = sets
+    T, L = 4, 300
+    acts = [synth.activations(g, T, True, s0=5000 + j) for j in range(8)]
+    R = [torch.from_numpy(x.R).to(dev) for x in acts]
+    P = [torch.from_numpy(x.P).to(dev) for x in acts]
+    o = [_outs(g, T, dev) for _ in range(L)]
+    descs = [_desc(w[j % 4], R[j % 8], P[j % 8], o[j]) for j in range(L)]
+    assert rd.batch_plan(descs, T) == 6
+    rd.batch(descs, T)
+    want = _outs(g, T, dev)
+    torch.cuda.synchronize()
+    assert rd.check() == hc.HC_OK
+    for j in range(L):
+        d = descs[j]
+        ref(d["R"], d["w_norm"], d["W_down"], d["W_up"], d["gate"], d["P"], T, want["out"], want["mean"], want["lo"])
+        _same_bits(o[j], want, f"read {j}")
+    for j in (0, 151, L - 1):
+        a = acts[j % 8]
+        res = orc.read(g.n, g.d, g.K, R=a.R, P=a.P, w_norm=host[j % 4].w_norm, W_down=host[j % 4].W_down,
+                       W_up=host[j % 4].W_up, gate=host[j % 4].gate, eps=EPS)
+        _close(o[j], res, f"read {j}")
