@@ -39,6 +39,7 @@ def build(src: str = SRC, out: str = LIB) -> str:
 _f32p = np.ctypeslib.ndpointer(dtype=np.float32, flags="C_CONTIGUOUS")
 _f64p = np.ctypeslib.ndpointer(dtype=np.float64, flags="C_CONTIGUOUS")
 _u16p = np.ctypeslib.ndpointer(dtype=np.uint16, flags="C_CONTIGUOUS")
+_i8p = np.ctypeslib.ndpointer(dtype=np.int8, flags="C_CONTIGUOUS")
 
 
 @dataclass
@@ -66,7 +67,50 @@ class Oracle:
             _f32p, ctypes.c_void_p, _f32p, _u16p, _u16p, _f32p,
             _f32p, _f64p, _f64p, _f64p, _f64p, _f64p, _f64p,
         ]
+        lib.hc_oracle_read_q8.restype = ctypes.c_int
+        lib.hc_oracle_read_q8.argtypes = [
+            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+            _f32p, ctypes.c_void_p, _f32p, _i8p, _u16p, _i8p, _u16p, _f32p,
+            _f32p, _f64p, _f64p, _f64p, _f64p, _f64p, _f64p,
+        ]
+        lib.hc_oracle_half.restype = ctypes.c_double
+        lib.hc_oracle_half.argtypes = [ctypes.c_uint16]
         self._lib = lib
+
+    def half(self, h: int) -> float:
+        """The value of the IEEE binary16 bit pattern h."""
+        return float(self._lib.hc_oracle_half(h))
+
+    def read_q8(self, n: int, d: int, K: int, R, w_norm, Wd_q, Wd_scale, Wu_q, Wu_scale, gate,
+                P=None, eps: float = 1e-6) -> OracleResult:
+        """The read over Q8_0 weights: Wd_q [K][n*d] int8 with Wd_scale
+        [K][n*d/32] binary16 bits (uint16); Wu_q [n*d][K] int8 with Wu_scale
+        [n*d][K/32]."""
+        N = n * d
+        R = np.ascontiguousarray(R, dtype=np.float32).reshape(-1, N)
+        T = R.shape[0]
+        w_norm = np.ascontiguousarray(w_norm, dtype=np.float32).reshape(N)
+        gate = np.ascontiguousarray(gate, dtype=np.float32).reshape(N)
+        Wd_q = np.ascontiguousarray(Wd_q, dtype=np.int8).reshape(K, N)
+        Wd_scale = np.ascontiguousarray(Wd_scale, dtype=np.uint16).reshape(K, N // 32)
+        Wu_q = np.ascontiguousarray(Wu_q, dtype=np.int8).reshape(N, K)
+        Wu_scale = np.ascontiguousarray(Wu_scale, dtype=np.uint16).reshape(N, K // 32)
+        if P is not None:
+            P = np.ascontiguousarray(P, dtype=np.float32).reshape(T, N)
+            p_ptr = P.ctypes.data_as(ctypes.c_void_p)
+        else:
+            p_ptr = None
+        res = OracleResult(
+            r_out=np.empty((T, N), np.float32), ss=np.empty((T, n)), rs=np.empty((T, n)),
+            lo=np.empty((T, K)), u=np.empty((T, N)), out=np.empty((T, N)),
+            mean=np.empty((T, d)),
+        )
+        rc = self._lib.hc_oracle_read_q8(
+            n, d, K, T, float(eps), R, p_ptr, w_norm, Wd_q, Wd_scale, Wu_q, Wu_scale, gate,
+            res.r_out, res.ss, res.rs, res.lo, res.u, res.out, res.mean)
+        if rc != 0:
+            raise ValueError(f"hc_oracle_read_q8 rejected its arguments (rc={rc})")
+        return res
 
     def read(self, n: int, d: int, K: int, R, w_norm, W_down, W_up, gate,
              P=None, eps: float = 1e-6) -> OracleResult:

@@ -27,6 +27,15 @@
 // inside a token).  W_down is [K][N] BF16, W_up is [N][K] BF16, both
 // row-major.  w_norm and gate have N entries.
 //
+// The Q8_0 read (hc_oracle_read_q8) is the same read over Q8_0 copies of the
+// two projections [P4 "Summary" and "Extra Notes": "STRATA_HC_Q8=1 reads the
+// Q8_0 hyper-connection projections", "the Q8_0 copies' extra VRAM"].  The
+// pages give no block layout; this library reads Q8_0 as: every row of a
+// weight matrix in blocks of 32 consecutive values along the dot-product axis
+// (the columns of W_down [K][N], the columns of W_up [N][K]), each block one
+// IEEE binary16 scale and 32 int8 values, weight = scale * q.  Quants and
+// scales are two arrays: q [rows][cols] int8, scale [rows][cols / 32] binary16.
+//
 // Parity status: every function below is pinned by the CPU tests (hand-expanded
 // tiny cases under tests/golden/, closed forms, invariants, brute force).
 
@@ -43,6 +52,30 @@ double bf16_to_double(uint16_t h) {
   float f;
   std::memcpy(&f, &bits, sizeof f);
   return static_cast<double>(f);
+}
+
+// IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction
+// bits; exponent 0 holds the subnormals (fraction * 2^-24), exponent 31 the
+// infinities and NaNs.  Every binary16 value is exact in double.
+double half_to_double(uint16_t h) {
+  const int sign = (h >> 15) & 1;
+  const int exponent = (h >> 10) & 0x1F;
+  const int fraction = h & 0x3FF;
+  double v;
+  if (exponent == 0) {
+    v = std::ldexp(static_cast<double>(fraction), -24);
+  } else if (exponent == 31) {
+    v = fraction == 0 ? HUGE_VAL : std::nan("");
+  } else {
+    v = std::ldexp(static_cast<double>(1024 + fraction), exponent - 25);
+  }
+  return sign ? -v : v;
+}
+
+// One Q8_0 weight: row r, column j of a matrix with `cols` columns.
+double q8_weight(const int8_t* q, const uint16_t* scale, int cols, int r, int j) {
+  return half_to_double(scale[(size_t)r * (cols / 32) + j / 32]) *
+         static_cast<double>(q[(size_t)r * cols + j]);
 }
 
 }  // namespace
@@ -142,6 +175,66 @@ void hc_oracle_epilogue(int n, int d, int T, const float* r_prime, const float* 
       mean[(size_t)t * d + c] = acc / n;
     }
   }
+}
+
+// Step 3 over Q8_0 weights: hc_oracle_down with W_down[k][i] = the Q8_0
+// value of row k, column i.
+void hc_oracle_down_q8(int n, int d, int K, int T, const float* r_prime,
+                       const float* w_norm, const int8_t* Wd_q, const uint16_t* Wd_scale,
+                       const double* rs, double* lo) {
+  const int N = n * d;
+  for (int t = 0; t < T; ++t) {
+    for (int k = 0; k < K; ++k) {
+      double total = 0.0;
+      for (int s = 0; s < n; ++s) {
+        double stream_sum = 0.0;
+        for (int c = 0; c < d; ++c) {
+          const int i = s * d + c;
+          double x = static_cast<double>(r_prime[(size_t)t * N + i]) *
+                     static_cast<double>(w_norm[i]);
+          stream_sum += q8_weight(Wd_q, Wd_scale, N, k, i) * x;
+        }
+        total += rs[t * n + s] * stream_sum;
+      }
+      lo[(size_t)t * K + k] = total;
+    }
+  }
+}
+
+// Step 4 over Q8_0 weights: u[t][i] = sum_k W_up[i][k] * lo[t][k] with
+// W_up[i][k] the Q8_0 value of row i, column k.
+void hc_oracle_up_q8(int N, int K, int T, const int8_t* Wu_q, const uint16_t* Wu_scale,
+                     const double* lo, double* u) {
+  for (int t = 0; t < T; ++t) {
+    for (int i = 0; i < N; ++i) {
+      double acc = 0.0;
+      for (int k = 0; k < K; ++k) acc += q8_weight(Wu_q, Wu_scale, K, i, k) * lo[(size_t)t * K + k];
+      u[(size_t)t * N + i] = acc;
+    }
+  }
+}
+
+// The binary16 value of h (exported for the tests of the decoding).
+double hc_oracle_half(uint16_t h) { return half_to_double(h); }
+
+// The whole Q8_0 read: steps 1, 2, 3 and 4 over Q8_0 weights, 5.  N and K
+// must be multiples of 32.  Buffers as for hc_oracle_read.
+int hc_oracle_read_q8(int n, int d, int K, int T, double eps, const float* R,
+                      const float* P, const float* w_norm, const int8_t* Wd_q,
+                      const uint16_t* Wd_scale, const int8_t* Wu_q, const uint16_t* Wu_scale,
+                      const float* gate, float* r_out, double* ss, double* rs, double* lo,
+                      double* u, double* out, double* mean) {
+  if (n <= 0 || d <= 0 || K <= 0 || T <= 0 || eps < 0.0) return -1;
+  if ((n * d) % 32 != 0 || K % 32 != 0) return -1;
+  if (!R || !w_norm || !Wd_q || !Wd_scale || !Wu_q || !Wu_scale || !gate) return -1;
+  if (!r_out || !ss || !rs || !lo || !u || !out || !mean) return -1;
+  const int N = n * d;
+  hc_oracle_commit(N, T, R, P, r_out);
+  hc_oracle_rms(n, d, T, eps, r_out, ss, rs);
+  hc_oracle_down_q8(n, d, K, T, r_out, w_norm, Wd_q, Wd_scale, rs, lo);
+  hc_oracle_up_q8(N, K, T, Wu_q, Wu_scale, lo, u);
+  hc_oracle_epilogue(n, d, T, r_out, gate, u, out, mean);
+  return 0;
 }
 
 // The whole read, steps 1-5 in order.  Any output pointer may be null except

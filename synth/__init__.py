@@ -143,6 +143,44 @@ def weight_set(g: Geometry, j: int = 0, s0: int = 0) -> WeightSet:
     )
 
 
+@dataclass
+class Q8WeightSet:
+    """Q8_0 copies of a weight set: per row, blocks of 32 consecutive values
+    along the dot-product axis, one IEEE binary16 scale and 32 int8 quants per
+    block (weight = scale * q); quants and scales as separate arrays."""
+    w_norm: np.ndarray    # [N] float32
+    gate: np.ndarray      # [N] float32
+    Wd_q: np.ndarray      # [K][N] int8
+    Wd_scale: np.ndarray  # [K][N/32] uint16 (binary16 bits)
+    Wu_q: np.ndarray      # [N][K] int8
+    Wu_scale: np.ndarray  # [N][K/32] uint16 (binary16 bits)
+
+
+def quantize_q8(w: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """Q8_0 blocks of a [rows][cols] float32 matrix (cols a multiple of 32):
+    scale = binary16(max |w| / 127) per block, q = round-to-nearest-even of
+    w / scale clamped to [-127, 127] (0 where the scale is 0)."""
+    rows, cols = w.shape
+    blocks = np.asarray(w, np.float32).reshape(rows, cols // 32, 32)
+    scale = (np.abs(blocks).max(axis=2) / np.float32(127)).astype(np.float16)
+    s = scale.astype(np.float32)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.where(s > 0, np.rint(blocks / np.where(s > 0, s, 1)), 0)
+    return np.clip(q, -127, 127).astype(np.int8).reshape(rows, cols), scale.view(np.uint16)
+
+
+def q8_weight_set(g: Geometry, j: int = 0, s0: int = 0) -> Q8WeightSet:
+    """Weight set j of ``weight_set`` with its projections drawn in float32
+    (the same draws BF16 rounds) and quantized to Q8_0."""
+    seed = s0 + 1 + j
+    wd_q, wd_s = quantize_q8(normal_f32(seed, TID_WDOWN, 0.0, g.w_std, (g.K, g.N)))
+    wu_q, wu_s = quantize_q8(normal_f32(seed, TID_WUP, 0.0, g.w_std, (g.N, g.K)))
+    return Q8WeightSet(
+        w_norm=normal_f32(seed, TID_WNORM, 1.0, 0.05, (g.N,)),
+        gate=normal_f32(seed, TID_GATE, 0.0, 1.0, (g.N,)),
+        Wd_q=wd_q, Wd_scale=wd_s, Wu_q=wu_q, Wu_scale=wu_s)
+
+
 def activations(g: Geometry, T: int, pending: bool, s0: int = 0) -> Activations:
     R = normal_f32(s0, TID_R, 0.0, 1.0, (T, g.N))
     P = normal_f32(s0, TID_P, 0.0, 0.1, (T, g.N)) if pending else None

@@ -270,6 +270,77 @@ def pin_probe_linearity(orc):
     _close(res.u, want_u, "u from lo")
 
 
+# ---------------------------------------------------------------- Q8_0 read
+
+def pin_half_decoding(orc):
+    """Every binary16 bit pattern decodes to the value NumPy's IEEE binary16 gives
+    (NaN patterns to NaN)."""
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    want = bits.view(np.float16).astype(np.float64)
+    for h in range(1 << 16):
+        got = orc.half(h)
+        w = want[h]
+        assert (math.isnan(got) and math.isnan(w)) or got == w, f"binary16 {h:#06x}: {got!r} != {w!r}"
+
+
+def _q8_exact_bf16(seed, rows, cols):
+    """Q8_0 weights whose values are exact BF16 numbers: int8 quants (7
+    significant bits at most) times power-of-two binary16 scales that differ
+    from block to block and row to row.  Returns (q, scale bits, BF16 bits)."""
+    rng = _rng(seed)
+    q = rng.integers(-127, 128, size=(rows, cols), dtype=np.int64).astype(np.int8)
+    r = np.arange(rows)[:, None]
+    b = np.arange(cols // 32)[None, :]
+    e = -(4 + (r * 7 + b * 3 + seed) % 6)               # 2^-4 ... 2^-9
+    scale = np.ldexp(np.ones((rows, cols // 32)), e).astype(np.float16)
+    w = q.astype(np.float64) * np.repeat(scale.astype(np.float64), 32, axis=1)
+    bf = (w.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal(_bf16_value(bf), w), "test weights must be exact in BF16"
+    return q, scale.view(np.uint16), bf
+
+
+def pin_q8_equals_bf16_read(orc):
+    """With Q8_0 values that are exact BF16 numbers, the Q8_0 read equals the BF16
+    read of the same values bit for bit (same formulas, same weights)."""
+    n, d, K, T = 4, 16, 64, 3
+    N = n * d
+    rd = _random_read(11, n, d, K, T, True)
+    qd, sd, bd = _q8_exact_bf16(12, K, N)
+    qu, su, bu = _q8_exact_bf16(13, N, K)
+    a = orc.read_q8(n, d, K, R=rd["R"], P=rd["P"], w_norm=rd["w_norm"], Wd_q=qd, Wd_scale=sd,
+                    Wu_q=qu, Wu_scale=su, gate=rd["gate"], eps=1e-6)
+    b = orc.read(n, d, K, R=rd["R"], P=rd["P"], w_norm=rd["w_norm"], W_down=bd, W_up=bu,
+                 gate=rd["gate"], eps=1e-6)
+    for key in ("r_out", "ss", "rs", "lo", "u", "out", "mean"):
+        assert np.array_equal(getattr(a, key), getattr(b, key)), f"Q8_0 vs BF16 read: {key}"
+
+
+def pin_q8_one_block(orc):
+    """W_up with a single quant q at row i, column k (scale s of its block) gives
+    u[t, i] = s * q * lo[t, k] exactly; all-zero scales give out = R' bit for bit."""
+    n, d, K, T = 2, 32, 64, 2
+    N = n * d
+    rd = _random_read(14, n, d, K, T, True)
+    qd, sd, _ = _q8_exact_bf16(15, K, N)
+    for (i, k, q, s) in [(0, 0, 3, 0.125), (N - 1, K - 1, -127, 2.0 ** -10), (37, 33, 64, 0.5)]:
+        qu = np.zeros((N, K), np.int8)
+        su = np.full((N, K // 32), np.float16(7.0)).view(np.uint16)   # every other block: scale 7
+        qu[i, k] = q
+        su_v = su.view(np.float16).copy()
+        su_v[i, k // 32] = np.float16(s)
+        res = orc.read_q8(n, d, K, R=rd["R"], P=rd["P"], w_norm=rd["w_norm"], Wd_q=qd, Wd_scale=sd,
+                          Wu_q=qu, Wu_scale=su_v.view(np.uint16), gate=rd["gate"], eps=1e-6)
+        want = np.zeros((T, N))
+        want[:, i] = s * q * res.lo[:, k]
+        assert np.array_equal(res.u, want), f"one quant at ({i}, {k})"
+    zero = np.zeros((K, N // 32), np.uint16)
+    res = orc.read_q8(n, d, K, R=rd["R"], P=rd["P"], w_norm=rd["w_norm"], Wd_q=qd, Wd_scale=zero,
+                      Wu_q=np.ones((N, K), np.int8), Wu_scale=np.zeros((N, K // 32), np.uint16),
+                      gate=rd["gate"], eps=1e-6)
+    assert np.array_equal(res.out, res.r_out.astype(np.float64)), "zero scales: out = R'"
+    assert not np.any(res.lo), "zero scales: lo = 0"
+
+
 ALL_PINS = [
     pin_hand_fixtures,
     pin_constant_streams,
@@ -283,6 +354,9 @@ ALL_PINS = [
     pin_token_independence,
     pin_pending_is_committed_first,
     pin_probe_linearity,
+    pin_half_decoding,
+    pin_q8_equals_bf16_read,
+    pin_q8_one_block,
 ]
 
 

@@ -31,6 +31,15 @@ MUTANTS = [
     ("mean token stride", "mean[(size_t)t * d + c]", "mean[(size_t)c * T + t]"),
     ("x squared", "acc += v * v;", "acc += v;"),
     ("bf16 widening", "<< 16;", "<< 15;"),
+    ("q8 scale block", "+ j / 32]", "+ j / 16]"),
+    ("q8 scale row stride", "scale[(size_t)r * (cols / 32)", "scale[(size_t)r * (cols / 16)"),
+    ("q8 quant transposed", "q[(size_t)r * cols + j]", "q[(size_t)j * cols + r]"),
+    ("q8 scale dropped", "return half_to_double(scale[(size_t)r * (cols / 32) + j / 32]) *", "return"),
+    ("half exponent bias", "exponent - 25", "exponent - 24"),
+    ("half subnormal scale", "fraction), -24)", "fraction), -25)"),
+    ("half implicit bit", "1024 + fraction", "fraction"),
+    ("half sign", "return sign ? -v : v;", "return v;"),
+    ("q8 down on bf16 path", "hc_oracle_down_q8(n, d, K, T, r_out, w_norm, Wd_q, Wd_scale, rs, lo);", "hc_oracle_down_q8(n, d, K, T, r_out, w_norm, Wd_q, Wu_scale, rs, lo);"),
 ]
 
 

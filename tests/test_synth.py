@@ -58,3 +58,24 @@ def test_weight_set_shapes():
     assert ws.W_down.shape == (8, 64) and ws.W_up.shape == (64, 8)
     assert ws.w_norm.shape == (64,) and ws.gate.shape == (64,)
     assert ws.W_down.dtype == np.uint16
+
+
+def test_q8_quantizer():
+    """Q8_0 blocks of the draws: |q| <= 127, every value within half a quant
+    step of its draw, the largest |q| of a nonzero block 127 (or 126 after the
+    binary16 rounding of its scale), zero blocks zero."""
+    rng = np.random.default_rng(3)
+    w = (rng.standard_normal((6, 128)) * 0.02).astype(np.float32)
+    w[2, 32:64] = 0.0
+    q, s = synth.quantize_q8(w)
+    assert q.dtype == np.int8 and s.dtype == np.uint16 and s.shape == (6, 4)
+    sc = np.repeat(s.view(np.float16).astype(np.float64), 32, axis=1)
+    assert np.all(np.abs(q.astype(np.int64)) <= 127)
+    nz = sc > 0
+    assert np.all(np.abs(q[nz] * sc[nz] - w[nz]) <= 0.5 * sc[nz] + 1e-12)
+    assert not np.any(q[2, 32:64]) and s[2, 1] == 0
+    top = np.abs(q.astype(np.int64)).reshape(6, 4, 32).max(axis=2)
+    assert np.all((top >= 126) | (s.view(np.float16) == 0))
+    ws = synth.q8_weight_set(synth.Geometry(n=4, d=64, K=64, w_std=0.02), 0)
+    assert ws.Wd_q.shape == (64, 256) and ws.Wd_scale.shape == (64, 8)
+    assert ws.Wu_q.shape == (256, 64) and ws.Wu_scale.shape == (256, 2)
