@@ -13,7 +13,7 @@ better); `us_per_read` gives the per-case times.
 Also reported on the same line: the same sweep as 300 hc_read calls on one
 stream, the 96-read chained window graph (T=4; hc_read_batch, the persistent
 window kernel, and 96 hc_read calls), the scaled-up width (d=4096, K=512) and
-the T=16/32/64 batches, the roofline of the read, an end-to-end figure through
+the T=16/32/64 batches, the same sweep over Q8_0 weights, the roofline of the read, an end-to-end figure through
 host buffers, and the FP64 oracle timed on one host core (a baseline only).
 
 `--impl reference` times the FP64 oracle as the reference arm (host cores, a
@@ -60,6 +60,13 @@ def read_bytes(g: synth.Geometry, T: int, pending: bool) -> int:
     """
     per_token = 8 * g.N + 4 * g.d + 4 * g.K + (4 * g.N if pending else 0)
     return 4 * g.K * g.N + 8 * g.N + T * per_token
+
+
+def read_bytes_q8(g: synth.Geometry, T: int, pending: bool) -> int:
+    """Algorithmic bytes of one Q8_0 read: quants 2*K*N (one byte a weight,
+    both projections) and scales 2*2*K*N/32 (binary16 per 32-weight block)
+    in place of the BF16 weights; the rest as read_bytes."""
+    return read_bytes(g, T, pending) - 4 * g.K * g.N + 2 * g.K * g.N + 4 * g.K * g.N // 32
 
 
 def sweep_cases():
@@ -269,12 +276,19 @@ class Sweep:
     stream, all into one set of output buffers."""
 
     def __init__(self, hc, torch, dev, g: synth.Geometry, Ts, pendings, sets: int, calls: int,
-                 stream, batch: bool = True):
-        self.g, self.calls, self.batch = g, calls, batch
+                 stream, batch: bool = True, q8: bool = False):
+        self.g, self.calls, self.batch, self.q8 = g, calls, batch, q8
         self.torch, self.hc, self.dev, self.stream = torch, hc, dev, stream
         Tmax = max(Ts)
         self.ws = []
         for j in range(sets):
+            if q8:
+                w = synth.q8_weight_set(g, j)
+                self.ws.append(dict(
+                    w_norm=torch.from_numpy(w.w_norm).to(dev), gate=torch.from_numpy(w.gate).to(dev),
+                    Wd_q=torch.from_numpy(w.Wd_q).to(dev), Wd_scale=torch.from_numpy(w.Wd_scale.view(np.int16)).to(dev),
+                    Wu_q=torch.from_numpy(w.Wu_q).to(dev), Wu_scale=torch.from_numpy(w.Wu_scale.view(np.int16)).to(dev)))
+                continue
             w = synth.weight_set(g, j)
             self.ws.append(dict(
                 w_norm=torch.from_numpy(w.w_norm).to(dev), gate=torch.from_numpy(w.gate).to(dev),
@@ -302,7 +316,11 @@ class Sweep:
         with self.torch.cuda.stream(self.stream):
             hc.hc_graph_begin(self.stream)
             if self.batch:
-                self.rd.batch(descs, T, stream=self.stream)
+                (self.rd.batch_q8 if self.q8 else self.rd.batch)(descs, T, stream=self.stream)
+            elif self.q8:
+                for d in descs:
+                    self.rd.q8(d["R"], d["w_norm"], d["Wd_q"], d["Wd_scale"], d["Wu_q"], d["Wu_scale"],
+                               d["gate"], d["P"], T, d["out"], d["mean"], d["lo"], stream=self.stream)
             else:
                 for d in descs:
                     self.rd(d["R"], d["w_norm"], d["W_down"], d["W_up"], d["gate"], d["P"], T,
@@ -311,7 +329,8 @@ class Sweep:
 
     def plan(self, case):
         T, pending = case
-        return self.rd.batch_plan([self._desc(T, pending, j) for j in range(self.calls)], T)
+        descs = [self._desc(T, pending, j) for j in range(self.calls)]
+        return (self.rd.batch_q8_plan if self.q8 else self.rd.batch_plan)(descs, T)
 
     def result(self):
         """The output buffers of the last read of a case."""
@@ -321,7 +340,7 @@ class Sweep:
         self.hc.hc_graph_launch(self.graphs[case], self.stream)
 
     def bytes_per_replay(self, case):
-        return self.calls * read_bytes(self.g, *case)
+        return self.calls * (read_bytes_q8 if self.q8 else read_bytes)(self.g, *case)
 
     def close(self):
         for gr in self.graphs.values():
@@ -440,6 +459,47 @@ def run_profile_case():
     return 0
 
 
+def run_profile_q8_case():
+    """Cold reads after a 256 MB L2 flush each: two BF16 and two Q8_0 reads at
+    T=4 (the same tensor-core kernels over the two weight formats), then two
+    Q8_0 reads at T=1 and two at T=8 (pending on); a small case for ncu."""
+    import torch
+    import hyper_connection_residual_gb300 as hc
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    g = synth.G1
+    bf, q8 = [], []
+    for j in range(2):
+        w = synth.weight_set(g, j)
+        bf.append(dict(w_norm=torch.from_numpy(w.w_norm).to(dev), gate=torch.from_numpy(w.gate).to(dev),
+                       W_down=torch.from_numpy(w.W_down.view(np.int16)).to(dev),
+                       W_up=torch.from_numpy(w.W_up.view(np.int16)).to(dev)))
+        w = synth.q8_weight_set(g, j)
+        q8.append(dict(w_norm=torch.from_numpy(w.w_norm).to(dev), gate=torch.from_numpy(w.gate).to(dev),
+                       Wd_q=torch.from_numpy(w.Wd_q).to(dev), Wd_scale=torch.from_numpy(w.Wd_scale.view(np.int16)).to(dev),
+                       Wu_q=torch.from_numpy(w.Wu_q).to(dev), Wu_scale=torch.from_numpy(w.Wu_scale.view(np.int16)).to(dev)))
+    act = synth.activations(g, 8, True)
+    R = torch.from_numpy(act.R).to(dev)
+    P = torch.from_numpy(act.P).to(dev)
+    out = torch.empty(8, g.N, device=dev)
+    mean = torch.empty(8, g.d, device=dev)
+    lo = torch.empty(8, g.K, device=dev)
+    flush = torch.empty(64 * 1024 * 1024, device=dev)
+    with hc.Read(g.n, g.d, g.K, T_max=8, eps=EPS) as rd:
+        for w in bf:
+            flush.zero_()
+            rd(R, w["w_norm"], w["W_down"], w["W_up"], w["gate"], P, 4, out, mean, lo)
+        for T in (4, 1, 8):
+            for w in q8:
+                flush.zero_()
+                rd.q8(R, w["w_norm"], w["Wd_q"], w["Wd_scale"], w["Wu_q"], w["Wu_scale"], w["gate"], P, T,
+                      out, mean, lo)
+        torch.cuda.synchronize()
+        assert rd.check() == hc.HC_OK
+    print("profile case done")
+    return 0
+
+
 def run_gpu(args):
     import torch
     import hyper_connection_residual_gb300 as hc
@@ -529,6 +589,18 @@ def run_gpu(args):
                                               "GBps": read_bytes(g, T, p) * 5 * CALLS / pc[(T, p)] / 1e9}
                                     for (T, p) in big.cases}
         big.close()
+        q8 = Sweep(hc, torch, dev, g, SWEEP_T, (False, True), SETS, CALLS, stream, q8=True)
+        tq, pc = time_cases(torch, q8, 5, 3, stream)
+        extra["q8_0_sweep"] = {
+            "note": "the sweep's reads over Q8_0 weights (int8 quants, one binary16 scale per 32 weights: "
+                    "6.96 MB a weight set), one hc_read_batch_q8 per case",
+            "batch_plan": sorted({q8.plan(c) for c in q8.cases}),
+            "us_per_read": {f"T{T}_{'pend' if p else 'nopend'}": 1e6 * pc[(T, p)] / (5 * CALLS)
+                            for (T, p) in q8.cases},
+            "GBps_per_case": {f"T{T}_{'pend' if p else 'nopend'}":
+                              read_bytes_q8(g, T, p) * 5 * CALLS / pc[(T, p)] / 1e9 for (T, p) in q8.cases},
+            "GBps": sum(q8.bytes_per_replay(c) for c in q8.cases) * 5 / tq / 1e9}
+        q8.close()
         g2 = synth.G2
         wide = Sweep(hc, torch, dev, g2, SWEEP_T, (True,), 12, CALLS, stream)
         tw, pc = time_cases(torch, wide, 5, 3, stream)
@@ -605,12 +677,17 @@ def main(argv=None):
     ap.add_argument("--profile", action="store_true",
                     help="no timing: a few cold direct reads at T=1 and T=8 (L2 flushed "
                          "before each), a small case for ncu captures")
+    ap.add_argument("--profile-q8", action="store_true",
+                    help="no timing: cold direct reads, BF16 and Q8_0 at T=4, Q8_0 at T=1 and T=8, "
+                         "a small case for ncu captures")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     if args.impl == "reference":
         return run_reference(args)
     if args.profile:
         return run_profile_case()
+    if args.profile_q8:
+        return run_profile_q8_case()
     return run_gpu(args)
 
 

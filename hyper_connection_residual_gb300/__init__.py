@@ -26,6 +26,11 @@ from ._binding import (  # noqa: F401
     hc_read_batch_groups,
     hc_read_batch_persistent,
     hc_read_batch_plan,
+    hc_read_batch_q8,
+    hc_read_batch_q8_groups,
+    hc_read_batch_q8_plan,
+    hc_read_q8,
+    hc_read_q8_desc,
     hc_read_check,
     hc_read_create,
     hc_read_desc,

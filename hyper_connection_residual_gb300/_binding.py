@@ -23,7 +23,8 @@ EXPORTS = (
     "hc_read_destroy", "hc_read_scratch_bytes", "hc_status_str",
     "hc_graph_begin", "hc_graph_end", "hc_graph_launch", "hc_graph_destroy",
     "hc_read_noalloc", "hc_read_batch", "hc_read_batch_persistent", "hc_read_error_word",
-    "hc_read_batch_plan", "hc_read_batch_groups", "hc_read_set_batch_lanes",
+    "hc_read_batch_plan", "hc_read_batch_groups", "hc_read_set_batch_lanes", "hc_read_q8",
+    "hc_read_batch_q8", "hc_read_batch_q8_plan", "hc_read_batch_q8_groups",
 )
 
 
@@ -31,6 +32,12 @@ class hc_read_desc(ctypes.Structure):
     """One read of hc_read_batch (field order of the C struct)."""
     _fields_ = [(name, ctypes.c_void_p) for name in (
         "R", "w_norm", "W_down", "W_up", "gate", "pending", "out", "mean", "lo")]
+
+
+class hc_read_q8_desc(ctypes.Structure):
+    """One Q8_0 read of hc_read_batch_q8 (field order of the C struct)."""
+    _fields_ = [(name, ctypes.c_void_p) for name in (
+        "R", "w_norm", "Wd_q", "Wd_scale", "Wu_q", "Wu_scale", "gate", "pending", "out", "mean", "lo")]
 
 
 class HcError(RuntimeError):
@@ -90,12 +97,22 @@ def load(path: str | None = None):
     lib.hc_read_batch.argtypes = [_vp, ctypes.POINTER(hc_read_desc), ctypes.c_int, ctypes.c_int, _vp]
     lib.hc_read_batch_plan.restype = ctypes.c_int
     lib.hc_read_batch_plan.argtypes = [_vp, ctypes.POINTER(hc_read_desc), ctypes.c_int, ctypes.c_int]
+    lib.hc_read_q8.restype = ctypes.c_int
+    lib.hc_read_q8.argtypes = [_vp] * 9 + [ctypes.c_int] + [_vp] * 6
     lib.hc_read_set_batch_lanes.restype = ctypes.c_int
     lib.hc_read_set_batch_lanes.argtypes = [_vp, ctypes.c_int]
     lib.hc_read_batch_groups.restype = ctypes.c_int
     lib.hc_read_batch_groups.argtypes = [ctypes.POINTER(hc_read_desc), ctypes.c_int, ctypes.c_int,
                                          ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                          ctypes.POINTER(ctypes.c_int)]
+    lib.hc_read_batch_q8.restype = ctypes.c_int
+    lib.hc_read_batch_q8.argtypes = [_vp, ctypes.POINTER(hc_read_q8_desc), ctypes.c_int, ctypes.c_int, _vp]
+    lib.hc_read_batch_q8_plan.restype = ctypes.c_int
+    lib.hc_read_batch_q8_plan.argtypes = [_vp, ctypes.POINTER(hc_read_q8_desc), ctypes.c_int, ctypes.c_int]
+    lib.hc_read_batch_q8_groups.restype = ctypes.c_int
+    lib.hc_read_batch_q8_groups.argtypes = [ctypes.POINTER(hc_read_q8_desc), ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                            ctypes.POINTER(ctypes.c_int)]
     lib.hc_read_error_word.restype = ctypes.c_int64
     lib.hc_read_error_word.argtypes = [_vp]
     lib.hc_read_batch_persistent.restype = ctypes.c_int
@@ -152,6 +169,8 @@ def _ptr(t, name: str, dtype_names: tuple[str, ...], numel: int | None):
 
 _F32 = ("float32",)
 _BF16 = ("bfloat16", "uint16", "int16")
+_I8 = ("int8",)
+_HALF_BITS = ("float16", "uint16", "int16")
 
 
 def hc_read_create(n: int, d: int, K: int, T_max: int, eps: float = 1e-6, device: int = 0) -> int:
@@ -176,6 +195,24 @@ def hc_read_ex(h: int, geometry, R, w_norm, W_down, W_up, gate, pending, T: int,
             _ptr(rs, "rs", _F32, T * n))
     _check(load().hc_read_ex(h, *args, T, *outs, _stream_ptr(stream)), "hc_read_ex")
 
+
+
+def hc_read_q8(h: int, geometry, R, w_norm, Wd_q, Wd_scale, Wu_q, Wu_scale, gate, pending, T: int,
+               out, mean, lo, r_out=None, rs=None, stream=None) -> None:
+    """Enqueue one read over Q8_0 weights (see include/hc_read.h): quants int8,
+    scales as binary16 bits (float16, int16 or uint16 tensors)."""
+    n, d, K = geometry
+    N = n * d
+    args = (
+        h,
+        _ptr(R, "R", _F32, T * N), _ptr(w_norm, "w_norm", _F32, N),
+        _ptr(Wd_q, "Wd_q", _I8, K * N), _ptr(Wd_scale, "Wd_scale", _HALF_BITS, K * N // 32),
+        _ptr(Wu_q, "Wu_q", _I8, N * K), _ptr(Wu_scale, "Wu_scale", _HALF_BITS, N * K // 32),
+        _ptr(gate, "gate", _F32, N), _ptr(pending, "pending", _F32, T * N), T,
+        _ptr(out, "out", _F32, T * N), _ptr(mean, "mean", _F32, T * d), _ptr(lo, "lo", _F32, T * K),
+        _ptr(r_out, "r_out", _F32, T * N), _ptr(rs, "rs", _F32, T * n), _stream_ptr(stream),
+    )
+    _check(load().hc_read_q8(*args), "hc_read_q8")
 
 def hc_read(h: int, geometry, R, w_norm, W_down, W_up, gate, pending, T: int,
             out, mean, lo, stream=None) -> None:
@@ -256,6 +293,48 @@ def hc_read_batch_groups(geometry, reads, T: int) -> list[int]:
     return list(group)
 
 
+def _q8_descs(geometry, reads, T: int):
+    """hc_read_q8_desc array of a list of Q8_0 reads (tensors checked; ints pass as addresses)."""
+    n, d, K = geometry
+    N = n * d
+    arr = (hc_read_q8_desc * len(reads))()
+    for i, r in enumerate(reads):
+        pend = r.get("pending", r.get("P"))
+        arr[i] = hc_read_q8_desc(
+            _ptr(r["R"], "R", _F32, T * N), _ptr(r["w_norm"], "w_norm", _F32, N),
+            _ptr(r["Wd_q"], "Wd_q", _I8, K * N), _ptr(r["Wd_scale"], "Wd_scale", _HALF_BITS, K * N // 32),
+            _ptr(r["Wu_q"], "Wu_q", _I8, N * K), _ptr(r["Wu_scale"], "Wu_scale", _HALF_BITS, N * K // 32),
+            _ptr(r["gate"], "gate", _F32, N), _ptr(pend, "pending", _F32, T * N),
+            _ptr(r["out"], "out", _F32, T * N), _ptr(r["mean"], "mean", _F32, T * d),
+            _ptr(r["lo"], "lo", _F32, T * K))
+    return arr
+
+
+def hc_read_batch_q8(h: int, geometry, reads, T: int, stream=None) -> None:
+    """Enqueue a list of Q8_0 reads in order (dicts with keys R, w_norm, Wd_q,
+    Wd_scale, Wu_q, Wu_scale, gate, pending or P, out, mean, lo)."""
+    arr = _q8_descs(geometry, reads, T)
+    _check(load().hc_read_batch_q8(h, arr, len(reads), T, _stream_ptr(stream)), "hc_read_batch_q8")
+
+
+def hc_read_batch_q8_plan(h: int, geometry, reads, T: int) -> int:
+    """0: read by read on the caller's stream, L >= 2: on L internal streams."""
+    st = load().hc_read_batch_q8_plan(h, _q8_descs(geometry, reads, T), len(reads), T)
+    if st < 0:
+        _check(st, "hc_read_batch_q8_plan")
+    return st
+
+
+def hc_read_batch_q8_groups(geometry, reads, T: int) -> list[int]:
+    """Group index of every Q8_0 read (host logic; reads may give int addresses)."""
+    n, d, K = geometry
+    group = (ctypes.c_int * len(reads))()
+    st = load().hc_read_batch_q8_groups(_q8_descs(geometry, reads, T), len(reads), n, d, K, T, group)
+    if st < 0:
+        _check(st, "hc_read_batch_q8_groups")
+    return list(group)
+
+
 def hc_read_batch_persistent(h: int, T: int) -> bool:
     """Whether batches of T-token reads run as the persistent kernel."""
     st = load().hc_read_batch_persistent(h, T)
@@ -319,6 +398,12 @@ class Read:
         self.eps = eps
         self.h = hc_read_create(n, d, K, T_max, eps, device)
 
+    def q8(self, R, w_norm, Wd_q, Wd_scale, Wu_q, Wu_scale, gate, pending, T, out, mean, lo,
+           r_out=None, rs=None, stream=None) -> None:
+        """One read over Q8_0 weights (hc_read_q8)."""
+        hc_read_q8(self.h, self.geometry, R, w_norm, Wd_q, Wd_scale, Wu_q, Wu_scale, gate, pending, T,
+                   out, mean, lo, r_out, rs, stream)
+
     def __call__(self, R, w_norm, W_down, W_up, gate, pending, T, out, mean, lo,
                  r_out=None, rs=None, stream=None) -> None:
         hc_read_ex(self.h, self.geometry, R, w_norm, W_down, W_up, gate, pending, T,
@@ -327,6 +412,13 @@ class Read:
     def batch(self, reads, T: int, stream=None) -> None:
         """Enqueue a list of reads (dicts, see hc_read_batch) in order."""
         hc_read_batch(self.h, self.geometry, reads, T, stream)
+
+    def batch_q8(self, reads, T: int, stream=None) -> None:
+        """Enqueue a list of Q8_0 reads (dicts, see hc_read_batch_q8) in order."""
+        hc_read_batch_q8(self.h, self.geometry, reads, T, stream)
+
+    def batch_q8_plan(self, reads, T: int) -> int:
+        return hc_read_batch_q8_plan(self.h, self.geometry, reads, T)
 
     def batch_persistent(self, T: int) -> bool:
         return hc_read_batch_persistent(self.h, T)

@@ -147,7 +147,9 @@ struct DownArgs {
   const float* R;          // [T][N]
   const float* P;          // [T][N] or null
   const float* w_norm;     // [N]
-  const uint16_t* W_down;  // [K][N] BF16
+  const uint16_t* W_down;  // [K][N] BF16 (BF16 kernels)
+  const int8_t* Wq;        // [K][N] int8 quants (Q8_0 kernels)
+  const uint16_t* Wscale;  // [K][N/32] binary16 block scales (Q8_0 kernels)
   float* part;             // scratch [4][T_max][K]: rs-scaled per-stream partials
   unsigned* err;           // scratch error word
   float* rs_out;           // [T][4] or null
@@ -161,7 +163,9 @@ struct UpArgs {
   const float* R;        // [T][N]
   const float* P;        // [T][N] or null
   const float* gate;     // [N]
-  const uint16_t* W_up;  // [N][K] BF16
+  const uint16_t* W_up;  // [N][K] BF16 (BF16 kernels)
+  const int8_t* Wq;      // [N][K] int8 quants (Q8_0 kernels)
+  const uint16_t* Wscale;  // [N][K/32] binary16 block scales (Q8_0 kernels)
   const float* part;     // scratch [4][T_max][K]
   float* out;            // [T][N]
   float* mean;           // [T][d]

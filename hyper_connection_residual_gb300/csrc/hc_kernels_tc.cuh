@@ -20,6 +20,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "hc_kernels.cuh"
 
@@ -41,15 +42,20 @@ __device__ __forceinline__ void split4(const float4 x, uint2& hi, uint2& lo) {
   lo = make_uint2(*reinterpret_cast<const uint32_t*>(&l01), *reinterpret_cast<const uint32_t*>(&l23));
 }
 
-template <int D, int KD, int NT>
+template <int D, int KD, int NT, bool Q8 = false>
 struct DownTcSmem {
   using G = Geo<D, KD>;
   static constexpr int TG = 4 * NT;
   static constexpr int NCOL = 8 * NT;
   static constexpr int XS_PITCH = G::SLAB * 2 + 16;   // bytes; = 16 (mod 128)
+  // W_down rows: BF16, or Q8_0 int8 quants with their block scales apart
+  // (pitch an odd multiple of 32 bytes: the 64-bit loads of four rows x four
+  // lanes cover the 32 banks once).
+  static constexpr int WPITCH = Q8 ? G::SLAB + 32 : G::DN_PITCH;
+  static constexpr int NB = G::SLAB / 32;              // Q8_0 blocks per row
   static constexpr int BAR = 0;
   static constexpr int W = 128;
-  static constexpr int XS = W + G::DN_ROWS * G::DN_PITCH;  // [NCOL][SLAB] bf16: hi, lo rows
+  static constexpr int XS = W + G::DN_ROWS * WPITCH;  // [NCOL][SLAB] bf16: hi, lo rows
   // [4 K-parts][TG][32] partials, over the x rows: written only once every
   // warp is past its MMAs (a CTA barrier), read before the next group's x.
   static constexpr int RED = XS;
@@ -57,32 +63,101 @@ struct DownTcSmem {
   // cluster barrier, when this CTA's own sums are done.
   static constexpr int RS = RED;
   static constexpr int SSW = XS + NCOL * XS_PITCH;    // [8 warps][TG]
-  static constexpr int RECV = SSW + kWarps * TG * 4;  // [4][T] ss, then [4][T][32] partials
+  // [32 rows][NB] binary16 block scales (Q8_0), copied in 8-byte pieces.
+  static constexpr int SC = (SSW + kWarps * TG * 4 + 15) / 16 * 16;
+  static constexpr int RECV = SC + (Q8 ? (G::DN_ROWS * NB * 2 + 15) / 16 * 16 : 0);  // [4][T] ss, then [4][T][32] partials
   static constexpr int bytes(int T) { return RECV + 4 * T * 4 + 4 * T * 32 * 4; }
   static constexpr int BYTES_MAX = RECV + 4 * kMaxT * 4 + 4 * kMaxT * 32 * 4;
   static_assert(XS_PITCH % 128 == 16, "x rows must be conflict-free for ldmatrix");
   static_assert(4 * TG * 32 * 4 <= NCOL * XS_PITCH && kMaxT <= 4 * TG * 32, "aliased regions fit");
+  static_assert(!Q8 || (NB % 4 == 0 && (G::N / 32 * 2) % 8 == 0 && (NB * 2) % 8 == 0),
+                "a row's scales are whole 8-byte pieces at 8-byte aligned addresses");
+  static_assert(!Q8 || WPITCH % 64 == 32, "Q8_0 rows: 64-bit fragment loads conflict-free");
 };
 
-template <int D, int KD, int NT>
+template <int D, int KD, int NT, bool Q8 = false>
 struct UpTcSmem {
   using G = Geo<D, KD>;
   static constexpr int TG = 4 * NT;
   static constexpr int NCOL = 8 * NT;
   static constexpr int LS_PITCH = KD * 2 + 16;        // bytes; = 16 (mod 128)
+  static constexpr int WPITCH = Q8 ? KD + 32 : G::UP_PITCH;  // W_up rows: BF16 or Q8_0 quants (as the down kernel's)
+  static constexpr int NB = KD / 32;                  // Q8_0 blocks per row
   static constexpr int BAR = 0;
   static constexpr int W = 128;
-  static constexpr int GATE = W + G::UP_ROWS * G::UP_PITCH;
+  static constexpr int GATE = W + G::UP_ROWS * WPITCH;
   static constexpr int SIG = GATE + G::UP_ROWS * 4;
   static constexpr int LS = SIG + G::UP_ROWS * 4;     // [NCOL][KD] bf16: hi, lo rows
   static constexpr int RED = LS + NCOL * LS_PITCH;    // [2 K-halves][TG][64]
   static constexpr int OUT = RED + 2 * TG * G::UP_ROWS * 4;
   static constexpr int RP = OUT + TG * G::UP_ROWS * 4;
-  static constexpr int BYTES = RP + TG * G::UP_ROWS * 4;
+  // [64 rows][NB] binary16 block scales (Q8_0): each stream's 16 rows are
+  // one contiguous run of 16 NB scales in global memory, copied in 16-byte
+  // pieces.
+  static constexpr int SC = (RP + TG * G::UP_ROWS * 4 + 15) / 16 * 16;
+  static constexpr int BYTES = SC + (Q8 ? G::UP_ROWS * NB * 2 : 0);
+  static_assert(!Q8 || (G::UP_COLS * NB * 2) % 16 == 0, "a stream's scale run is whole 16-byte pieces");
+  static_assert(!Q8 || WPITCH % 64 == 32, "Q8_0 rows: 64-bit fragment loads conflict-free");
   static constexpr int bytes(int) { return BYTES; }
   static constexpr int BYTES_MAX = BYTES;
   static_assert(LS_PITCH % 128 == 16, "lo rows must be conflict-free for ldmatrix");
 };
+
+// ---- Q8_0 weights on the BF16 MMA.
+//
+// Inside each 32-column block the MMA's k index is a permutation of the
+// memory column, chosen so that the eight quants a thread needs of one row
+// (both k-steps of the block) are eight consecutive bytes: lane (g, q) loads
+// bytes 8q .. 8q + 7 of rows g and g + 8 with one 64-bit load each.  Column
+// p = 8q + j of a block is MMA k
+//   kperm(p) = 16 (j >> 2) + 8 (j & 1) + 2q + ((j >> 1) & 1),
+// a bijection of 0..31; the activations are staged at kperm of their column,
+// so every product pairs a weight with its own activation.
+__device__ __forceinline__ int q8_kperm(int p) {
+  const int q = (p >> 3) & 3, j = p & 7;
+  return 16 * (j >> 2) + 8 * (j & 1) + 2 * q + ((j >> 1) & 1);
+}
+
+// The int8 values in bytes 0 and 2 of w as a BF16 pair (byte 0 low), exact:
+// with m = b & 127 and s the sign bit, BF16 0x4300 | m is 128 + m and
+// 0x4300 | (b & 128) is 128 or 256, so their difference is m - 128 s = b.
+__device__ __forceinline__ uint32_t q8_bytes02(uint32_t w) {
+  const uint32_t mag = (w & 0x007F007Fu) | 0x43004300u;
+  const uint32_t sub = (w & 0x00800080u) | 0x43004300u;
+  const __nv_bfloat162 r = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&mag),
+                                   *reinterpret_cast<const __nv_bfloat162*>(&sub));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// A fragments of the two k-steps of one block from rows g and g + 8 (eight
+// quants each, `r0` and `r1`): bytes 0, 2 / 1, 3 of the first word are
+// k = 2q, 2q + 1 / 2q + 8, 2q + 9 of k-step 0; the second word the same for
+// k-step 1 (kperm).
+__device__ __forceinline__ void q8_afrags(const uint2 r0, const uint2 r1, uint32_t (&a0)[4], uint32_t (&a1)[4]) {
+  a0[0] = q8_bytes02(r0.x);
+  a0[1] = q8_bytes02(r1.x);
+  a0[2] = q8_bytes02(r0.x >> 8);
+  a0[3] = q8_bytes02(r1.x >> 8);
+  a1[0] = q8_bytes02(r0.y);
+  a1[1] = q8_bytes02(r1.y);
+  a1[2] = q8_bytes02(r0.y >> 8);
+  a1[3] = q8_bytes02(r1.y >> 8);
+}
+
+// Stores the hi/lo split of four consecutive activations (columns p0 .. p0+3
+// of a 32-column block, p0 % 4 == 0) into a staging row at their kperm
+// positions: columns p0, p0 + 2 and p0 + 1, p0 + 3 are adjacent there.
+__device__ __forceinline__ void q8_stage4(unsigned char* row_hi, unsigned char* row_lo, int block_col0, int p0,
+                                          const float4 x) {
+  uint2 hi, lo;
+  split4(x, hi, lo);
+  const int k02 = block_col0 + q8_kperm(p0);      // k of column p0; p0 + 2 follows it
+  const int k13 = block_col0 + q8_kperm(p0 + 1);  // k of column p0 + 1; p0 + 3 follows it
+  *reinterpret_cast<uint32_t*>(row_hi + 2 * k02) = __byte_perm(hi.x, hi.y, 0x5410);
+  *reinterpret_cast<uint32_t*>(row_hi + 2 * k13) = __byte_perm(hi.x, hi.y, 0x7632);
+  *reinterpret_cast<uint32_t*>(row_lo + 2 * k02) = __byte_perm(lo.x, lo.y, 0x5410);
+  *reinterpret_cast<uint32_t*>(row_lo + 2 * k13) = __byte_perm(lo.x, lo.y, 0x7632);
+}
 
 // CTAs per SM the register budget is cut for: at d = 2560 four for one token
 // group (no spills at 64 registers; reads of a batch overlap better, measured
@@ -96,10 +171,10 @@ constexpr int tc_min_blocks() {
 
 // ------------------------------------------------------------------ kernel 1
 // Grid (16 slabs, K/32 row groups), clusters of 4 along x (one stream).
-template <int D, int KD, int NT>
+template <int D, int KD, int NT, bool Q8 = false>
 __global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_down_tc_kernel(const DownArgs a) {
   using G = Geo<D, KD>;
-  using S = DownTcSmem<D, KD, NT>;
+  using S = DownTcSmem<D, KD, NT, Q8>;
   constexpr int TG = S::TG;
   constexpr int KPART = G::SLAB / 4;   // columns per K-part
   constexpr int KS = KPART / 16;       // k-steps per warp
@@ -129,16 +204,28 @@ __global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_down_tc_k
   float* recv_p = recv_ss + 4 * T;
 
   ptx::cluster_arrive_relaxed();
+  constexpr int WROW = Q8 ? G::SLAB : G::SLAB * 2;  // bytes of one W_down row of the slab
   if (warp == 0) {
     if (lane == 0) {
       ptx::mbar_init(bar_w, 1);
       ptx::fence_barrier_init();
-      ptx::mbar_arrive_expect_tx(bar_w, G::DN_ROWS * G::SLAB * 2);
+      ptx::mbar_arrive_expect_tx(bar_w, G::DN_ROWS * WROW);
     }
     __syncwarp();
     const uint64_t once = ptx::policy_evict_first();
-    ptx::bulk_g2s(w_s + lane * G::DN_PITCH, a.W_down + (size_t)(row0 + lane) * G::N + col0,
-                  G::SLAB * 2, bar_w, once);
+    const void* src = Q8 ? static_cast<const void*>(a.Wq + (size_t)(row0 + lane) * G::N + col0)
+                         : static_cast<const void*>(a.W_down + (size_t)(row0 + lane) * G::N + col0);
+    ptx::bulk_g2s(w_s + lane * S::WPITCH, src, WROW, bar_w, once);
+  }
+  if constexpr (Q8) {
+    // The slab's block scales of the CTA's 32 rows (binary16), copied
+    // asynchronously: waited for with the weight tile, before the MMAs.
+    constexpr int PIECES = S::NB / 4;  // 8-byte pieces per row
+    for (int idx = tid; idx < G::DN_ROWS * PIECES; idx += kThreads) {
+      const int r = idx / PIECES, c = idx - r * PIECES;
+      ptx::cp_async8(smem + S::SC + (r * S::NB + 4 * c) * 2,
+                     a.Wscale + (size_t)(row0 + r) * (G::N / 32) + col0 / 32 + 4 * c);
+    }
   }
   // This thread's float4 of the w_norm slab goes straight to registers (it is
   // not written by the previous kernel): no shared copy, no barrier.
@@ -158,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_down_tc_k
   // Lane address pattern of an ldmatrix.x4 on a 16x16 A tile.
   const int a_row = mt * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
   const int a_col = kp * KPART + 8 * (lane >> 4);
-  const uint32_t a_base = ptx::smem_u32(w_s + a_row * G::DN_PITCH + a_col * 2);
+  const uint32_t a_base = ptx::smem_u32(w_s + a_row * S::WPITCH + a_col * 2);
   // ... and of the B operand (rows = MMA columns).
   const int b_row = (lane & 7) + 8 * (lane >> 4);
   const int b_col = kp * KPART + 8 * ((lane >> 3) & 1);
@@ -198,10 +285,14 @@ __global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_down_tc_k
         r.w = __fadd_rn(r.w, pv[t].w);
         const float4 x = make_float4(__fmul_rn(r.x, wn.x), __fmul_rn(r.y, wn.y), __fmul_rn(r.z, wn.z),
                                      __fmul_rn(r.w, wn.w));
-        uint2 hi, lo;
-        split4(x, hi, lo);  // tokens past tg carry zeros
-        *reinterpret_cast<uint2*>(xs + (2 * t) * S::XS_PITCH + c4 * 8) = hi;
-        *reinterpret_cast<uint2*>(xs + (2 * t + 1) * S::XS_PITCH + c4 * 8) = lo;
+        if constexpr (Q8) {
+          q8_stage4(xs + (2 * t) * S::XS_PITCH, xs + (2 * t + 1) * S::XS_PITCH, (4 * c4) & ~31, (4 * c4) & 31, x);
+        } else {
+          uint2 hi, lo;
+          split4(x, hi, lo);  // tokens past tg carry zeros
+          *reinterpret_cast<uint2*>(xs + (2 * t) * S::XS_PITCH + c4 * 8) = hi;
+          *reinterpret_cast<uint2*>(xs + (2 * t + 1) * S::XS_PITCH + c4 * 8) = lo;
+        }
         ssl[t] = __fmaf_rn(r.x, r.x, ssl[t]);
         ssl[t] = __fmaf_rn(r.y, r.y, ssl[t]);
         ssl[t] = __fmaf_rn(r.z, r.z, ssl[t]);
@@ -216,7 +307,10 @@ __global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_down_tc_k
       for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
       if (lane == 0) ssw_s[warp * TG + t] = v;
     }
-    if (t0 == 0) ok = wait_bar(bar_w, 0, a.err, kErrDownWeights) && ok;
+    if (t0 == 0) {
+      ok = wait_bar(bar_w, 0, a.err, kErrDownWeights) && ok;
+      if constexpr (Q8) ptx::cp_async_wait_all();
+    }
     __syncthreads();  // x (hi, lo) and the per-warp sums of squares are complete
     if (tid < tg) {
       float v = 0.f;
@@ -225,39 +319,87 @@ __global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_down_tc_k
       recv_ss[rank * T + t0 + tid] = v;
     }
 
-    // Two accumulator sets (even and odd k-steps), added at the end: half the
-    // dependent-MMA chain, a fixed order.
-    float acc[NT][4], acc2[NT][4];
-#pragma unroll
-    for (int n = 0; n < NT; ++n) {
-      acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-      acc2[n][0] = acc2[n][1] = acc2[n][2] = acc2[n][3] = 0.f;
-    }
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      uint32_t afrag[4];
-      ptx::ldsm_x4(a_base + ks * 32, afrag[0], afrag[1], afrag[2], afrag[3]);
+    // One k-step of 16 columns: B rows from the x staging, MMA into cc.
+    auto kstep = [&](int ks, const uint32_t(&af)[4], float(&cc)[NT][4]) {
 #pragma unroll
       for (int n = 0; n < NT; n += 2) {
         uint32_t b0, b1, b2, b3;
-        float (&c0)[4] = (ks & 1) ? acc2[n] : acc[n];
         if (n + 1 < NT) {
-          float (&c1)[4] = (ks & 1) ? acc2[n + 1] : acc[n + 1];
           ptx::ldsm_x4(ptx::smem_u32(xs + (n * 8 + b_row) * S::XS_PITCH + (b_col + ks * 16) * 2), b0, b1,
                        b2, b3);
-          ptx::mma_bf16_16816(c0, afrag, b0, b1);
-          ptx::mma_bf16_16816(c1, afrag, b2, b3);
+          ptx::mma_bf16_16816(cc[n], af, b0, b1);
+          ptx::mma_bf16_16816(cc[n + 1], af, b2, b3);
         } else {
           ptx::ldsm_x2(ptx::smem_u32(xs + (n * 8 + (lane & 7)) * S::XS_PITCH + (b_col + ks * 16) * 2), b0,
                        b1);
-          ptx::mma_bf16_16816(c0, afrag, b0, b1);
+          ptx::mma_bf16_16816(cc[n], af, b0, b1);
         }
       }
-    }
+    };
+    // The two k-steps of one Q8_0 block into cc, started at zero.
+    auto kstep_q8 = [&](int ks, const uint32_t(&a0)[4], const uint32_t(&a1)[4], float(&cc)[NT][4]) {
 #pragma unroll
-    for (int n = 0; n < NT; ++n) {
+      for (int n = 0; n < NT; n += 2) {
+        uint32_t b0, b1, b2, b3, c0, c1, c2, c3;
+        if (n + 1 < NT) {
+          ptx::ldsm_x4(ptx::smem_u32(xs + (n * 8 + b_row) * S::XS_PITCH + (b_col + ks * 16) * 2), b0, b1, b2, b3);
+          ptx::ldsm_x4(ptx::smem_u32(xs + (n * 8 + b_row) * S::XS_PITCH + (b_col + ks * 16 + 16) * 2), c0, c1, c2,
+                       c3);
+          ptx::mma_bf16_16816_zero(cc[n], a0, b0, b1);
+          ptx::mma_bf16_16816_zero(cc[n + 1], a0, b2, b3);
+          ptx::mma_bf16_16816(cc[n], a1, c0, c1);
+          ptx::mma_bf16_16816(cc[n + 1], a1, c2, c3);
+        } else {
+          ptx::ldsm_x2(ptx::smem_u32(xs + (n * 8 + (lane & 7)) * S::XS_PITCH + (b_col + ks * 16) * 2), b0, b1);
+          ptx::ldsm_x2(ptx::smem_u32(xs + (n * 8 + (lane & 7)) * S::XS_PITCH + (b_col + ks * 16 + 16) * 2), c0, c1);
+          ptx::mma_bf16_16816_zero(cc[n], a0, b0, b1);
+          ptx::mma_bf16_16816(cc[n], a1, c0, c1);
+        }
+      }
+    };
+    float acc[NT][4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[n][e] = __fadd_rn(acc[n][e], acc2[n][e]);
+    for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+    if constexpr (!Q8) {
+      // Two accumulator sets (even and odd k-steps), added at the end: half
+      // the dependent-MMA chain, a fixed order.
+      float acc2[NT][4];
+#pragma unroll
+      for (int n = 0; n < NT; ++n) acc2[n][0] = acc2[n][1] = acc2[n][2] = acc2[n][3] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        uint32_t afrag[4];
+        ptx::ldsm_x4(a_base + ks * 32, afrag[0], afrag[1], afrag[2], afrag[3]);
+        kstep(ks, afrag, (ks & 1) ? acc2 : acc);
+      }
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[n][e] = __fadd_rn(acc[n][e], acc2[n][e]);
+      }
+    } else {
+      // Q8_0: each 32-column block (two k-steps into one accumulator started
+      // at zero) is scaled by its rows' block scales and added, blocks in
+      // order.
+      const int g = lane >> 2, q = lane & 3;
+      const unsigned char* qa = w_s + (mt * 16 + g) * S::WPITCH + kp * KPART + 8 * q;
+      const __half* sc = reinterpret_cast<const __half*>(smem + S::SC) + (mt * 16 + g) * S::NB + kp * (KPART / 32);
+#pragma unroll 2  // fully unrolled, the 64-register variants spill
+      for (int bk = 0; bk < KS / 2; ++bk) {
+        uint32_t a0[4], a1[4];
+        q8_afrags(*reinterpret_cast<const uint2*>(qa + 32 * bk),
+                  *reinterpret_cast<const uint2*>(qa + 8 * S::WPITCH + 32 * bk), a0, a1);
+        float blk[NT][4];
+        kstep_q8(2 * bk, a0, a1, blk);
+        const float s0 = __half2float(sc[bk]), s1 = __half2float(sc[8 * S::NB + bk]);  // rows g and g + 8
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          acc[n][0] = __fmaf_rn(s0, blk[n][0], acc[n][0]);
+          acc[n][1] = __fmaf_rn(s0, blk[n][1], acc[n][1]);
+          acc[n][2] = __fmaf_rn(s1, blk[n][2], acc[n][2]);
+          acc[n][3] = __fmaf_rn(s1, blk[n][3], acc[n][3]);
+        }
+      }
     }
     __syncthreads();  // every warp is done with the x rows the partials overwrite
     // Column 2t holds token t's hi part, 2t + 1 its lo part.
@@ -307,10 +449,10 @@ __global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_down_tc_k
 }
 
 // ------------------------------------------------------------------ kernel 2
-template <int D, int KD, int NT>
+template <int D, int KD, int NT, bool Q8 = false>
 __global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_up_tc_kernel(const UpArgs a) {
   using G = Geo<D, KD>;
-  using S = UpTcSmem<D, KD, NT>;
+  using S = UpTcSmem<D, KD, NT, Q8>;
   constexpr int TG = S::TG;
   constexpr int KHALF = KD / 2;
   constexpr int KS = KHALF / 16;
@@ -339,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_up_tc_ker
       ptx::mbar_init(bar_w, 1);
       ptx::mbar_init(bar_g, 1);
       ptx::fence_barrier_init();
-      ptx::mbar_arrive_expect_tx(bar_w, G::UP_ROWS * KD * 2);
+      ptx::mbar_arrive_expect_tx(bar_w, G::UP_ROWS * KD * (Q8 ? 1 : 2));
       ptx::mbar_arrive_expect_tx(bar_g, G::UP_ROWS * 4);
     }
     __syncwarp();
@@ -350,7 +492,21 @@ __global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_up_tc_ker
     }
     for (int r = lane; r < G::UP_ROWS; r += 32) {
       const int grow = (r / G::UP_COLS) * D + c0 + (r % G::UP_COLS);
-      ptx::bulk_g2s(w_s + r * G::UP_PITCH, a.W_up + (size_t)grow * KD, KD * 2, bar_w, once);
+      if constexpr (Q8) {
+        ptx::bulk_g2s(w_s + r * S::WPITCH, a.Wq + (size_t)grow * KD, KD, bar_w, once);
+      } else {
+        ptx::bulk_g2s(w_s + r * S::WPITCH, a.W_up + (size_t)grow * KD, KD * 2, bar_w, once);
+      }
+    }
+  }
+  if constexpr (Q8) {
+    // The block scales of the CTA's 64 rows (binary16), copied
+    // asynchronously: waited for with the weight tile, before the MMAs.
+    constexpr int PIECES = G::UP_COLS * S::NB * 2 / 16;  // 16-byte pieces per stream
+    for (int idx = tid; idx < kStreams * PIECES; idx += kThreads) {
+      const int st = idx / PIECES, c = idx - st * PIECES;
+      ptx::cp_async16(smem + S::SC + st * G::UP_COLS * S::NB * 2 + 16 * c,
+                      reinterpret_cast<const unsigned char*>(a.Wscale + ((size_t)st * D + c0) * S::NB) + 16 * c);
     }
   }
   __syncthreads();  // the mbarriers are initialised before any thread waits on them
@@ -368,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_up_tc_ker
 
   const int a_row = mt * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
   const int a_col = kh * KHALF + 8 * (lane >> 4);
-  const uint32_t a_base = ptx::smem_u32(w_s + a_row * G::UP_PITCH + a_col * 2);
+  const uint32_t a_base = ptx::smem_u32(w_s + a_row * S::WPITCH + a_col * 2);
   const int b_row = (lane & 7) + 8 * (lane >> 4);
   const int b_col = kh * KHALF + 8 * ((lane >> 3) & 1);
 
@@ -421,10 +577,14 @@ __global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_up_tc_ker
         l.z = ((pv[m][0].z + pv[m][1].z) + pv[m][2].z) + pv[m][3].z;
         l.w = ((pv[m][0].w + pv[m][1].w) + pv[m][2].w) + pv[m][3].w;
         const int t = idx / (KD / 4), k4 = idx % (KD / 4);
-        uint2 hi, lo;
-        split4(l, hi, lo);  // tokens past tg carry zeros
-        *reinterpret_cast<uint2*>(ls + (2 * t) * S::LS_PITCH + k4 * 8) = hi;
-        *reinterpret_cast<uint2*>(ls + (2 * t + 1) * S::LS_PITCH + k4 * 8) = lo;
+        if constexpr (Q8) {
+          q8_stage4(ls + (2 * t) * S::LS_PITCH, ls + (2 * t + 1) * S::LS_PITCH, (4 * k4) & ~31, (4 * k4) & 31, l);
+        } else {
+          uint2 hi, lo;
+          split4(l, hi, lo);  // tokens past tg carry zeros
+          *reinterpret_cast<uint2*>(ls + (2 * t) * S::LS_PITCH + k4 * 8) = hi;
+          *reinterpret_cast<uint2*>(ls + (2 * t + 1) * S::LS_PITCH + k4 * 8) = lo;
+        }
         const int k = k4 * 4;
         const float lv[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
@@ -440,42 +600,93 @@ __global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_up_tc_ker
       if (idx < tg * G::UP_ROWS) rp_s[idx] = __fadd_rn(rr[m], pp[m]);
     }
     if (kEarly && t0 + TG < T) load_group(t0 + TG);
-    if (t0 == 0) ok = wait_bar(bar_w, 0, a.err, kErrUpWeights) && ok;
+    if (t0 == 0) {
+      ok = wait_bar(bar_w, 0, a.err, kErrUpWeights) && ok;
+      if constexpr (Q8) ptx::cp_async_wait_all();
+    }
     __syncthreads();  // lo (hi, lo), R' and the gates are in shared memory
 
-    // Two accumulator sets (even and odd k-steps), added at the end: half the
-    // dependent-MMA chain, a fixed order.
-    float acc[NT][4], acc2[NT][4];
-#pragma unroll
-    for (int n = 0; n < NT; ++n) {
-      acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-      acc2[n][0] = acc2[n][1] = acc2[n][2] = acc2[n][3] = 0.f;
-    }
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      uint32_t afrag[4];
-      ptx::ldsm_x4(a_base + ks * 32, afrag[0], afrag[1], afrag[2], afrag[3]);
+    // One k-step of 16 along K: B rows from the lo staging, MMA into cc.
+    auto kstep = [&](int ks, const uint32_t(&af)[4], float(&cc)[NT][4]) {
 #pragma unroll
       for (int n = 0; n < NT; n += 2) {
         uint32_t b0, b1, b2, b3;
-        float (&c0)[4] = (ks & 1) ? acc2[n] : acc[n];
         if (n + 1 < NT) {
-          float (&c1)[4] = (ks & 1) ? acc2[n + 1] : acc[n + 1];
           ptx::ldsm_x4(ptx::smem_u32(ls + (n * 8 + b_row) * S::LS_PITCH + (b_col + ks * 16) * 2), b0, b1,
                        b2, b3);
-          ptx::mma_bf16_16816(c0, afrag, b0, b1);
-          ptx::mma_bf16_16816(c1, afrag, b2, b3);
+          ptx::mma_bf16_16816(cc[n], af, b0, b1);
+          ptx::mma_bf16_16816(cc[n + 1], af, b2, b3);
         } else {
           ptx::ldsm_x2(ptx::smem_u32(ls + (n * 8 + (lane & 7)) * S::LS_PITCH + (b_col + ks * 16) * 2), b0,
                        b1);
-          ptx::mma_bf16_16816(c0, afrag, b0, b1);
+          ptx::mma_bf16_16816(cc[n], af, b0, b1);
         }
       }
-    }
+    };
+    // The two k-steps of one Q8_0 block into cc, started at zero.
+    auto kstep_q8 = [&](int ks, const uint32_t(&a0)[4], const uint32_t(&a1)[4], float(&cc)[NT][4]) {
 #pragma unroll
-    for (int n = 0; n < NT; ++n) {
+      for (int n = 0; n < NT; n += 2) {
+        uint32_t b0, b1, b2, b3, c0, c1, c2, c3;
+        if (n + 1 < NT) {
+          ptx::ldsm_x4(ptx::smem_u32(ls + (n * 8 + b_row) * S::LS_PITCH + (b_col + ks * 16) * 2), b0, b1, b2, b3);
+          ptx::ldsm_x4(ptx::smem_u32(ls + (n * 8 + b_row) * S::LS_PITCH + (b_col + ks * 16 + 16) * 2), c0, c1, c2,
+                       c3);
+          ptx::mma_bf16_16816_zero(cc[n], a0, b0, b1);
+          ptx::mma_bf16_16816_zero(cc[n + 1], a0, b2, b3);
+          ptx::mma_bf16_16816(cc[n], a1, c0, c1);
+          ptx::mma_bf16_16816(cc[n + 1], a1, c2, c3);
+        } else {
+          ptx::ldsm_x2(ptx::smem_u32(ls + (n * 8 + (lane & 7)) * S::LS_PITCH + (b_col + ks * 16) * 2), b0, b1);
+          ptx::ldsm_x2(ptx::smem_u32(ls + (n * 8 + (lane & 7)) * S::LS_PITCH + (b_col + ks * 16 + 16) * 2), c0, c1);
+          ptx::mma_bf16_16816_zero(cc[n], a0, b0, b1);
+          ptx::mma_bf16_16816(cc[n], a1, c0, c1);
+        }
+      }
+    };
+    float acc[NT][4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[n][e] = __fadd_rn(acc[n][e], acc2[n][e]);
+    for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+    if constexpr (!Q8) {
+      // Two accumulator sets (even and odd k-steps), added at the end: half
+      // the dependent-MMA chain, a fixed order.
+      float acc2[NT][4];
+#pragma unroll
+      for (int n = 0; n < NT; ++n) acc2[n][0] = acc2[n][1] = acc2[n][2] = acc2[n][3] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        uint32_t afrag[4];
+        ptx::ldsm_x4(a_base + ks * 32, afrag[0], afrag[1], afrag[2], afrag[3]);
+        kstep(ks, afrag, (ks & 1) ? acc2 : acc);
+      }
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[n][e] = __fadd_rn(acc[n][e], acc2[n][e]);
+      }
+    } else {
+      // Q8_0: each 32-wide block of K (two k-steps into one accumulator
+      // started at zero) is scaled by its rows' block scales and added,
+      // blocks in order.
+      const int g = lane >> 2, q = lane & 3;
+      const unsigned char* qa = w_s + (mt * 16 + g) * S::WPITCH + kh * KHALF + 8 * q;
+      const __half* sc = reinterpret_cast<const __half*>(smem + S::SC) + (mt * 16 + g) * S::NB + kh * (KHALF / 32);
+#pragma unroll 2  // fully unrolled, the 64-register variants spill
+      for (int bk = 0; bk < KS / 2; ++bk) {
+        uint32_t a0[4], a1[4];
+        q8_afrags(*reinterpret_cast<const uint2*>(qa + 32 * bk),
+                  *reinterpret_cast<const uint2*>(qa + 8 * S::WPITCH + 32 * bk), a0, a1);
+        float blk[NT][4];
+        kstep_q8(2 * bk, a0, a1, blk);
+        const float s0 = __half2float(sc[bk]), s1 = __half2float(sc[8 * S::NB + bk]);  // rows g and g + 8
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          acc[n][0] = __fmaf_rn(s0, blk[n][0], acc[n][0]);
+          acc[n][1] = __fmaf_rn(s0, blk[n][1], acc[n][1]);
+          acc[n][2] = __fmaf_rn(s1, blk[n][2], acc[n][2]);
+          acc[n][3] = __fmaf_rn(s1, blk[n][3], acc[n][3]);
+        }
+      }
     }
 #pragma unroll
     for (int n = 0; n < NT; ++n) {

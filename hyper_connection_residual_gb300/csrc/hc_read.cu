@@ -125,23 +125,25 @@ cudaError_t configure_one() {
                               hc::UpSmem<D, KD, TT>::BYTES_MAX);
 }
 
-template <int D, int KD, int NT>
+template <int D, int KD, int NT, bool Q8>
 cudaError_t configure_tc() {
-  cudaError_t e = cudaFuncSetAttribute(hc::hc_down_tc_kernel<D, KD, NT>,
+  cudaError_t e = cudaFuncSetAttribute(hc::hc_down_tc_kernel<D, KD, NT, Q8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       hc::DownTcSmem<D, KD, NT>::BYTES_MAX);
+                                       hc::DownTcSmem<D, KD, NT, Q8>::BYTES_MAX);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(hc::hc_up_tc_kernel<D, KD, NT>,
+  return cudaFuncSetAttribute(hc::hc_up_tc_kernel<D, KD, NT, Q8>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              hc::UpTcSmem<D, KD, NT>::BYTES_MAX);
+                              hc::UpTcSmem<D, KD, NT, Q8>::BYTES_MAX);
 }
 
 template <int D, int KD>
 cudaError_t configure_geometry() {
   cudaError_t e;
   if ((e = configure_one<D, KD, 1>()) != cudaSuccess) return e;
-  if ((e = configure_tc<D, KD, 1>()) != cudaSuccess) return e;
-  return configure_tc<D, KD, 2>();
+  if ((e = configure_tc<D, KD, 1, false>()) != cudaSuccess) return e;
+  if ((e = configure_tc<D, KD, 2, false>()) != cudaSuccess) return e;
+  if ((e = configure_tc<D, KD, 1, true>()) != cudaSuccess) return e;
+  return configure_tc<D, KD, 2, true>();
 }
 
 template <int D, int KD, int TT>
@@ -159,19 +161,19 @@ cudaError_t launch_pair(const DownArgs& da, const UpArgs& ua, cudaStream_t st) {
   return cudaLaunchKernelEx(&c2, hc::hc_up_kernel<D, KD, TT>, ua);
 }
 
-template <int D, int KD, int NT>
+template <int D, int KD, int NT, bool Q8 = false>
 cudaError_t launch_pair_tc(const DownArgs& da, const UpArgs& ua, cudaStream_t st) {
   using G = hc::Geo<D, KD>;
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t c1 = pdl_config(dim3(G::SLABS, G::ROW_GROUPS),
-                                      hc::DownTcSmem<D, KD, NT>::bytes(da.T), st, attr,
+                                      hc::DownTcSmem<D, KD, NT, Q8>::bytes(da.T), st, attr,
                                       G::SLABS_PER_STREAM);
-  cudaError_t e = cudaLaunchKernelEx(&c1, hc::hc_down_tc_kernel<D, KD, NT>, da);
+  cudaError_t e = cudaLaunchKernelEx(&c1, hc::hc_down_tc_kernel<D, KD, NT, Q8>, da);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr2[2];
-  cudaLaunchConfig_t c2 = pdl_config(dim3(G::UP_CTAS), hc::UpTcSmem<D, KD, NT>::bytes(ua.T), st,
+  cudaLaunchConfig_t c2 = pdl_config(dim3(G::UP_CTAS), hc::UpTcSmem<D, KD, NT, Q8>::bytes(ua.T), st,
                                       attr2, 1);
-  return cudaLaunchKernelEx(&c2, hc::hc_up_tc_kernel<D, KD, NT>, ua);
+  return cudaLaunchKernelEx(&c2, hc::hc_up_tc_kernel<D, KD, NT, Q8>, ua);
 }
 
 // From T = 2 on the tensor-core kernels are faster on GB300 (measured: T=2
@@ -188,6 +190,23 @@ cudaError_t launch_geometry(int T, const DownArgs& da, const UpArgs& ua, cudaStr
   constexpr int kOneGroupMaxT = D == 2560 ? 8 : 4;
   return T <= kOneGroupMaxT ? launch_pair_tc<D, KD, 1>(da, ua, st) : launch_pair_tc<D, KD, 2>(da, ua, st);
 }
+
+// The Q8_0 read: the tensor-core kernels at every T (no CUDA-core variant),
+// token groups as for BF16.
+template <int D, int KD>
+cudaError_t launch_geometry_q8(int T, const DownArgs& da, const UpArgs& ua, cudaStream_t st) {
+  constexpr int kOneGroupMaxT = D == 2560 ? 8 : 4;
+  return T <= kOneGroupMaxT ? launch_pair_tc<D, KD, 1, true>(da, ua, st)
+                            : launch_pair_tc<D, KD, 2, true>(da, ua, st);
+}
+
+// Q8_0 weights of a read (quants and block scales of both projections).
+struct Q8Weights {
+  const int8_t* Wd_q;
+  const uint16_t* Wd_scale;
+  const int8_t* Wu_q;
+  const uint16_t* Wu_scale;
+};
 
 // ---- Which reads may overlap their predecessor.
 // For every (device, stream) the output ranges of the last read enqueued
@@ -216,9 +235,63 @@ Range range_of(const void* p, size_t bytes) {
   return Range{b, p != nullptr ? b + bytes : b};
 }
 
+// One read as the host handles it: BF16 projections (W_down, W_up) or Q8_0
+// ones (q8.Wd_q set, W_down and W_up null).
+struct ReadDesc {
+  const float* R;
+  const float* pending;
+  const float* w_norm;
+  const float* gate;
+  const uint16_t* W_down;
+  const uint16_t* W_up;
+  Q8Weights q8;
+  float* out;
+  float* mean;
+  float* lo;
+  bool is_q8() const { return q8.Wd_q != nullptr; }
+};
+
+constexpr int kReadInputs = 8;
+
+// The byte ranges a T-token read takes as inputs: R, pending, w_norm, gate,
+// the two projections and (Q8_0) their block scales.
+void input_ranges(const ReadDesc& q, size_t N, int K, int T, Range (&r)[kReadInputs]) {
+  r[0] = range_of(q.R, T * N * 4);
+  r[1] = range_of(q.pending, T * N * 4);
+  r[2] = range_of(q.w_norm, N * 4);
+  r[3] = range_of(q.gate, N * 4);
+  if (q.is_q8()) {
+    r[4] = range_of(q.q8.Wd_q, N * K);
+    r[5] = range_of(q.q8.Wu_q, N * K);
+    r[6] = range_of(q.q8.Wd_scale, N * K / 32 * 2);
+    r[7] = range_of(q.q8.Wu_scale, N * K / 32 * 2);
+  } else {
+    r[4] = range_of(q.W_down, N * K * 2);
+    r[5] = range_of(q.W_up, N * K * 2);
+    r[6] = range_of(nullptr, 0);
+    r[7] = range_of(nullptr, 0);
+  }
+}
+
+// Its outputs out, mean and lo.
+void output_ranges(const ReadDesc& q, int n, int d, int K, int T, Range (&r)[3]) {
+  r[0] = range_of(q.out, (size_t)T * n * d * 4);
+  r[1] = range_of(q.mean, (size_t)T * d * 4);
+  r[2] = range_of(q.lo, (size_t)T * K * 4);
+}
+
+ReadDesc from_desc(const hc_read_desc& d) {
+  return ReadDesc{d.R, d.pending, d.w_norm, d.gate, d.W_down, d.W_up, Q8Weights{}, d.out, d.mean, d.lo};
+}
+
+ReadDesc from_desc(const hc_read_q8_desc& d) {
+  return ReadDesc{d.R,      d.pending, d.w_norm, d.gate, nullptr, nullptr,
+                  Q8Weights{d.Wd_q, d.Wd_scale, d.Wu_q, d.Wu_scale}, d.out, d.mean, d.lo};
+}
+
 // Records this read's outputs for (device, stream); returns whether its inputs
 // are disjoint from the outputs of the previous read recorded there.
-bool record_and_check(int device, void* stream, const Range (&ins)[6], const Range (&outs)[5]) {
+bool record_and_check(int device, void* stream, const Range (&ins)[kReadInputs], const Range (&outs)[5]) {
   std::lock_guard<std::mutex> lock(g_track_mutex);
   LastRead* slot = nullptr;
   for (auto& e : g_track) {
@@ -393,23 +466,23 @@ namespace {
 
 // Enqueues one validated read on `st` with partial-sum slot `part` (the two
 // kernels of the read; the caller alternates between its two slots).
-int enqueue_read(hc_read_t h, float* part, int device, const float* R, const float* w_norm,
-                 const uint16_t* W_down, const uint16_t* W_up, const float* gate, const float* pending,
-                 int T, float* out, float* mean, float* lo, float* r_out, float* rs, cudaStream_t st) {
+int enqueue_read(hc_read_t h, float* part, int device, const ReadDesc& q, int T, float* r_out, float* rs,
+                 cudaStream_t st) {
   const size_t N = (size_t)h->n * h->d;
-  const Range ins[6] = {range_of(R, T * N * 4),        range_of(pending, T * N * 4),
-                        range_of(w_norm, N * 4),        range_of(gate, N * 4),
-                        range_of(W_down, N * h->K * 2), range_of(W_up, N * h->K * 2)};
-  const Range outs[5] = {range_of(out, T * N * 4),  range_of(mean, (size_t)T * h->d * 4),
-                         range_of(lo, (size_t)T * h->K * 4), range_of(r_out, T * N * 4),
+  Range ins[kReadInputs];
+  input_ranges(q, N, h->K, T, ins);
+  const Range outs[5] = {range_of(q.out, T * N * 4),  range_of(q.mean, (size_t)T * h->d * 4),
+                         range_of(q.lo, (size_t)T * h->K * 4), range_of(r_out, T * N * 4),
                          range_of(rs, (size_t)T * h->n * 4)};
   const int independent = record_and_check(device, st, ins, outs) ? 1 : 0;
 
-  DownArgs da;
-  da.R = R;
-  da.P = pending;
-  da.w_norm = w_norm;
-  da.W_down = W_down;
+  DownArgs da{};
+  da.R = q.R;
+  da.P = q.pending;
+  da.w_norm = q.w_norm;
+  da.W_down = q.W_down;
+  da.Wq = q.q8.Wd_q;
+  da.Wscale = q.q8.Wd_scale;
   da.part = part;
   da.err = h->err;
   da.rs_out = rs;
@@ -418,28 +491,64 @@ int enqueue_read(hc_read_t h, float* part, int device, const float* R, const flo
   da.independent = independent;
   da.eps = h->eps;
 
-  UpArgs ua;
-  ua.R = R;
-  ua.P = pending;
-  ua.gate = gate;
-  ua.W_up = W_up;
+  UpArgs ua{};
+  ua.R = q.R;
+  ua.P = q.pending;
+  ua.gate = q.gate;
+  ua.W_up = q.W_up;
+  ua.Wq = q.q8.Wu_q;
+  ua.Wscale = q.q8.Wu_scale;
   ua.part = part;
-  ua.out = out;
-  ua.mean = mean;
-  ua.lo = lo;
+  ua.out = q.out;
+  ua.mean = q.mean;
+  ua.lo = q.lo;
   ua.r_out = r_out;
   ua.err = h->err;
   ua.T = T;
   ua.T_max = h->T_max;
   ua.independent = independent;
 
-  cudaError_t e = (h->d == 2560) ? launch_geometry<2560, 320>(T, da, ua, st)
-                                 : launch_geometry<4096, 512>(T, da, ua, st);
+  cudaError_t e;
+  if (q.is_q8()) {
+    e = (h->d == 2560) ? launch_geometry_q8<2560, 320>(T, da, ua, st) : launch_geometry_q8<4096, 512>(T, da, ua, st);
+  } else {
+    e = (h->d == 2560) ? launch_geometry<2560, 320>(T, da, ua, st) : launch_geometry<4096, 512>(T, da, ua, st);
+  }
   if (e != cudaSuccess) {
     cudaGetLastError();  // clear the sticky launch error for this thread
     return HC_ERR_CUDA;
   }
   return HC_OK;
+}
+
+// Argument checks of one read: required pointers set, every pointer 16-byte
+// aligned (Q8_0 scales included: they are copied in 8- and 16-byte pieces).
+int check_read(const ReadDesc& q, const float* r_out, const float* rs) {
+  if (!q.R || !q.w_norm || !q.gate || !q.out || !q.mean || !q.lo) return HC_ERR_ARG;
+  if (q.is_q8() ? (!q.q8.Wd_scale || !q.q8.Wu_q || !q.q8.Wu_scale || q.W_down || q.W_up) : (!q.W_down || !q.W_up)) {
+    return HC_ERR_ARG;
+  }
+  const void* ptrs[] = {q.R,           q.w_norm,      q.W_down, q.W_up, q.q8.Wd_q, q.q8.Wd_scale, q.q8.Wu_q,
+                        q.q8.Wu_scale, q.gate,        q.pending, q.out, q.mean,    q.lo,          r_out,
+                        rs};
+  for (const void* p : ptrs) {
+    if (p != nullptr && !aligned16(p)) return HC_ERR_ALIGN;
+  }
+  return HC_OK;
+}
+
+// One checked read on the handle's own partial-sum slots.
+int single_read(hc_read_t h, const ReadDesc& q, int T, float* r_out, float* rs, hc_stream_t stream) {
+  if (h == nullptr) return HC_ERR_ARG;
+  if (T < 1 || T > h->T_max) return HC_ERR_ARG;
+  const int c = check_read(q, r_out, rs);
+  if (c != HC_OK) return c;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return HC_ERR_CUDA;
+  if (cur != h->device) return HC_ERR_ARG;
+  float* part = h->part[h->parity];
+  h->parity ^= 1;
+  return enqueue_read(h, part, cur, q, T, r_out, rs, static_cast<cudaStream_t>(stream));
 }
 
 }  // namespace
@@ -448,21 +557,19 @@ HC_EXPORT int hc_read_ex(hc_read_t h, const float* R, const float* w_norm, const
                          const uint16_t* W_up, const float* gate, const float* pending, int T,
                          float* out, float* mean, float* lo, float* r_out, float* rs,
                          hc_stream_t stream) {
-  if (h == nullptr) return HC_ERR_ARG;
-  if (T < 1 || T > h->T_max) return HC_ERR_ARG;
-  if (!R || !w_norm || !W_down || !W_up || !gate || !out || !mean || !lo) return HC_ERR_ARG;
-  const void* ptrs[] = {R, w_norm, W_down, W_up, gate, pending, out, mean, lo, r_out, rs};
-  for (const void* p : ptrs) {
-    if (p != nullptr && !aligned16(p)) return HC_ERR_ALIGN;
-  }
-  int cur = -1;
-  if (cudaGetDevice(&cur) != cudaSuccess) return HC_ERR_CUDA;
-  if (cur != h->device) return HC_ERR_ARG;
+  if (W_down == nullptr || W_up == nullptr) return HC_ERR_ARG;
+  return single_read(h, ReadDesc{R, pending, w_norm, gate, W_down, W_up, Q8Weights{}, out, mean, lo}, T, r_out, rs,
+                     stream);
+}
 
-  float* part = h->part[h->parity];
-  h->parity ^= 1;
-  return enqueue_read(h, part, cur, R, w_norm, W_down, W_up, gate, pending, T, out, mean, lo, r_out, rs,
-                      static_cast<cudaStream_t>(stream));
+HC_EXPORT int hc_read_q8(hc_read_t h, const float* R, const float* w_norm, const int8_t* Wd_q,
+                         const uint16_t* Wd_scale, const int8_t* Wu_q, const uint16_t* Wu_scale,
+                         const float* gate, const float* pending, int T, float* out, float* mean, float* lo,
+                         float* r_out, float* rs, hc_stream_t stream) {
+  if (Wd_q == nullptr) return HC_ERR_ARG;
+  return single_read(
+      h, ReadDesc{R, pending, w_norm, gate, nullptr, nullptr, Q8Weights{Wd_q, Wd_scale, Wu_q, Wu_scale}, out, mean, lo},
+      T, r_out, rs, stream);
 }
 
 HC_EXPORT int hc_read(hc_read_t h, const float* R, const float* w_norm, const uint16_t* W_down,
@@ -486,7 +593,7 @@ int find_root(std::vector<int>& parent, int x) {
 // when an output of one overlaps an input or an output of the other, directly
 // or through other reads.  group[j] numbers the groups in order of first
 // appearance; returns how many there are.
-int group_reads(const hc_read_desc* descs, int count, int n, int d, int K, int T, int* group) {
+int group_reads(const ReadDesc* descs, int count, int n, int d, int K, int T, int* group) {
   const size_t N = (size_t)n * d;
   struct Out {
     Range r;
@@ -495,9 +602,8 @@ int group_reads(const hc_read_desc* descs, int count, int n, int d, int K, int T
   std::vector<Out> outs;
   outs.reserve(3 * (size_t)count);
   for (int j = 0; j < count; ++j) {
-    const hc_read_desc& q = descs[j];
-    const Range rs[3] = {range_of(q.out, T * N * 4), range_of(q.mean, (size_t)T * d * 4),
-                         range_of(q.lo, (size_t)T * K * 4)};
+    Range rs[3];
+    output_ranges(descs[j], n, d, K, T, rs);
     for (const Range& r : rs) {
       if (r.lo != r.hi) outs.push_back({r, j});
     }
@@ -508,12 +614,13 @@ int group_reads(const hc_read_desc* descs, int count, int n, int d, int K, int T
   std::vector<int> parent(count);
   std::iota(parent.begin(), parent.end(), 0);
   for (int j = 0; j < count; ++j) {
-    const hc_read_desc& q = descs[j];
-    const Range mine[9] = {range_of(q.R, T * N * 4),         range_of(q.pending, T * N * 4),
-                           range_of(q.w_norm, N * 4),         range_of(q.gate, N * 4),
-                           range_of(q.W_down, N * K * 2),     range_of(q.W_up, N * K * 2),
-                           range_of(q.out, T * N * 4),        range_of(q.mean, (size_t)T * d * 4),
-                           range_of(q.lo, (size_t)T * K * 4)};
+    Range mine[kReadInputs + 3];
+    Range ins[kReadInputs];
+    Range own[3];
+    input_ranges(descs[j], N, K, T, ins);
+    output_ranges(descs[j], n, d, K, T, own);
+    std::copy(ins, ins + kReadInputs, mine);
+    std::copy(own, own + 3, mine + kReadInputs);
     for (const Range& m : mine) {
       if (m.lo == m.hi) continue;
       // Outputs starting below m.hi, walked down while one of them may still
@@ -539,8 +646,8 @@ int group_reads(const hc_read_desc* descs, int count, int n, int d, int K, int T
 
 // Runs the reads of a batch on the handle's lanes, group g on lane g mod L,
 // each lane in the batch's order; forks from and joins back into `caller`.
-int run_lanes(hc_read_t h, const hc_read_desc* descs, int count, int T, const int* group, int lanes,
-              int device, cudaStream_t caller) {
+int run_lanes(hc_read_t h, const ReadDesc* descs, int count, int T, const int* group, int lanes, int device,
+              cudaStream_t caller) {
   if (cudaEventRecord(h->fork, caller) != cudaSuccess) {
     cudaGetLastError();
     return HC_ERR_CUDA;
@@ -554,11 +661,9 @@ int run_lanes(hc_read_t h, const hc_read_desc* descs, int count, int T, const in
   int status = forked == lanes ? HC_OK : HC_ERR_CUDA;
   for (int j = 0; j < count && status == HC_OK; ++j) {
     hc_read_s::Lane& ln = h->lanes[group[j] % lanes];
-    const hc_read_desc& q = descs[j];
     float* part = ln.part[ln.parity];
     ln.parity ^= 1;
-    status = enqueue_read(h, part, device, q.R, q.w_norm, q.W_down, q.W_up, q.gate, q.pending, T, q.out,
-                          q.mean, q.lo, nullptr, nullptr, ln.st);
+    status = enqueue_read(h, part, device, descs[j], T, nullptr, nullptr, ln.st);
   }
   // Every forked lane joins, also after a failure: a capture must not end
   // with work left on a lane.
@@ -581,7 +686,7 @@ int lanes_for(hc_read_t h, int groups) {
 }
 
 // One launch of the persistent kernel over descs[0..count) (count <= kWinMaxReads).
-int launch_window(hc_read_t h, const hc_read_desc* descs, int count, int T, cudaStream_t st) {
+int launch_window(hc_read_t h, const ReadDesc* descs, int count, int T, cudaStream_t st) {
   hc::WinArgs* a = new (std::nothrow) hc::WinArgs();
   if (a == nullptr) return HC_ERR_ARG;
   a->xbuf = h->xbuf;
@@ -594,7 +699,7 @@ int launch_window(hc_read_t h, const hc_read_desc* descs, int count, int T, cuda
   a->T = T;
   a->eps = h->eps;
   for (int j = 0; j < count; ++j) {
-    const hc_read_desc& d = descs[j];
+    const ReadDesc& d = descs[j];
     a->rd[j] = hc::WinRead{d.R, d.pending, d.w_norm, d.W_down, d.W_up, d.gate, d.out, d.mean, d.lo};
     a->chained[j] = (j > 0 && d.R == descs[j - 1].out) ? 1 : 0;
   }
@@ -609,82 +714,128 @@ int launch_window(hc_read_t h, const hc_read_desc* descs, int count, int T, cuda
   return HC_OK;
 }
 
-}  // namespace
+// Whether the persistent kernel covers a batch of T-token reads on this handle
+// (BF16 weights only).
+bool window_covers(hc_read_t h, int T, bool q8) { return !q8 && h->window && T <= 4; }
 
-HC_EXPORT int hc_read_batch_persistent(hc_read_t h, int T) {
-  if (h == nullptr || T < 1 || T > h->T_max) return HC_ERR_ARG;
-  return (h->window && T <= 4) ? 1 : 0;
-}
-
-HC_EXPORT int hc_read_batch(hc_read_t h, const hc_read_desc* descs, int count, int T, hc_stream_t stream) {
-  if (h == nullptr || descs == nullptr || count < 1) return HC_ERR_ARG;
-  if (T < 1 || T > h->T_max) return HC_ERR_ARG;
-  int cur = -1;
-  if (cudaGetDevice(&cur) != cudaSuccess) return HC_ERR_CUDA;
-  if (cur != h->device) return HC_ERR_ARG;
+// Argument checks of a whole batch (see hc_read_batch).
+int check_batch(hc_read_t h, const ReadDesc* descs, int count, int T) {
   const size_t N = (size_t)h->n * h->d;
   for (int j = 0; j < count; ++j) {
-    const hc_read_desc& d = descs[j];
-    if (!d.R || !d.w_norm || !d.W_down || !d.W_up || !d.gate || !d.out || !d.mean || !d.lo) return HC_ERR_ARG;
-    const void* ptrs[] = {d.R, d.w_norm, d.W_down, d.W_up, d.gate, d.pending, d.out, d.mean, d.lo};
-    for (const void* p : ptrs) {
-      if (p != nullptr && !aligned16(p)) return HC_ERR_ALIGN;
-    }
+    const ReadDesc& d = descs[j];
+    const int c = check_read(d, nullptr, nullptr);
+    if (c != HC_OK) return c;
+    if (d.is_q8() != descs[0].is_q8()) return HC_ERR_ARG;
     const Range p_in = range_of(d.pending, T * N * 4);
     if (overlaps(p_in, range_of(d.out, T * N * 4))) return HC_ERR_ARG;
     // Inputs may not depend on earlier reads of the batch, except R taking
     // the previous read's out exactly (a chained read, whose R is never
-    // loaded: it is the previous read's output tile, still on chip).
+    // loaded by the persistent kernel: it is the previous read's output
+    // tile, still on chip).
     const bool chained = j > 0 && d.R == descs[j - 1].out;
     const Range r_in = chained ? range_of(nullptr, 0) : range_of(d.R, T * N * 4);
     for (int i = 0; i < j; ++i) {
-      const hc_read_desc& o = descs[i];
-      const Range outs[3] = {range_of(o.out, T * N * 4), range_of(o.mean, (size_t)T * h->d * 4),
-                             range_of(o.lo, (size_t)T * h->K * 4)};
-      for (int k = 0; k < 3; ++k) {
-        if (overlaps(r_in, outs[k]) || overlaps(p_in, outs[k])) return HC_ERR_ARG;
+      Range outs[3];
+      output_ranges(descs[i], h->n, h->d, h->K, T, outs);
+      for (const Range& o : outs) {
+        if (overlaps(r_in, o) || overlaps(p_in, o)) return HC_ERR_ARG;
       }
     }
   }
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return HC_OK;
+}
+
+// How a checked batch runs: 0 read by read, 1 the persistent kernel, L >= 2 lanes.
+int plan_batch(hc_read_t h, const ReadDesc* descs, int count, int T, int* group) {
   if (count >= 2 && lanes_for(h, count) >= 2) {
-    std::vector<int> group(count);
-    const int lanes = lanes_for(h, group_reads(descs, count, h->n, h->d, h->K, T, group.data()));
-    if (lanes >= 2) return run_lanes(h, descs, count, T, group.data(), lanes, cur, st);
+    const int lanes = lanes_for(h, group_reads(descs, count, h->n, h->d, h->K, T, group));
+    if (lanes >= 2) return lanes;
   }
-  if (hc_read_batch_persistent(h, T) != 1) {
-    // Shapes the persistent kernel does not cover: the reads one by one.
-    for (int j = 0; j < count; ++j) {
-      const hc_read_desc& d = descs[j];
-      const int r = hc_read_ex(h, d.R, d.w_norm, d.W_down, d.W_up, d.gate, d.pending, T, d.out, d.mean, d.lo,
-                               nullptr, nullptr, stream);
+  return window_covers(h, T, descs[0].is_q8()) ? 1 : 0;
+}
+
+int run_batch(hc_read_t h, const std::vector<ReadDesc>& descs, int T, hc_stream_t stream) {
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return HC_ERR_CUDA;
+  if (cur != h->device) return HC_ERR_ARG;
+  const int count = (int)descs.size();
+  const int c = check_batch(h, descs.data(), count, T);
+  if (c != HC_OK) return c;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  std::vector<int> group(count);
+  const int plan = plan_batch(h, descs.data(), count, T, group.data());
+  if (plan >= 2) return run_lanes(h, descs.data(), count, T, group.data(), plan, cur, st);
+  if (plan == 0) {
+    for (const ReadDesc& d : descs) {
+      float* part = h->part[h->parity];
+      h->parity ^= 1;
+      const int r = enqueue_read(h, part, cur, d, T, nullptr, nullptr, st);
       if (r != HC_OK) return r;
     }
     return HC_OK;
   }
   for (int j0 = 0; j0 < count; j0 += hc::kWinMaxReads) {
-    const int r = launch_window(h, descs + j0, count - j0 < hc::kWinMaxReads ? count - j0 : hc::kWinMaxReads, T, st);
+    const int r = launch_window(h, descs.data() + j0, std::min(count - j0, hc::kWinMaxReads), T, st);
     if (r != HC_OK) return r;
   }
   // A later hc_read that consumes the last read's outputs must wait for them.
-  const hc_read_desc& last = descs[count - 1];
-  const Range ins[6] = {range_of(last.R, T * N * 4),         range_of(last.pending, T * N * 4),
-                        range_of(last.w_norm, N * 4),         range_of(last.gate, N * 4),
-                        range_of(last.W_down, N * h->K * 2), range_of(last.W_up, N * h->K * 2)};
+  const size_t N = (size_t)h->n * h->d;
+  const ReadDesc& last = descs[count - 1];
+  Range ins[kReadInputs];
+  input_ranges(last, N, h->K, T, ins);
   const Range outs[5] = {range_of(last.out, T * N * 4), range_of(last.mean, (size_t)T * h->d * 4),
                          range_of(last.lo, (size_t)T * h->K * 4), range_of(nullptr, 0), range_of(nullptr, 0)};
   record_and_check(cur, stream, ins, outs);
   return HC_OK;
 }
 
+template <class Desc>
+std::vector<ReadDesc> read_descs(const Desc* descs, int count) {
+  std::vector<ReadDesc> v;
+  v.reserve(count);
+  for (int j = 0; j < count; ++j) v.push_back(from_desc(descs[j]));
+  return v;
+}
+
+}  // namespace
+
+HC_EXPORT int hc_read_batch_persistent(hc_read_t h, int T) {
+  if (h == nullptr || T < 1 || T > h->T_max) return HC_ERR_ARG;
+  return window_covers(h, T, false) ? 1 : 0;
+}
+
+HC_EXPORT int hc_read_batch(hc_read_t h, const hc_read_desc* descs, int count, int T, hc_stream_t stream) {
+  if (h == nullptr || descs == nullptr || count < 1) return HC_ERR_ARG;
+  if (T < 1 || T > h->T_max) return HC_ERR_ARG;
+  for (int j = 0; j < count; ++j) {
+    if (descs[j].W_down == nullptr || descs[j].W_up == nullptr) return HC_ERR_ARG;
+  }
+  return run_batch(h, read_descs(descs, count), T, stream);
+}
+
+HC_EXPORT int hc_read_batch_q8(hc_read_t h, const hc_read_q8_desc* descs, int count, int T, hc_stream_t stream) {
+  if (h == nullptr || descs == nullptr || count < 1) return HC_ERR_ARG;
+  if (T < 1 || T > h->T_max) return HC_ERR_ARG;
+  for (int j = 0; j < count; ++j) {
+    if (descs[j].Wd_q == nullptr) return HC_ERR_ARG;
+  }
+  return run_batch(h, read_descs(descs, count), T, stream);
+}
+
 HC_EXPORT int hc_read_batch_plan(hc_read_t h, const hc_read_desc* descs, int count, int T) {
   if (h == nullptr || descs == nullptr || count < 1 || T < 1 || T > h->T_max) return HC_ERR_ARG;
-  if (count >= 2) {
-    std::vector<int> group(count);
-    const int lanes = lanes_for(h, group_reads(descs, count, h->n, h->d, h->K, T, group.data()));
-    if (lanes >= 2) return lanes;
+  std::vector<int> group(count);
+  return plan_batch(h, read_descs(descs, count).data(), count, T, group.data());
+}
+
+HC_EXPORT int hc_read_batch_q8_plan(hc_read_t h, const hc_read_q8_desc* descs, int count, int T) {
+  if (h == nullptr || descs == nullptr || count < 1 || T < 1 || T > h->T_max) return HC_ERR_ARG;
+  std::vector<int> group(count);
+  const std::vector<ReadDesc> v = read_descs(descs, count);
+  for (const ReadDesc& d : v) {
+    if (!d.is_q8()) return HC_ERR_ARG;
   }
-  return hc_read_batch_persistent(h, T) == 1 ? 1 : 0;
+  return plan_batch(h, v.data(), count, T, group.data());
 }
 
 HC_EXPORT int hc_read_set_batch_lanes(hc_read_t h, int lanes) {
@@ -697,7 +848,15 @@ HC_EXPORT int hc_read_set_batch_lanes(hc_read_t h, int lanes) {
 HC_EXPORT int hc_read_batch_groups(const hc_read_desc* descs, int count, int n, int d, int K, int T,
                                    int* group) {
   if (descs == nullptr || group == nullptr || count < 1 || T < 1 || n < 1 || d < 1 || K < 1) return HC_ERR_ARG;
-  return group_reads(descs, count, n, d, K, T, group);
+  return group_reads(read_descs(descs, count).data(), count, n, d, K, T, group);
+}
+
+HC_EXPORT int hc_read_batch_q8_groups(const hc_read_q8_desc* descs, int count, int n, int d, int K, int T,
+                                      int* group) {
+  if (descs == nullptr || group == nullptr || count < 1 || T < 1 || n < 1 || d < 1 || K < 1) return HC_ERR_ARG;
+  // Scale rows are K/32 or n*d/32 binary16 values: both widths multiples of 32.
+  if ((n * d) % 32 != 0 || K % 32 != 0) return HC_ERR_ARG;
+  return group_reads(read_descs(descs, count).data(), count, n, d, K, T, group);
 }
 
 HC_EXPORT int hc_read_check(hc_read_t h) {
@@ -867,15 +1026,14 @@ HC_EXPORT int hc_read_noalloc(int n, int d, int K, float eps, const float* R, co
   // that consumes these outputs waits for them.  (This path has one scratch
   // slot and always waits for the previous kernel before it computes.)
   const size_t N = (size_t)n * d;
-  const Range ins[6] = {range_of(R, T * N * 4),     range_of(pending, T * N * 4),
-                        range_of(w_norm, N * 4),     range_of(gate, N * 4),
-                        range_of(W_down, N * K * 2), range_of(W_up, N * K * 2)};
+  Range ins[kReadInputs];
+  input_ranges(ReadDesc{R, pending, w_norm, gate, W_down, W_up, Q8Weights{}, out, mean, lo}, N, K, T, ins);
   const Range outs[5] = {range_of(out, T * N * 4), range_of(mean, (size_t)T * d * 4),
                          range_of(lo, (size_t)T * K * 4), range_of(nullptr, 0),
                          range_of(nullptr, 0)};
   record_and_check(dev, stream, ins, outs);
 
-  DownArgs da;
+  DownArgs da{};
   da.R = R;
   da.P = pending;
   da.w_norm = w_norm;
@@ -888,7 +1046,7 @@ HC_EXPORT int hc_read_noalloc(int n, int d, int K, float eps, const float* R, co
   da.independent = 0;
   da.eps = eps;
 
-  UpArgs ua;
+  UpArgs ua{};
   ua.R = R;
   ua.P = pending;
   ua.gate = gate;

@@ -104,6 +104,27 @@ int hc_read_ex(hc_read_t h, const float* R, const float* w_norm, const uint16_t*
                float* out, float* mean, float* lo, float* r_out, float* rs,
                hc_stream_t stream);
 
+/* hc_read over Q8_0 copies of the two projections.
+ *
+ * The pages name a Q8_0 read of the hyper-connection projections ("#2812
+ * sycl: STRATA_GR_FUSED=1 ...", "Summary": the two-kernel read "is the
+ * structure of the Q8_0 read of the PR it builds on"; #2810 "reads the Q8_0
+ * hyper-connection projections") without its block layout.  This library
+ * reads Q8_0 as: every row of a weight matrix in blocks of 32 consecutive
+ * values along the dot-product axis, each block one IEEE binary16 scale and
+ * 32 int8 values, weight = scale * q, with quants and scales in separate
+ * arrays:
+ *   Wd_q     [K][n*d] int8,   Wd_scale [K][n*d/32] binary16 bits (W_down),
+ *   Wu_q     [n*d][K] int8,   Wu_scale [n*d][K/32] binary16 bits (W_up),
+ * row-major.  Everything else as hc_read_ex (the same norm, partial sums,
+ * epilogue and outputs).  Every pointer, scales included, must be 16-byte
+ * aligned (HC_ERR_ALIGN).  The MMA takes the int8 values as
+ * BF16 (exact) and applies each block's scale to the block's FP32 sum. */
+int hc_read_q8(hc_read_t h, const float* R, const float* w_norm, const int8_t* Wd_q,
+               const uint16_t* Wd_scale, const int8_t* Wu_q, const uint16_t* Wu_scale,
+               const float* gate, const float* pending, int T, float* out, float* mean, float* lo,
+               float* r_out, float* rs, hc_stream_t stream);
+
 /* One read of a batch: the arguments of hc_read, same meaning and layouts. */
 typedef struct {
   const float* R;
@@ -172,6 +193,39 @@ int hc_read_set_batch_lanes(hc_read_t h, int lanes);
  * Host logic only: the pointers are compared, never dereferenced, and no
  * device is needed. */
 int hc_read_batch_groups(const hc_read_desc* descs, int count, int n, int d, int K, int T, int* group);
+
+/* One Q8_0 read of a batch: the arguments of hc_read_q8, same meaning and
+ * layouts. */
+typedef struct {
+  const float* R;
+  const float* w_norm;
+  const int8_t* Wd_q;
+  const uint16_t* Wd_scale;
+  const int8_t* Wu_q;
+  const uint16_t* Wu_scale;
+  const float* gate;
+  const float* pending;  /* NULL = no pending write */
+  float* out;
+  float* mean;
+  float* lo;
+} hc_read_q8_desc;
+
+/* hc_read_batch over Q8_0 reads: the same rules on the reads' buffers, the
+ * same groups (the scale arrays count as inputs) and the same internal
+ * streams.  The persistent kernel takes BF16 weights only, so a one-group
+ * Q8_0 batch runs read by read on `stream`.  Alignment as hc_read_q8. */
+int hc_read_batch_q8(hc_read_t h, const hc_read_q8_desc* descs, int count, int T, hc_stream_t stream);
+
+/* How hc_read_batch_q8 would run this batch: 0 read by read on the caller's
+ * stream, L >= 2 on L internal streams; HC_ERR_ARG as hc_read_batch_plan.
+ * Enqueues nothing. */
+int hc_read_batch_q8_plan(hc_read_t h, const hc_read_q8_desc* descs, int count, int T);
+
+/* hc_read_batch_groups for Q8_0 reads: the inputs are R, pending, w_norm,
+ * gate, Wd_q and Wu_q ([K][n d] and [n d][K] bytes) and Wd_scale and Wu_scale
+ * ([K][n d / 32] and [n d][K / 32] binary16); HC_ERR_ARG also when n d or K
+ * is not a multiple of 32.  Host logic only. */
+int hc_read_batch_q8_groups(const hc_read_q8_desc* descs, int count, int n, int d, int K, int T, int* group);
 
 /* 1 if hc_read_batch on this handle runs batches of T-token reads as the
  * persistent kernel, 0 if it runs them read by read; HC_ERR_ARG for a NULL

@@ -208,3 +208,110 @@ def test_group_count_return_and_argument_errors():
     assert lib.hc_read_batch_groups(arr, 3, *G, 0, out) == hc.HC_ERR_ARG
     assert lib.hc_read_batch_groups(arr, 3, *G, 1, None) == hc.HC_ERR_ARG
     assert lib.hc_read_batch_plan(None, arr, 3, 1) == hc.HC_ERR_ARG
+
+
+# ---- Q8_0 reads: quants one byte per weight, scales as further inputs
+
+ORDER_IN_Q8 = ("R", "pending", "w_norm", "gate", "Wd_q", "Wd_scale", "Wu_q", "Wu_scale")
+
+
+def sizes_q8(T):
+    n, d, K = G
+    sz = sizes(T)
+    return {**{k: sz[k] for k in ("R", "pending", "w_norm", "gate", "out", "mean", "lo")},
+            "Wd_q": N * K, "Wu_q": N * K, "Wd_scale": N * K // 32 * 2, "Wu_scale": N * K // 32 * 2}
+
+
+def q8_weights(arena):
+    sz = sizes_q8(1)
+    return {k: arena.take(sz[k]) for k in ("w_norm", "gate", "Wd_q", "Wd_scale", "Wu_q", "Wu_scale")}
+
+
+def brute_partition_q8(reads, T):
+    sz = sizes_q8(T)
+
+    def rng(r, k):
+        a = r.get(k)
+        return None if a is None else (a, a + sz[k])
+
+    m = len(reads)
+    parent = list(range(m))
+
+    def find(x):
+        while parent[x] != x:
+            x = parent[x]
+        return x
+
+    for j in range(m):
+        for k in range(m):
+            if j != k and any(a and b and a[0] < b[1] and b[0] < a[1]
+                              for a in (rng(reads[j], o) for o in ORDER_OUT)
+                              for b in (rng(reads[k], o) for o in ORDER_IN_Q8 + ORDER_OUT)):
+                parent[find(j)] = find(k)
+    ids = {}
+    return [ids.setdefault(find(j), len(ids)) for j in range(m)]
+
+
+def q8_groups(reads, T):
+    return hc.hc_read_batch_q8_groups(G, reads, T)
+
+
+def test_q8_output_into_a_scale_array_links_reads():
+    a = Arena()
+    w = q8_weights(a)
+    r0 = read(a, 1, w)
+    far = Arena(base=1 << 44)
+    r1 = read(far, 1, q8_weights(far))
+    r1["Wu_scale"] = r0["lo"]  # scales are inputs: written by read 0
+    assert q8_groups([r0, r1], 1) == [0, 0]
+    # the byte just past read 1's Wd_scale array is not part of it
+    r2 = read(far, 1, q8_weights(far))
+    r0b = read(a, 1, w, lo=r2["Wd_scale"] + sizes_q8(1)["Wd_scale"])  # 1280 bytes, inside the gap
+    assert q8_groups([r0b, r2], 1) == [0, 1]
+
+
+def test_q8_quant_range_is_one_byte_per_weight():
+    a = Arena()
+    w = q8_weights(a)
+    r0 = read(a, 1, w)
+    r1 = read(a, 1, w)
+    # an output placed right after r0's Wd_q bytes (N*K, not N*K*2) stays apart
+    r1["lo"] = w["Wd_q"] + N * G[2]
+    assert q8_groups([r0, r1], 1) == [0, 1]
+    r1["lo"] = w["Wd_q"] + N * G[2] - 4
+    assert q8_groups([r0, r1], 1) == [0, 0]
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_q8_random_layouts_match_brute_force(seed):
+    rnd = random.Random(100 + seed)
+    T = rnd.choice((1, 2, 4, 8))
+    sz = sizes_q8(T)
+    a = Arena()
+    pool = [a.take(sz["R"]) for _ in range(6)]
+    wsets = [q8_weights(a) for _ in range(3)]
+    reads = []
+    for _ in range(rnd.randint(1, 24)):
+        r = read(a, T, rnd.choice(wsets))
+        for k in ("R", "pending", "out", "mean", "lo"):
+            if rnd.random() < 0.25:
+                r[k] = rnd.choice(pool) + 256 * rnd.randint(0, 3)
+        for k in ("Wd_scale", "Wu_scale"):
+            if rnd.random() < 0.1:
+                r[k] = rnd.choice(pool) + 2 * rnd.randint(0, 7)
+        reads.append(r)
+    assert q8_groups(reads, T) == brute_partition_q8(reads, T)
+
+
+def test_q8_group_argument_errors():
+    lib = hc.load()
+    a = Arena()
+    w = q8_weights(a)
+    reads = [read(a, 1, w) for _ in range(2)]
+    arr = hc._binding._q8_descs(G, reads, 1)
+    out = (ctypes.c_int * 2)()
+    assert lib.hc_read_batch_q8_groups(arr, 2, *G, 1, out) == 2
+    assert lib.hc_read_batch_q8_groups(arr, 2, 4, 2560, 300, 1, out) == hc.HC_ERR_ARG  # K not a multiple of 32
+    assert lib.hc_read_batch_q8_groups(None, 2, *G, 1, out) == hc.HC_ERR_ARG
+    assert lib.hc_read_batch_q8_plan(None, arr, 2, 1) == hc.HC_ERR_ARG
+    assert lib.hc_read_batch_q8(None, arr, 2, 1, None) == hc.HC_ERR_ARG

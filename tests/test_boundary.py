@@ -61,3 +61,4 @@ def test_null_handle_rejected(lib):
     lib.hc_read_destroy(None)
     assert lib.hc_graph_launch(None, None) == hc.HC_ERR_ARG
     assert lib.hc_graph_end(None, None) == hc.HC_ERR_ARG
+    assert lib.hc_read_q8(None, *([None] * 8), 1, *([None] * 6)) == hc.HC_ERR_ARG
