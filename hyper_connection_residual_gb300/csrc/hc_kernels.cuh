@@ -36,8 +36,8 @@
 // sycl: STRATA_GR_FUSED=1, the two-kernel BF16 hyper-connection read
 // (opt-in)", section "What changed"): a CTA owns 32 rows of W_down x one slab
 // of d/4 columns.  It commits the pending write for its slab, stages
-// x = R' * w_norm unscaled with the slab's sums of squares and forms 32
-// partial dot products per token (lane = row, so the x reads are shared-memory
+// x = R' * w_norm (rs not yet applied), accumulates the squares over its
+// slab and forms 32 partial dot products per token (lane = row, so the x reads are shared-memory
 // broadcasts).  The cluster of the stream's four slabs then sums the slabs in
 // a fixed order, applies rs and writes part[s][t][k] = rs[t][s] * (slab sum).
 // Partials live in one scratch slot per handle: a read's down kernel writes

@@ -6,8 +6,8 @@
  *   committed (R_out), a per-stream RMS norm's sums of squares give rs, the
  *   BF16 down projection of R' * w_norm is scaled by rs per stream into lo, and
  *   the BF16 up projection of lo feeds an epilogue of pending write, gate and
- *   stream mean.  Strata pull request #2070 (Turing up/down kernels): 96 reads
- *   per window, 13 MB of BF16 weights per read.  The pages give no formula for
+ *   stream mean.  Strata pull request #2070 (Turing up/down kernels): a verify
+ *   window runs 96 reads, each moving about 13 MB of BF16 projection weights.  The pages give no formula for
  *   the epilogue; this library defines it as written below.
  *
  * For T tokens, n = 4 streams of width d, N = n*d, down width K, i = s*d + c:
@@ -106,20 +106,21 @@ int hc_read_ex(hc_read_t h, const float* R, const float* w_norm, const uint16_t*
 
 /* hc_read over Q8_0 copies of the two projections.
  *
- * The pages name a Q8_0 read of the hyper-connection projections ("#2812
- * sycl: STRATA_GR_FUSED=1 ...", "Summary": the two-kernel read "is the
- * structure of the Q8_0 read of the PR it builds on"; #2810 "reads the Q8_0
- * hyper-connection projections") without its block layout.  This library
- * reads Q8_0 as: every row of a weight matrix in blocks of 32 consecutive
- * values along the dot-product axis, each block one IEEE binary16 scale and
+ * The pages say that this two-kernel read follows the structure of an
+ * earlier read over Q8_0 copies of the projections, switched on by
+ * STRATA_HC_Q8=1 ("#2812 sycl: STRATA_GR_FUSED=1, the two-kernel BF16
+ * hyper-connection read (opt-in)", sections "Summary" and "Extra Notes"),
+ * but not how Q8_0 lays out its blocks.  This library reads Q8_0 as: every
+ * row of a weight matrix in blocks of 32 consecutive values along the
+ * dot-product axis, each block one IEEE binary16 scale and
  * 32 int8 values, weight = scale * q, with quants and scales in separate
  * arrays:
  *   Wd_q     [K][n*d] int8,   Wd_scale [K][n*d/32] binary16 bits (W_down),
  *   Wu_q     [n*d][K] int8,   Wu_scale [n*d][K/32] binary16 bits (W_up),
  * row-major.  Everything else as hc_read_ex (the same norm, partial sums,
  * epilogue and outputs).  Every pointer, scales included, must be 16-byte
- * aligned (HC_ERR_ALIGN).  The MMA takes the int8 values as
- * BF16 (exact) and applies each block's scale to the block's FP32 sum. */
+ * aligned (HC_ERR_ALIGN).  The MMA takes the int8 values as BF16 (exact)
+ * and applies each block's scale to the block's FP32 sum. */
 int hc_read_q8(hc_read_t h, const float* R, const float* w_norm, const int8_t* Wd_q,
                const uint16_t* Wd_scale, const int8_t* Wu_q, const uint16_t* Wu_scale,
                const float* gate, const float* pending, int T, float* out, float* mean, float* lo,

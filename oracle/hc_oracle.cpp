@@ -11,10 +11,12 @@
 //        read (opt-in)", sections "Summary" and "What changed"
 //        (gr_fused_down_kernel / gr_fused_up_kernel descriptions): the read is a
 //        per-stream RMS norm, a BF16 down projection whose partial sums are
-//        scaled by rs per stream, a BF16 up projection, then an epilogue of
-//        "pending write, gate, stream mean"; R_out is "the pending write".
+//        scaled by rs per stream, a BF16 up projection, then an epilogue that
+//        commits the pending write, applies the gate and averages the
+//        streams; R_out is the residual with the pending write committed.
 //   [P1] Strata pull request #2070 (Turing up/down kernels), first paragraph:
-//        96 reads per window, 13 MB of BF16 weights each.
+//        a verify window runs 96 reads, each moving about 13 MB of BF16
+//        projection weights.
 //   The pages give no formula for the epilogue.  This library fixes it as
 //        out = R' + sigmoid(g) * (W_up . lo),   m[c] = mean_s out[s, c],
 //   with R' = fl32(R + P) the residual after the pending write P.
@@ -28,9 +30,10 @@
 // row-major.  w_norm and gate have N entries.
 //
 // The Q8_0 read (hc_oracle_read_q8) is the same read over Q8_0 copies of the
-// two projections [P4 "Summary" and "Extra Notes": "STRATA_HC_Q8=1 reads the
-// Q8_0 hyper-connection projections", "the Q8_0 copies' extra VRAM"].  The
-// pages give no block layout; this library reads Q8_0 as: every row of a
+// two projections [P4, sections "Summary" and "Extra Notes": the branch
+// builds on an earlier one whose read takes Q8_0 copies of both projections
+// (switched on by STRATA_HC_Q8=1), copies that cost device memory on top of
+// the BF16 weights].  The pages give no block layout; this library reads Q8_0 as: every row of a
 // weight matrix in blocks of 32 consecutive values along the dot-product axis
 // (the columns of W_down [K][N], the columns of W_up [N][K]), each block one
 // IEEE binary16 scale and 32 int8 values, weight = scale * q.  Quants and
@@ -97,7 +100,8 @@ void hc_oracle_commit(int N, int T, const float* R, const float* P, float* r_out
   }
 }
 
-// Step 2 [P4 "What changed": the slab's sums of squares; "rs per stream"].
+// Step 2 [P4, "What changed": the down kernel accumulates squares over its
+// slab, and rs scales the partial sums stream by stream].
 // ss[t][s] = sum_c R'[t][s*d+c]^2 ; rs[t][s] = 1 / sqrt(ss[t][s] / d + eps).
 void hc_oracle_rms(int n, int d, int T, double eps, const float* r_prime,
                    double* ss, double* rs) {
@@ -155,8 +159,9 @@ void hc_oracle_up(int N, int K, int T, const uint16_t* W_up, const double* lo,
   }
 }
 
-// Step 5 [P4 "What changed": "the default read's epilogue: pending write,
-// gate, stream mean"; the formula is this library's reading, see the header].
+// Step 5 [P4, "What changed": the up kernel ends with the default read's
+// epilogue, which commits the pending write, applies the gate and averages
+// the streams; the formula is this library's reading, see the header].
 // out[t][i] = R'[t][i] + sigmoid(g[i]) * u[t][i], sigmoid(x) = 1 / (1 + exp(-x));
 // m[t][c] = (1/n) * sum_s out[t][s*d+c].
 void hc_oracle_epilogue(int n, int d, int T, const float* r_prime, const float* gate,
