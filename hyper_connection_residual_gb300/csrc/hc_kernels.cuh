@@ -290,7 +290,15 @@ __global__ void __launch_bounds__(kThreads, D == 2560 ? 3 : 2) hc_down_kernel(co
     ptx::bulk_g2s(w_s + lane * G::DN_PITCH, a.W_down + (size_t)(row0 + lane) * G::N + col0,
                   G::SLAB * 2, bar_w, once);
   }
-  ptx::launch_dependents();
+  // An independent read of one token group lets its up kernel launch only
+  // at the end of this kernel: the up CTAs then hold SM slots for less time
+  // and more reads of a batch overlap (measured on six streams: 2.58 ->
+  // 2.53-2.56 us per read at T = 1, 2.70 -> 2.64-2.67 at T = 4).  Chained
+  // reads keep the early launch: there the up kernel's weights must stream
+  // while this kernel waits (96 chained calls: 5.9 us per read, 7.3 with a
+  // late launch).  Reads of two token groups measured slower with it.
+  const bool late_launch = a.independent && a.T <= TT;
+  if (!late_launch) ptx::launch_dependents();
   __syncthreads();  // the mbarriers are initialised before any thread waits on them
   // w_norm is a parameter: wait for it before the previous kernel finishes.
   bool ok = true;
@@ -412,6 +420,7 @@ __global__ void __launch_bounds__(kThreads, D == 2560 ? 3 : 2) hc_down_kernel(co
     drain(bar_n, 0);
     drain(bar_w, 0);
   }
+  if (late_launch) ptx::launch_dependents();
   // One cluster barrier: every slab's pushes are visible to the leader.
   ptx::cluster_arrive_release();
   ptx::cluster_wait();

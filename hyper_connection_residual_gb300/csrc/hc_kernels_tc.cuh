@@ -233,7 +233,10 @@ __global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_down_tc_k
   static_assert(G::DN_F4 <= kThreads, "one float4 per thread and token");
   const float4 wn = c4 < G::DN_F4 ? __ldg(reinterpret_cast<const float4*>(a.w_norm + col0) + c4)
                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-  ptx::launch_dependents();
+  // Late launch of the up kernel for independent reads of one token group,
+  // as in hc_down_kernel.
+  const bool late_launch = a.independent && a.T <= TG;
+  if (!late_launch) ptx::launch_dependents();
   __syncthreads();  // the mbarriers are initialised before any thread waits on them
   bool ok = true;
   // R, P and the scratch slot belong to the previous kernel until its end
@@ -421,6 +424,7 @@ __global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_down_tc_k
     __syncthreads();
   }
   if (!ok) drain(bar_w, 0);
+  if (late_launch) ptx::launch_dependents();
   ptx::cluster_arrive_release();
   ptx::cluster_wait();
   if (rank != 0) {
