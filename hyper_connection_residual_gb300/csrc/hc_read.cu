@@ -1,6 +1,8 @@
 // Host side of the C ABI declared in include/hc_read.h: handle and scratch
 // management, argument validation, kernel selection and launch with
 // programmatic dependent launch, CUDA-graph helpers.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -13,6 +15,7 @@
 
 #include "hc_kernels.cuh"
 #include "hc_kernels_tc.cuh"
+#include "hc_kernels_umma.cuh"
 #include "hc_read.h"
 #include "hc_window.cuh"
 
@@ -22,6 +25,17 @@
 // (cold reads, d = 2560): one stream 5.2 us per read at T = 1; 4 / 6 / 8
 // streams 2.60 / 2.52 / 2.51 us; at T = 8 6.9 -> 3.88 / 3.79 / 3.82 us.
 constexpr int kBatchLanes = 6;
+
+// The tensor maps of the W_down matrices a handle has seen (boxes of 64
+// columns x 64 rows, for the tensor-memory down kernel), by address: a map
+// holds only the address, sizes and strides, so an entry stays valid for
+// the handle's geometry whatever the memory holds.
+struct MapCache {
+  static constexpr int kSlots = 64;
+  const void* down[kSlots];
+  CUtensorMap maps[kSlots];
+  unsigned next;
+};
 
 struct hc_read_s {
   int n, d, K, T_max, device;
@@ -49,6 +63,7 @@ struct hc_read_s {
     float* part[2];
     int parity;
   } lanes[kBatchLanes];
+  MapCache* map_cache;  // created on first use
   int nlanes;         // lanes created (0: batches run on the caller's stream only)
   int batch_lanes;    // most lanes a batch may use (hc_read_set_batch_lanes)
   cudaEvent_t fork;
@@ -94,10 +109,10 @@ void destroy_lanes(hc_read_s* h) {
 // Launch configuration with programmatic dependent launch and, when
 // cluster_x > 1, thread-block clusters of cluster_x CTAs along x.
 cudaLaunchConfig_t pdl_config(dim3 grid, size_t smem, cudaStream_t st, cudaLaunchAttribute* attr,
-                              unsigned cluster_x) {
+                              unsigned cluster_x, unsigned threads = hc::kThreads) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(hc::kThreads);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -137,8 +152,17 @@ cudaError_t configure_tc() {
 }
 
 template <int D, int KD>
+cudaError_t configure_umma() {
+  return cudaFuncSetAttribute(hc::hc_down_u_kernel<D, KD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              hc::UGeo<D, KD>::DN_BYTES);
+}
+
+template <int D, int KD>
 cudaError_t configure_geometry() {
   cudaError_t e;
+  if constexpr (D == 2560) {
+    if ((e = configure_umma<D, KD>()) != cudaSuccess) return e;
+  }
   if ((e = configure_one<D, KD, 1>()) != cudaSuccess) return e;
   if ((e = configure_tc<D, KD, 1, false>()) != cudaSuccess) return e;
   if ((e = configure_tc<D, KD, 2, false>()) != cudaSuccess) return e;
@@ -176,6 +200,59 @@ cudaError_t launch_pair_tc(const DownArgs& da, const UpArgs& ua, cudaStream_t st
   return cudaLaunchKernelEx(&c2, hc::hc_up_tc_kernel<D, KD, NT, Q8>, ua);
 }
 
+// The driver's tensor-map encoder (null when the driver does not offer it;
+// the reads then take the mma.sync kernels).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || p == nullptr) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// Tensor map of a row-major BF16 matrix [rows][cols] read in boxes of 64
+// columns x box_rows rows with the 128-byte swizzle.
+bool encode_bf16_tiles(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The tensor-memory down kernel (all T <= 8 in one pass) and the mma.sync
+// up kernel of 4-token groups (d = 2560, K = 320), for T = 5..8.  Measured
+// on six streams with independent reads: 3.42 -> 3.14 us per read at T = 5,
+// 3.56 -> 3.26 at T = 8; at T = 2..4 the pair is 2-3 % slower than the
+// mma.sync pair, which keeps those.  The choice depends on the read's shape
+// only, never on what ran before it, so a read's bits do not depend on its
+// history (direct calls, batches and graph replays agree).
+template <int D, int KD>
+cudaError_t launch_pair_u(const DownArgs& da, const UpArgs& ua, const CUtensorMap& w_down, cudaStream_t st) {
+  using U = hc::UGeo<D, KD>;
+  using G = hc::Geo<D, KD>;
+  hc::DownUArgs dargs;
+  dargs.w = w_down;
+  dargs.a = da;
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t c1 = pdl_config(dim3(U::CHUNKS, U::ROW_GROUPS), U::DN_BYTES, st, attr, U::CPS, U::THREADS);
+  cudaError_t e = cudaLaunchKernelEx(&c1, hc::hc_down_u_kernel<D, KD>, dargs);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr2[2];
+  cudaLaunchConfig_t c2 = pdl_config(dim3(G::UP_CTAS), hc::UpTcSmem<D, KD, 1>::bytes(ua.T), st, attr2, 1);
+  return cudaLaunchKernelEx(&c2, hc::hc_up_tc_kernel<D, KD, 1>, ua);
+}
+
 // From T = 2 on the tensor-core kernels are faster on GB300 (measured: T=2
 // 6.1 vs 6.7 us, T=8 7.9 vs 11.1 us per read); at T = 1 the CUDA-core kernels
 // are (5.2 vs 6.0 us): the MMA path stages four tokens there.  At d = 2560,
@@ -185,8 +262,12 @@ cudaError_t launch_pair_tc(const DownArgs& da, const UpArgs& ua, cudaStream_t st
 // 8-token groups).  At d = 4096 (two CTAs per SM either way) 8-token groups
 // stay faster from T = 5 (8.5 against 9.0 us).
 template <int D, int KD>
-cudaError_t launch_geometry(int T, const DownArgs& da, const UpArgs& ua, cudaStream_t st) {
+cudaError_t launch_geometry(int T, const DownArgs& da, const UpArgs& ua, cudaStream_t st,
+                            const CUtensorMap* w_down) {
   if (T == 1) return launch_pair<D, KD, 1>(da, ua, st);
+  if constexpr (D == 2560) {
+    if (w_down != nullptr) return launch_pair_u<D, KD>(da, ua, *w_down, st);
+  }
   constexpr int kOneGroupMaxT = D == 2560 ? 8 : 4;
   return T <= kOneGroupMaxT ? launch_pair_tc<D, KD, 1>(da, ua, st) : launch_pair_tc<D, KD, 2>(da, ua, st);
 }
@@ -464,6 +545,30 @@ HC_EXPORT int hc_read_create(hc_read_t* out, int n, int d, int K, int T_max, flo
 
 namespace {
 
+// Whether a BF16 read takes the tensor-memory down kernel: d = 2560 and
+// 5 <= T <= 8.
+bool takes_umma(int d, int T) { return d == 2560 && T > 4 && T <= hc::UGeo<2560, 320>::TMAX; }
+
+// The W_down tensor map of a read that takes the tensor-memory down kernel,
+// from the handle's cache; null: the read takes the mma.sync kernels (also
+// when the driver offers no tensor-map encoder).
+const CUtensorMap* down_map_for(hc_read_t h, const ReadDesc& q, int T) {
+  if (q.is_q8() || !takes_umma(h->d, T)) return nullptr;
+  MapCache* c = h->map_cache;
+  if (c == nullptr) {
+    c = h->map_cache = new (std::nothrow) MapCache();
+    if (c == nullptr) return nullptr;
+  }
+  for (int i = 0; i < MapCache::kSlots; ++i) {
+    if (c->down[i] == q.W_down) return &c->maps[i];
+  }
+  const int i = (int)(c->next++ % MapCache::kSlots);
+  c->down[i] = nullptr;
+  if (!encode_bf16_tiles(&c->maps[i], q.W_down, h->K, (uint64_t)h->n * h->d, 64)) return nullptr;
+  c->down[i] = q.W_down;
+  return &c->maps[i];
+}
+
 // Enqueues one validated read on `st` with partial-sum slot `part` (the two
 // kernels of the read; the caller alternates between its two slots).
 int enqueue_read(hc_read_t h, float* part, int device, const ReadDesc& q, int T, float* r_out, float* rs,
@@ -512,7 +617,8 @@ int enqueue_read(hc_read_t h, float* part, int device, const ReadDesc& q, int T,
   if (q.is_q8()) {
     e = (h->d == 2560) ? launch_geometry_q8<2560, 320>(T, da, ua, st) : launch_geometry_q8<4096, 512>(T, da, ua, st);
   } else {
-    e = (h->d == 2560) ? launch_geometry<2560, 320>(T, da, ua, st) : launch_geometry<4096, 512>(T, da, ua, st);
+    e = (h->d == 2560) ? launch_geometry<2560, 320>(T, da, ua, st, down_map_for(h, q, T))
+                       : launch_geometry<4096, 512>(T, da, ua, st, nullptr);
   }
   if (e != cudaSuccess) {
     cudaGetLastError();  // clear the sticky launch error for this thread
@@ -906,6 +1012,7 @@ HC_EXPORT void hc_read_destroy(hc_read_t h) {
     cudaFree(h->scratch);
     cudaSetDevice(prev);
   }
+  delete h->map_cache;
   delete h;
 }
 
@@ -1061,8 +1168,12 @@ HC_EXPORT int hc_read_noalloc(int n, int d, int K, float eps, const float* R, co
   ua.T_max = HC_NOALLOC_MAX_T;
   ua.independent = 0;
 
-  cudaError_t e = (d == 2560) ? launch_geometry<2560, 320>(T, da, ua, st)
-                              : launch_geometry<4096, 512>(T, da, ua, st);
+  // The same kernels as a handle's read; the W_down tensor map is encoded
+  // per call (a host structure, no allocation).
+  CUtensorMap w_down;
+  const bool mapped = takes_umma(d, T) && encode_bf16_tiles(&w_down, W_down, K, (uint64_t)n * d, 64);
+  cudaError_t e = (d == 2560) ? launch_geometry<2560, 320>(T, da, ua, st, mapped ? &w_down : nullptr)
+                              : launch_geometry<4096, 512>(T, da, ua, st, nullptr);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return HC_ERR_CUDA;
