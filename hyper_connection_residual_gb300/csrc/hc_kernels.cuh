@@ -157,6 +157,7 @@ struct DownArgs {
   int T_max;
   float eps;
   int independent;         // 1: no read in flight writes R or P (see below)
+  int late_launch;         // 1: the read runs among others on the batch lanes (see hc_down_kernel)
 };
 
 struct UpArgs {
@@ -290,14 +291,16 @@ __global__ void __launch_bounds__(kThreads, D == 2560 ? 3 : 2) hc_down_kernel(co
     ptx::bulk_g2s(w_s + lane * G::DN_PITCH, a.W_down + (size_t)(row0 + lane) * G::N + col0,
                   G::SLAB * 2, bar_w, once);
   }
-  // An independent read of one token group lets its up kernel launch only
-  // at the end of this kernel: the up CTAs then hold SM slots for less time
-  // and more reads of a batch overlap (measured on six streams: 2.58 ->
-  // 2.53-2.56 us per read at T = 1, 2.70 -> 2.64-2.67 at T = 4).  Chained
-  // reads keep the early launch: there the up kernel's weights must stream
-  // while this kernel waits (96 chained calls: 5.9 us per read, 7.3 with a
-  // late launch).  Reads of two token groups measured slower with it.
-  const bool late_launch = a.independent && a.T <= TT;
+  // An independent read of one token group that runs among others on the
+  // batch lanes lets its up kernel launch only at the end of this kernel:
+  // the up CTAs then hold SM slots for less time and more reads of the batch
+  // overlap (six streams: 2.58 -> 2.53-2.56 us per read at T = 1, 2.70 ->
+  // 2.64-2.67 at T = 4).  A read on its own keeps the early launch, which
+  // streams the up kernel's weights while this kernel runs (one read after
+  // another on one stream: 5.16 us per read at T = 1, 6.10 with a late
+  // launch; 96 chained calls: 5.9 against 7.3).  Reads of two token groups
+  // measured slower with it.
+  const bool late_launch = a.late_launch && a.independent && a.T <= TT;
   if (!late_launch) ptx::launch_dependents();
   __syncthreads();  // the mbarriers are initialised before any thread waits on them
   // w_norm is a parameter: wait for it before the previous kernel finishes.

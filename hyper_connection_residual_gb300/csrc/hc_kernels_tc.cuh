@@ -233,9 +233,9 @@ __global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_down_tc_k
   static_assert(G::DN_F4 <= kThreads, "one float4 per thread and token");
   const float4 wn = c4 < G::DN_F4 ? __ldg(reinterpret_cast<const float4*>(a.w_norm + col0) + c4)
                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-  // Late launch of the up kernel for independent reads of one token group,
-  // as in hc_down_kernel.
-  const bool late_launch = a.independent && a.T <= TG;
+  // Late launch of the up kernel for independent reads of one token group
+  // on the batch lanes, as in hc_down_kernel.
+  const bool late_launch = a.late_launch && a.independent && a.T <= TG;
   if (!late_launch) ptx::launch_dependents();
   __syncthreads();  // the mbarriers are initialised before any thread waits on them
   bool ok = true;

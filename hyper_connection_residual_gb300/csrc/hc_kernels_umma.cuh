@@ -149,9 +149,9 @@ __global__ void __launch_bounds__(UGeo<D, KD>::THREADS, 4) hc_down_u_kernel(cons
     ptx::tmem_alloc(tslot, U::TMEM_COLS);
     ptx::tmem_relinquish();
   }
-  // Independent reads let the up kernel launch only at the end (see
-  // hc_down_kernel); all T of this kernel are one pass.
-  const bool late_launch = a.independent != 0;
+  // Independent reads on the batch lanes let the up kernel launch only at
+  // the end (see hc_down_kernel); all T of this kernel are one pass.
+  const bool late_launch = a.late_launch && a.independent;
   if (!late_launch) ptx::launch_dependents();
   ptx::tc_fence_before();
   __syncthreads();  // tensor-memory address and mbarrier visible to all

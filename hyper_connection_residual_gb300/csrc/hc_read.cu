@@ -572,7 +572,7 @@ const CUtensorMap* down_map_for(hc_read_t h, const ReadDesc& q, int T) {
 // Enqueues one validated read on `st` with partial-sum slot `part` (the two
 // kernels of the read; the caller alternates between its two slots).
 int enqueue_read(hc_read_t h, float* part, int device, const ReadDesc& q, int T, float* r_out, float* rs,
-                 cudaStream_t st) {
+                 cudaStream_t st, bool on_lanes = false) {
   const size_t N = (size_t)h->n * h->d;
   Range ins[kReadInputs];
   input_ranges(q, N, h->K, T, ins);
@@ -594,6 +594,7 @@ int enqueue_read(hc_read_t h, float* part, int device, const ReadDesc& q, int T,
   da.T = T;
   da.T_max = h->T_max;
   da.independent = independent;
+  da.late_launch = on_lanes ? 1 : 0;
   da.eps = h->eps;
 
   UpArgs ua{};
@@ -769,7 +770,7 @@ int run_lanes(hc_read_t h, const ReadDesc* descs, int count, int T, const int* g
     hc_read_s::Lane& ln = h->lanes[group[j] % lanes];
     float* part = ln.part[ln.parity];
     ln.parity ^= 1;
-    status = enqueue_read(h, part, device, descs[j], T, nullptr, nullptr, ln.st);
+    status = enqueue_read(h, part, device, descs[j], T, nullptr, nullptr, ln.st, true);
   }
   // Every forked lane joins, also after a failure: a capture must not end
   // with work left on a lane.

@@ -110,9 +110,9 @@ def test_zero_weights_give_committed_residual(dev, rd1):
     assert float(o["lo"].abs().max()) == 0.0
 
 
-def test_repeat_and_graph_replay_bitwise(dev, g1, rd1):
+@pytest.mark.parametrize("T", [4, 8], ids=["T4_mma_sync", "T8_tensor_memory"])
+def test_repeat_and_graph_replay_bitwise(dev, g1, rd1, T):
     g, ws, w = g1
-    T = 4
     act = synth.activations(g, T, True, s0=11)
     a = dev_act(act, dev)
     o1 = outputs(g, T, dev)
@@ -216,12 +216,13 @@ def _oracle_from_gpu_inputs(orc, g, ws, R, P):
                     W_up=ws.W_up, gate=ws.gate, eps=EPS)
 
 
+@pytest.mark.parametrize("T", [4, 6])
 @pytest.mark.parametrize("use_graph", [False, True], ids=["direct", "graph"])
-def test_chained_reads(dev, orc, rd1, use_graph):
+def test_chained_reads(dev, orc, rd1, use_graph, T):
     """Read i's out is read i+1's R (the window's chaining): each read is
     checked against the oracle fed with that read's GPU input."""
     g = synth.G1
-    T, n_reads = 4, 5
+    n_reads = 5
     sets = [synth.weight_set(g, 20 + i) for i in range(n_reads)]
     w = [dev_weights(ws, dev) for ws in sets]
     act = synth.activations(g, T, True, s0=31)
