@@ -48,6 +48,7 @@ EPS = 1e-6
 SWEEP_T = (1, 2, 3, 4, 5, 6, 8)
 CALLS = 300
 SETS = 16
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e nominal, context beside the measured copy rate
 WINDOW_READS = 96
 WINDOW_T = 4
 
@@ -624,6 +625,7 @@ def run_gpu(args):
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"],
                 "traffic": traffic["dram_bytes_per_read_T1"] if traffic else None,
+                "peak_nominal": NOMINAL_HBM_GBS, "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
                 "unit_of_work": "one read (down + up kernel) at T=1, pending off: algorithmic bytes "
                                 "over the 300-read batch's time per read (reads overlap on the "
                                 "library's streams)",
