@@ -42,16 +42,18 @@ __device__ __forceinline__ void split4(const float4 x, uint2& hi, uint2& lo) {
   lo = make_uint2(*reinterpret_cast<const uint32_t*>(&l01), *reinterpret_cast<const uint32_t*>(&l23));
 }
 
-template <int D, int KD, int NT, bool Q8 = false>
+template <int D, int KD, int NT, int Q8 = 0>
 struct DownTcSmem {
   using G = Geo<D, KD>;
   static constexpr int TG = 4 * NT;
   static constexpr int NCOL = 8 * NT;
   static constexpr int XS_PITCH = G::SLAB * 2 + 16;   // bytes; = 16 (mod 128)
   // W_down rows: BF16, or Q8_0 int8 quants with their block scales apart
-  // (pitch an odd multiple of 32 bytes: the 64-bit loads of four rows x four
-  // lanes cover the 32 banks once).
-  static constexpr int WPITCH = Q8 ? G::SLAB + 32 : G::DN_PITCH;
+  // (mode 1: pitch an odd multiple of 32 bytes, so the 64-bit loads of four
+  // rows x four lanes cover the 32 banks once; mode 2: BF16 rows, the quants
+  // landing at byte Q8_OFF of each).
+  static constexpr int WPITCH = Q8 == 1 ? G::SLAB + 32 : G::DN_PITCH;
+  static constexpr int Q8_OFF = Q8 == 2 ? WPITCH - G::SLAB : 0;
   static constexpr int NB = G::SLAB / 32;              // Q8_0 blocks per row
   static constexpr int BAR = 0;
   static constexpr int W = 128;
@@ -72,16 +74,18 @@ struct DownTcSmem {
   static_assert(4 * TG * 32 * 4 <= NCOL * XS_PITCH && kMaxT <= 4 * TG * 32, "aliased regions fit");
   static_assert(!Q8 || (NB % 4 == 0 && (G::N / 32 * 2) % 8 == 0 && (NB * 2) % 8 == 0),
                 "a row's scales are whole 8-byte pieces at 8-byte aligned addresses");
-  static_assert(!Q8 || WPITCH % 64 == 32, "Q8_0 rows: 64-bit fragment loads conflict-free");
+  static_assert(Q8 != 1 || WPITCH % 64 == 32, "Q8_0 rows: 64-bit fragment loads conflict-free");
+  static_assert(Q8 != 2 || (Q8_OFF % 16 == 0 && Q8_OFF >= G::SLAB), "int8 rows on 16 bytes, past the BF16 half");
 };
 
-template <int D, int KD, int NT, bool Q8 = false>
+template <int D, int KD, int NT, int Q8 = 0>
 struct UpTcSmem {
   using G = Geo<D, KD>;
   static constexpr int TG = 4 * NT;
   static constexpr int NCOL = 8 * NT;
   static constexpr int LS_PITCH = KD * 2 + 16;        // bytes; = 16 (mod 128)
-  static constexpr int WPITCH = Q8 ? KD + 32 : G::UP_PITCH;  // W_up rows: BF16 or Q8_0 quants (as the down kernel's)
+  static constexpr int WPITCH = Q8 == 1 ? KD + 32 : G::UP_PITCH;  // W_up rows, as the down kernel's
+  static constexpr int Q8_OFF = Q8 == 2 ? WPITCH - KD : 0;
   static constexpr int NB = KD / 32;                  // Q8_0 blocks per row
   static constexpr int BAR = 0;
   static constexpr int W = 128;
@@ -97,7 +101,8 @@ struct UpTcSmem {
   static constexpr int SC = (RP + TG * G::UP_ROWS * 4 + 15) / 16 * 16;
   static constexpr int BYTES = SC + (Q8 ? G::UP_ROWS * NB * 2 : 0);
   static_assert(!Q8 || (G::UP_COLS * NB * 2) % 16 == 0, "a stream's scale run is whole 16-byte pieces");
-  static_assert(!Q8 || WPITCH % 64 == 32, "Q8_0 rows: 64-bit fragment loads conflict-free");
+  static_assert(Q8 != 1 || WPITCH % 64 == 32, "Q8_0 rows: 64-bit fragment loads conflict-free");
+  static_assert(Q8 != 2 || (Q8_OFF % 16 == 0 && Q8_OFF >= KD), "int8 rows on 16 bytes, past the BF16 half");
   static constexpr int bytes(int) { return BYTES; }
   static constexpr int BYTES_MAX = BYTES;
   static_assert(LS_PITCH % 128 == 16, "lo rows must be conflict-free for ldmatrix");
@@ -159,6 +164,49 @@ __device__ __forceinline__ void q8_stage4(unsigned char* row_hi, unsigned char* 
   *reinterpret_cast<uint32_t*>(row_lo + 2 * k13) = __byte_perm(lo.x, lo.y, 0x7632);
 }
 
+// Q8_0 modes of the tensor-core kernels: 1 decodes the quants in registers
+// inside the MMA loop (the layout above; fastest for one token group), 2
+// widens the tile to BF16 once in shared memory right after it lands and
+// runs the BF16 MMA loop with per-block scales (the second and later token
+// groups reuse the widened tile: 4.9 -> 4.4-4.7 us per read at T = 5..8 on
+// six streams, while one group measured 5 % slower than mode 1).  For mode 2
+// the int8 rows land at byte Q8_OFF of the BF16 rows of the same tile.  Each
+// row is widened in place: every lane loads its bytes of the row, the warp
+// synchronises, then the lanes write the BF16 values from the row's start;
+// rows do not overlap and inside a row all loads precede all stores.
+// Widens ROWS int8 rows of COLS bytes (at byte `q8_off` of each row, rows
+// `pitch` bytes apart) to BF16 at the start of the same rows.  Called by
+// every thread of the CTA after the tile has landed; LANES_PER_ROW lanes
+// take one row, each COLS / LANES_PER_ROW bytes (a multiple of 4).  A warp
+// loads all its rows first, synchronises once, then stores them all.
+template <int ROWS, int COLS, int LANES_PER_ROW>
+__device__ __forceinline__ void q8_widen_rows(unsigned char* tile, int pitch, int q8_off, int warp, int lane) {
+  constexpr int BPL = COLS / LANES_PER_ROW;  // bytes per lane
+  constexpr int WPL = BPL / 4;               // words per lane
+  constexpr int RPW = 32 / LANES_PER_ROW;    // rows per warp step
+  constexpr int STEPS = ROWS / (kWarps * RPW);
+  static_assert(COLS % LANES_PER_ROW == 0 && BPL % 4 == 0 && 32 % LANES_PER_ROW == 0, "whole words per lane");
+  static_assert(ROWS % (kWarps * RPW) == 0, "every warp takes the same number of rows");
+  const int sub = lane / LANES_PER_ROW, l = lane - sub * LANES_PER_ROW;
+  uint32_t v[STEPS][WPL];
+#pragma unroll
+  for (int st = 0; st < STEPS; ++st) {
+    const unsigned char* row = tile + (st * kWarps * RPW + warp * RPW + sub) * pitch;
+#pragma unroll
+    for (int i = 0; i < WPL; ++i) v[st][i] = *reinterpret_cast<const uint32_t*>(row + q8_off + BPL * l + 4 * i);
+  }
+  __syncwarp();
+#pragma unroll
+  for (int st = 0; st < STEPS; ++st) {
+    unsigned char* row = tile + (st * kWarps * RPW + warp * RPW + sub) * pitch;
+#pragma unroll
+    for (int i = 0; i < WPL; ++i) {
+      *reinterpret_cast<uint2*>(row + 2 * (BPL * l + 4 * i)) =
+          make_uint2(q8_bytes02(__byte_perm(v[st][i], 0, 0x4140)), q8_bytes02(__byte_perm(v[st][i], 0, 0x4342)));
+    }
+  }
+}
+
 // CTAs per SM the register budget is cut for: at d = 2560 four for one token
 // group (no spills at 64 registers; reads of a batch overlap better, measured
 // 3.06 -> 2.71 us per read at T = 2 and 3.15 -> 2.82 at T = 4 on six
@@ -171,7 +219,7 @@ constexpr int tc_min_blocks() {
 
 // ------------------------------------------------------------------ kernel 1
 // Grid (16 slabs, K/32 row groups), clusters of 4 along x (one stream).
-template <int D, int KD, int NT, bool Q8 = false>
+template <int D, int KD, int NT, int Q8 = 0>
 __global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_down_tc_kernel(const DownArgs a) {
   using G = Geo<D, KD>;
   using S = DownTcSmem<D, KD, NT, Q8>;
@@ -215,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_down_tc_k
     const uint64_t once = ptx::policy_evict_first();
     const void* src = Q8 ? static_cast<const void*>(a.Wq + (size_t)(row0 + lane) * G::N + col0)
                          : static_cast<const void*>(a.W_down + (size_t)(row0 + lane) * G::N + col0);
-    ptx::bulk_g2s(w_s + lane * S::WPITCH, src, WROW, bar_w, once);
+    ptx::bulk_g2s(w_s + lane * S::WPITCH + S::Q8_OFF, src, WROW, bar_w, once);
   }
   if constexpr (Q8) {
     // The slab's block scales of the CTA's 32 rows (binary16), copied
@@ -288,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_down_tc_k
         r.w = __fadd_rn(r.w, pv[t].w);
         const float4 x = make_float4(__fmul_rn(r.x, wn.x), __fmul_rn(r.y, wn.y), __fmul_rn(r.z, wn.z),
                                      __fmul_rn(r.w, wn.w));
-        if constexpr (Q8) {
+        if constexpr (Q8 == 1) {
           q8_stage4(xs + (2 * t) * S::XS_PITCH, xs + (2 * t + 1) * S::XS_PITCH, (4 * c4) & ~31, (4 * c4) & 31, x);
         } else {
           uint2 hi, lo;
@@ -312,9 +360,10 @@ __global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_down_tc_k
     }
     if (t0 == 0) {
       ok = wait_bar(bar_w, 0, a.err, kErrDownWeights) && ok;
-      if constexpr (Q8) ptx::cp_async_wait_all();
+      if constexpr (Q8 != 0) ptx::cp_async_wait_all();
+      if constexpr (Q8 == 2) q8_widen_rows<G::DN_ROWS, G::SLAB, 32>(w_s, S::WPITCH, S::Q8_OFF, warp, lane);
     }
-    __syncthreads();  // x (hi, lo) and the per-warp sums of squares are complete
+    __syncthreads();  // x (hi, lo), the per-warp sums of squares (and a widened tile) are complete
     if (tid < tg) {
       float v = 0.f;
 #pragma unroll
@@ -390,8 +439,13 @@ __global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_down_tc_k
 #pragma unroll 2  // fully unrolled, the 64-register variants spill
       for (int bk = 0; bk < KS / 2; ++bk) {
         uint32_t a0[4], a1[4];
-        q8_afrags(*reinterpret_cast<const uint2*>(qa + 32 * bk),
-                  *reinterpret_cast<const uint2*>(qa + 8 * S::WPITCH + 32 * bk), a0, a1);
+        if constexpr (Q8 == 1) {
+          q8_afrags(*reinterpret_cast<const uint2*>(qa + 32 * bk),
+                    *reinterpret_cast<const uint2*>(qa + 8 * S::WPITCH + 32 * bk), a0, a1);
+        } else {
+          ptx::ldsm_x4(a_base + (2 * bk) * 32, a0[0], a0[1], a0[2], a0[3]);
+          ptx::ldsm_x4(a_base + (2 * bk + 1) * 32, a1[0], a1[1], a1[2], a1[3]);
+        }
         float blk[NT][4];
         kstep_q8(2 * bk, a0, a1, blk);
         const float s0 = __half2float(sc[bk]), s1 = __half2float(sc[8 * S::NB + bk]);  // rows g and g + 8
@@ -453,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_down_tc_k
 }
 
 // ------------------------------------------------------------------ kernel 2
-template <int D, int KD, int NT, bool Q8 = false>
+template <int D, int KD, int NT, int Q8 = 0>
 __global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_up_tc_kernel(const UpArgs a) {
   using G = Geo<D, KD>;
   using S = UpTcSmem<D, KD, NT, Q8>;
@@ -497,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_up_tc_ker
     for (int r = lane; r < G::UP_ROWS; r += 32) {
       const int grow = (r / G::UP_COLS) * D + c0 + (r % G::UP_COLS);
       if constexpr (Q8) {
-        ptx::bulk_g2s(w_s + r * S::WPITCH, a.Wq + (size_t)grow * KD, KD, bar_w, once);
+        ptx::bulk_g2s(w_s + r * S::WPITCH + S::Q8_OFF, a.Wq + (size_t)grow * KD, KD, bar_w, once);
       } else {
         ptx::bulk_g2s(w_s + r * S::WPITCH, a.W_up + (size_t)grow * KD, KD * 2, bar_w, once);
       }
@@ -581,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_up_tc_ker
         l.z = ((pv[m][0].z + pv[m][1].z) + pv[m][2].z) + pv[m][3].z;
         l.w = ((pv[m][0].w + pv[m][1].w) + pv[m][2].w) + pv[m][3].w;
         const int t = idx / (KD / 4), k4 = idx % (KD / 4);
-        if constexpr (Q8) {
+        if constexpr (Q8 == 1) {
           q8_stage4(ls + (2 * t) * S::LS_PITCH, ls + (2 * t + 1) * S::LS_PITCH, (4 * k4) & ~31, (4 * k4) & 31, l);
         } else {
           uint2 hi, lo;
@@ -606,9 +660,10 @@ __global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_up_tc_ker
     if (kEarly && t0 + TG < T) load_group(t0 + TG);
     if (t0 == 0) {
       ok = wait_bar(bar_w, 0, a.err, kErrUpWeights) && ok;
-      if constexpr (Q8) ptx::cp_async_wait_all();
+      if constexpr (Q8 != 0) ptx::cp_async_wait_all();
+      if constexpr (Q8 == 2) q8_widen_rows<G::UP_ROWS, KD, 16>(w_s, S::WPITCH, S::Q8_OFF, warp, lane);
     }
-    __syncthreads();  // lo (hi, lo), R' and the gates are in shared memory
+    __syncthreads();  // lo (hi, lo), R', the gates (and a widened tile) are in shared memory
 
     // One k-step of 16 along K: B rows from the lo staging, MMA into cc.
     auto kstep = [&](int ks, const uint32_t(&af)[4], float(&cc)[NT][4]) {
@@ -678,8 +733,13 @@ __global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_up_tc_ker
 #pragma unroll 2  // fully unrolled, the 64-register variants spill
       for (int bk = 0; bk < KS / 2; ++bk) {
         uint32_t a0[4], a1[4];
-        q8_afrags(*reinterpret_cast<const uint2*>(qa + 32 * bk),
-                  *reinterpret_cast<const uint2*>(qa + 8 * S::WPITCH + 32 * bk), a0, a1);
+        if constexpr (Q8 == 1) {
+          q8_afrags(*reinterpret_cast<const uint2*>(qa + 32 * bk),
+                    *reinterpret_cast<const uint2*>(qa + 8 * S::WPITCH + 32 * bk), a0, a1);
+        } else {
+          ptx::ldsm_x4(a_base + (2 * bk) * 32, a0[0], a0[1], a0[2], a0[3]);
+          ptx::ldsm_x4(a_base + (2 * bk + 1) * 32, a1[0], a1[1], a1[2], a1[3]);
+        }
         float blk[NT][4];
         kstep_q8(2 * bk, a0, a1, blk);
         const float s0 = __half2float(sc[bk]), s1 = __half2float(sc[8 * S::NB + bk]);  // rows g and g + 8

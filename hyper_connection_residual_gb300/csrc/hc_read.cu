@@ -140,7 +140,7 @@ cudaError_t configure_one() {
                               hc::UpSmem<D, KD, TT>::BYTES_MAX);
 }
 
-template <int D, int KD, int NT, bool Q8>
+template <int D, int KD, int NT, int Q8>
 cudaError_t configure_tc() {
   cudaError_t e = cudaFuncSetAttribute(hc::hc_down_tc_kernel<D, KD, NT, Q8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -164,10 +164,11 @@ cudaError_t configure_geometry() {
     if ((e = configure_umma<D, KD>()) != cudaSuccess) return e;
   }
   if ((e = configure_one<D, KD, 1>()) != cudaSuccess) return e;
-  if ((e = configure_tc<D, KD, 1, false>()) != cudaSuccess) return e;
-  if ((e = configure_tc<D, KD, 2, false>()) != cudaSuccess) return e;
-  if ((e = configure_tc<D, KD, 1, true>()) != cudaSuccess) return e;
-  return configure_tc<D, KD, 2, true>();
+  if ((e = configure_tc<D, KD, 1, 0>()) != cudaSuccess) return e;
+  if ((e = configure_tc<D, KD, 2, 0>()) != cudaSuccess) return e;
+  if ((e = configure_tc<D, KD, 1, 1>()) != cudaSuccess) return e;
+  if ((e = configure_tc<D, KD, 1, 2>()) != cudaSuccess) return e;
+  return configure_tc<D, KD, 2, 2>();
 }
 
 template <int D, int KD, int TT>
@@ -185,7 +186,7 @@ cudaError_t launch_pair(const DownArgs& da, const UpArgs& ua, cudaStream_t st) {
   return cudaLaunchKernelEx(&c2, hc::hc_up_kernel<D, KD, TT>, ua);
 }
 
-template <int D, int KD, int NT, bool Q8 = false>
+template <int D, int KD, int NT, int Q8 = 0>
 cudaError_t launch_pair_tc(const DownArgs& da, const UpArgs& ua, cudaStream_t st) {
   using G = hc::Geo<D, KD>;
   cudaLaunchAttribute attr[2];
@@ -277,8 +278,10 @@ cudaError_t launch_geometry(int T, const DownArgs& da, const UpArgs& ua, cudaStr
 template <int D, int KD>
 cudaError_t launch_geometry_q8(int T, const DownArgs& da, const UpArgs& ua, cudaStream_t st) {
   constexpr int kOneGroupMaxT = D == 2560 ? 8 : 4;
-  return T <= kOneGroupMaxT ? launch_pair_tc<D, KD, 1, true>(da, ua, st)
-                            : launch_pair_tc<D, KD, 2, true>(da, ua, st);
+  // One token group: quants decoded in registers (mode 1); several groups:
+  // the tile widened once in shared memory (mode 2), reused by every group.
+  if (T <= 4) return launch_pair_tc<D, KD, 1, 1>(da, ua, st);
+  return T <= kOneGroupMaxT ? launch_pair_tc<D, KD, 1, 2>(da, ua, st) : launch_pair_tc<D, KD, 2, 2>(da, ua, st);
 }
 
 // Q8_0 weights of a read (quants and block scales of both projections).
