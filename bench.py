@@ -100,14 +100,19 @@ def whole_job_gbs(world: int, bytes_per_step: int, steps: int, seconds: float) -
     return world * bytes_per_step * steps / seconds / 1e9
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(names=None) -> str:
+    """Hash of the CUDA sources (all of them, or the files in `names`)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "hyper_connection_residual_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in sorted(names if names is not None else os.listdir(csrc)):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+# The device code of the T=1 read kernels, whose DRAM counters profiles/traffic.json records.
+T1_KERNEL_SOURCES = ("hc_kernels.cuh", "hc_ptx.cuh")
 
 
 def measured_peaks() -> dict:
@@ -126,7 +131,7 @@ def profiled_traffic() -> dict | None:
         return None
     with open(path) as f:
         d = json.load(f)
-    if d.get("kernel_hash") != kernel_source_hash():
+    if d.get("kernel_hash") != kernel_source_hash(T1_KERNEL_SOURCES):
         return None
     return d
 
