@@ -1,4 +1,5 @@
-"""FP64 CPU oracle of the hyper-connection read (test infrastructure only).
+"""FP64 CPU oracle of the hyper-connection read and of the Q2_0 matrix-vector
+product (test infrastructure only).
 
 Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's CPU
 baseline / reference arm may import this package.  The CUDA library never
@@ -40,6 +41,7 @@ _f32p = np.ctypeslib.ndpointer(dtype=np.float32, flags="C_CONTIGUOUS")
 _f64p = np.ctypeslib.ndpointer(dtype=np.float64, flags="C_CONTIGUOUS")
 _u16p = np.ctypeslib.ndpointer(dtype=np.uint16, flags="C_CONTIGUOUS")
 _i8p = np.ctypeslib.ndpointer(dtype=np.int8, flags="C_CONTIGUOUS")
+_u8p = np.ctypeslib.ndpointer(dtype=np.uint8, flags="C_CONTIGUOUS")
 
 
 @dataclass
@@ -73,6 +75,10 @@ class Oracle:
             _f32p, ctypes.c_void_p, _f32p, _i8p, _u16p, _i8p, _u16p, _f32p,
             _f32p, _f64p, _f64p, _f64p, _f64p, _f64p, _f64p,
         ]
+        lib.hc_oracle_q2_0_matvec.restype = ctypes.c_int
+        lib.hc_oracle_q2_0_matvec.argtypes = [
+            ctypes.c_int, ctypes.c_int, ctypes.c_int, _u8p, _u16p, _f32p, _f64p,
+        ]
         lib.hc_oracle_half.restype = ctypes.c_double
         lib.hc_oracle_half.argtypes = [ctypes.c_uint16]
         self._lib = lib
@@ -80,6 +86,21 @@ class Oracle:
     def half(self, h: int) -> float:
         """The value of the IEEE binary16 bit pattern h."""
         return float(self._lib.hc_oracle_half(h))
+
+    def q2_0_matvec(self, Wq, Wscale, x) -> np.ndarray:
+        """y [ncols][rows] float64 = W x for Q2_0 weights: Wq [rows][cols/4]
+        uint8 (four two-bit codes a byte), Wscale [rows][cols/64] binary16 bits
+        (uint16), x [ncols][cols] float32."""
+        Wq = np.ascontiguousarray(Wq, dtype=np.uint8)
+        rows = Wq.shape[0]
+        cols = Wq.shape[1] * 4
+        Wscale = np.ascontiguousarray(Wscale, dtype=np.uint16).reshape(rows, cols // 64)
+        x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1, cols)
+        y = np.empty((x.shape[0], rows))
+        rc = self._lib.hc_oracle_q2_0_matvec(rows, cols, x.shape[0], Wq, Wscale, x, y)
+        if rc != 0:
+            raise ValueError(f"hc_oracle_q2_0_matvec rejected its arguments (rc={rc})")
+        return y
 
     def read_q8(self, n: int, d: int, K: int, R, w_norm, Wd_q, Wd_scale, Wu_q, Wu_scale, gate,
                 P=None, eps: float = 1e-6) -> OracleResult:

@@ -39,6 +39,20 @@
 // IEEE binary16 scale and 32 int8 values, weight = scale * q.  Quants and
 // scales are two arrays: q [rows][cols] int8, scale [rows][cols / 32] binary16.
 //
+// The Q2_0 matrix-vector product (hc_oracle_q2_0_matvec) is the decode
+// windows' other bandwidth-bound step [P3: Strata pull request #2221, first
+// paragraph and the table "Kernel (2560 x 12288, cold weights ...)": the QSA
+// layers' attn_q projection from 2560 inputs to 12288 outputs over Q2_0
+// weights, for one to four columns].  The pages name the format and its
+// 64-value blocks but not its bits; this library reads Q2_0 as: every row in
+// blocks of 64 consecutive values, each block one IEEE binary16 scale d and
+// 64 two-bit codes q in {0, 1, 2, 3}, weight = d * (q - 2); the codes of a
+// row packed four to a byte, value j at byte j / 4, bits 2 * (j % 4) and
+// 2 * (j % 4) + 1 (least significant first); codes and scales in separate
+// arrays, Wq [rows][cols / 4] bytes and Wscale [rows][cols / 64] binary16.
+// (The pages' 80 us at about 110 GB/s for 2560 x 12288 is about 8.8 MB per
+// call: two bits per value and 16 bits per 64-value block give 8,847,360 B.)
+//
 // Parity status: every function below is pinned by the CPU tests (hand-expanded
 // tiny cases under tests/golden/, closed forms, invariants, brute force).
 
@@ -79,6 +93,13 @@ double half_to_double(uint16_t h) {
 double q8_weight(const int8_t* q, const uint16_t* scale, int cols, int r, int j) {
   return half_to_double(scale[(size_t)r * (cols / 32) + j / 32]) *
          static_cast<double>(q[(size_t)r * cols + j]);
+}
+
+// One Q2_0 weight: row r, column j of a matrix with `cols` columns.
+double q2_weight(const uint8_t* codes, const uint16_t* scale, int cols, int r, int j) {
+  const uint8_t byte = codes[(size_t)r * (cols / 4) + j / 4];
+  const int q = (byte >> (2 * (j % 4))) & 3;
+  return half_to_double(scale[(size_t)r * (cols / 64) + j / 64]) * static_cast<double>(q - 2);
 }
 
 }  // namespace
@@ -239,6 +260,26 @@ int hc_oracle_read_q8(int n, int d, int K, int T, double eps, const float* R,
   hc_oracle_down_q8(n, d, K, T, r_out, w_norm, Wd_q, Wd_scale, rs, lo);
   hc_oracle_up_q8(N, K, T, Wu_q, Wu_scale, lo, u);
   hc_oracle_epilogue(n, d, T, r_out, gate, u, out, mean);
+  return 0;
+}
+
+// The Q2_0 matrix-vector product [P3, first paragraph and the kernel table]:
+// y[c][r] = sum_j W[r][j] * x[c][j] for columns c < ncols, with W[r][j] the
+// Q2_0 value of row r, column j.  x [ncols][cols] float, y [ncols][rows]
+// double.  cols must be a multiple of 64.  Returns 0, or -1 on a bad argument.
+int hc_oracle_q2_0_matvec(int rows, int cols, int ncols, const uint8_t* Wq,
+                          const uint16_t* Wscale, const float* x, double* y) {
+  if (rows <= 0 || cols <= 0 || cols % 64 != 0 || ncols <= 0) return -1;
+  if (!Wq || !Wscale || !x || !y) return -1;
+  for (int c = 0; c < ncols; ++c) {
+    for (int r = 0; r < rows; ++r) {
+      double acc = 0.0;
+      for (int j = 0; j < cols; ++j) {
+        acc += q2_weight(Wq, Wscale, cols, r, j) * static_cast<double>(x[(size_t)c * cols + j]);
+      }
+      y[(size_t)c * rows + r] = acc;
+    }
+  }
   return 0;
 }
 

@@ -19,6 +19,11 @@ W_up         [n*d][K] BF16 (uint16)      N(0, w_std)            5
 Activations (R, P) use seed ``s0``; weight set ``j`` (W_down, W_up, w_norm,
 gate) uses seed ``s0 + 1 + j``.  ``w_std`` is 0.02 at d=2560, K=320 and 0.015
 at d=4096, K=512.
+
+Q2_0 matrix-vector product (rows x cols weights, ncols input columns): the
+weights are N(0, 0.02) float32 draws (seed ``s0 + 1 + j`` for copy j, tensor
+id 6) quantized to Q2_0 by ``quantize_q2``; the input columns are N(0, 1)
+(seed ``s0 + j``, tensor id 7).
 """
 
 from __future__ import annotations
@@ -35,7 +40,7 @@ SRC = os.path.join(HERE, "hc_synth.c")
 LIB = os.path.join(HERE, "libhcsynth.so")
 CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math", "-pthread"]
 
-TID_R, TID_P, TID_WNORM, TID_GATE, TID_WDOWN, TID_WUP = range(6)
+TID_R, TID_P, TID_WNORM, TID_GATE, TID_WDOWN, TID_WUP, TID_Q2_W, TID_Q2_X = range(8)
 
 
 def compile_cmd(out: str = LIB) -> list[str]:
@@ -179,6 +184,50 @@ def q8_weight_set(g: Geometry, j: int = 0, s0: int = 0) -> Q8WeightSet:
         w_norm=normal_f32(seed, TID_WNORM, 1.0, 0.05, (g.N,)),
         gate=normal_f32(seed, TID_GATE, 0.0, 1.0, (g.N,)),
         Wd_q=wd_q, Wd_scale=wd_s, Wu_q=wu_q, Wu_scale=wu_s)
+
+
+@dataclass
+class Q2Matrix:
+    """A Q2_0 matrix: per row, blocks of 64 consecutive values, one IEEE
+    binary16 scale d and 64 two-bit codes q per block (weight = d * (q - 2)),
+    the codes packed four to a byte, least significant bits first."""
+    Wq: np.ndarray       # [rows][cols/4] uint8
+    Wscale: np.ndarray   # [rows][cols/64] uint16 (binary16 bits)
+
+
+def pack_q2(codes: np.ndarray) -> np.ndarray:
+    """Pack [rows][cols] codes in 0..3 four to a byte: value j of a row at
+    bits 2*(j % 4) of byte j // 4."""
+    c = np.asarray(codes, np.uint8)
+    rows, cols = c.shape
+    c = c.reshape(rows, cols // 4, 4)
+    return (c[..., 0] | (c[..., 1] << 2) | (c[..., 2] << 4) | (c[..., 3] << 6)).astype(np.uint8)
+
+
+def quantize_q2(w: np.ndarray) -> Q2Matrix:
+    """Q2_0 blocks of a [rows][cols] float32 matrix (cols a multiple of 64):
+    scale = binary16(max |w| / 2) per block, q - 2 = round-to-nearest-even of
+    w / scale clamped to [-2, 1] (q = 2 where the scale is 0)."""
+    rows, cols = w.shape
+    blocks = np.asarray(w, np.float32).reshape(rows, cols // 64, 64)
+    scale = (np.abs(blocks).max(axis=2) / np.float32(2)).astype(np.float16)
+    s = scale.astype(np.float32)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.where(s > 0, np.rint(blocks / np.where(s > 0, s, 1)), 0)
+    codes = (np.clip(q, -2, 1) + 2).astype(np.uint8).reshape(rows, cols)
+    return Q2Matrix(Wq=pack_q2(codes), Wscale=scale.view(np.uint16))
+
+
+def q2_0_matrix(rows: int, cols: int, j: int = 0, s0: int = 0, w_std: float = 0.02) -> Q2Matrix:
+    """Q2_0 copy j of a [rows][cols] projection drawn as N(0, w_std) in
+    float32 (seed s0 + 1 + j, tensor id TID_Q2_W)."""
+    return quantize_q2(normal_f32(s0 + 1 + j, TID_Q2_W, 0.0, w_std, (rows, cols)))
+
+
+def q2_0_columns(cols: int, ncols: int, j: int = 0, s0: int = 0) -> np.ndarray:
+    """[ncols][cols] float32 input columns, N(0, 1) (seed s0 + j, tensor id
+    TID_Q2_X)."""
+    return normal_f32(s0 + j, TID_Q2_X, 0.0, 1.0, (ncols, cols))
 
 
 def activations(g: Geometry, T: int, pending: bool, s0: int = 0) -> Activations:

@@ -341,6 +341,80 @@ def pin_q8_one_block(orc):
     assert not np.any(res.lo), "zero scales: lo = 0"
 
 
+
+# ---------------------------------------------------------------- Q2_0 matvec
+
+def _half_bits(values):
+    return np.asarray(values, np.float16).view(np.uint16)
+
+
+def pin_q2_hand_packing(orc):
+    """Hand-built bytes: one row of two 64-value blocks (scales 1/2 and -1/4).
+    Byte 0 = 0b11100100 holds codes 0, 1, 2, 3 for values 0..3 (least
+    significant bits first), byte 17 = 0b00011011 codes 3, 2, 1, 0 for values
+    68..71, every other byte 0b10101010 (code 2: weight 0).  Weight =
+    scale * (code - 2), so probing with unit columns gives exactly
+    -1, -1/2, 0, 1/2 at values 0..3 and -1/4, 0, 1/4, 1/2 at values 68..71."""
+    Wq = np.full((1, 32), 0xAA, np.uint8)
+    Wq[0, 0] = 0xE4
+    Wq[0, 17] = 0x1B
+    Wscale = _half_bits([[0.5, -0.25]])
+    y = orc.q2_0_matvec(Wq, Wscale, np.eye(128, dtype=np.float32))
+    want = np.zeros(128)
+    want[0:4] = [-1.0, -0.5, 0.0, 0.5]
+    want[68:72] = [-0.25, 0.0, 0.25, 0.5]
+    assert np.array_equal(y[:, 0], want), f"hand packing: {y[:8, 0]} ... {y[64:72, 0]}"
+
+
+def pin_q2_block_sums(orc):
+    """All codes 3 (weight = +scale) and all codes 0 (weight = -2 scale): y is
+    the scale-weighted sum of each block's inputs, here summed exactly
+    (math.fsum) from the inputs; scales differ by row and block."""
+    rows, cols, ncols = 3, 192, 2
+    rng = _rng(21)
+    x = rng.standard_normal((ncols, cols)).astype(np.float32)
+    scale = np.ldexp(1.0, -(1 + (np.arange(rows)[:, None] * 5 + np.arange(3)[None, :] * 2) % 7))
+    for byte, factor in ((0xFF, 1.0), (0x00, -2.0)):
+        y = orc.q2_0_matvec(np.full((rows, cols // 4), byte, np.uint8), _half_bits(scale), x)
+        for c in range(ncols):
+            for r in range(rows):
+                want = math.fsum(factor * scale[r, b] * float(v)
+                                 for b in range(3) for v in x[c, 64 * b:64 * (b + 1)])
+                assert abs(y[c, r] - want) <= 1e-14 * max(1.0, abs(want)), f"block sums ({c}, {r})"
+
+
+def pin_q2_probes(orc):
+    """Brute force: codes drawn as an array of 0..3, packed by the input
+    generator, scales random powers of two; probing with every unit column
+    gives back each weight scale * (code - 2) exactly."""
+    import synth
+    rows, cols = 5, 128
+    rng = _rng(22)
+    codes = rng.integers(0, 4, size=(rows, cols))
+    scale = np.ldexp(1.0, rng.integers(-12, 4, size=(rows, cols // 64))) * \
+        rng.choice([-1.0, 1.0], size=(rows, cols // 64))
+    y = orc.q2_0_matvec(synth.pack_q2(codes), _half_bits(scale), np.eye(cols, dtype=np.float32))
+    want = (codes - 2) * np.repeat(scale, 64, axis=1)
+    assert np.array_equal(y, want.T), "probed weights"
+
+
+def pin_q2_invariants(orc):
+    """Linear in x (a power-of-two factor scales y exactly), negating the scales
+    negates y, zero scales and zero inputs give y = 0."""
+    import synth
+    rows, cols, ncols = 7, 256, 3
+    m = synth.quantize_q2((_rng(23).standard_normal((rows, cols)) * 0.02).astype(np.float32))
+    x = _rng(24).standard_normal((ncols, cols)).astype(np.float32)
+    y = orc.q2_0_matvec(m.Wq, m.Wscale, x)
+    assert np.array_equal(orc.q2_0_matvec(m.Wq, m.Wscale, x * np.float32(4.0)), 4.0 * y), "4 x"
+    neg = (m.Wscale ^ np.uint16(0x8000)).astype(np.uint16)
+    assert np.array_equal(orc.q2_0_matvec(m.Wq, neg, x), -y), "negated scales"
+    assert not np.any(orc.q2_0_matvec(m.Wq, np.zeros_like(m.Wscale), x)), "zero scales"
+    assert not np.any(orc.q2_0_matvec(m.Wq, m.Wscale, np.zeros_like(x))), "zero inputs"
+    for c in range(ncols):
+        assert np.array_equal(orc.q2_0_matvec(m.Wq, m.Wscale, x[c:c + 1])[0], y[c]), "columns independent"
+
+
 ALL_PINS = [
     pin_hand_fixtures,
     pin_constant_streams,
@@ -357,6 +431,10 @@ ALL_PINS = [
     pin_half_decoding,
     pin_q8_equals_bf16_read,
     pin_q8_one_block,
+    pin_q2_hand_packing,
+    pin_q2_block_sums,
+    pin_q2_probes,
+    pin_q2_invariants,
 ]
 
 

@@ -39,6 +39,15 @@ MUTANTS = [
     ("half subnormal scale", "fraction), -24)", "fraction), -25)"),
     ("half implicit bit", "1024 + fraction", "fraction"),
     ("half sign", "return sign ? -v : v;", "return v;"),
+    ("q2 offset", "static_cast<double>(q - 2)", "static_cast<double>(q - 1)"),
+    ("q2 bit order", "(byte >> (2 * (j % 4))) & 3", "(byte >> (6 - 2 * (j % 4))) & 3"),
+    ("q2 two-bit mask", "(2 * (j % 4))) & 3;", "(2 * (j % 4))) & 1;"),
+    ("q2 block size", "+ j / 64]", "+ j / 32]"),
+    ("q2 scale row stride", "scale[(size_t)r * (cols / 64)", "scale[(size_t)r * (cols / 32)"),
+    ("q2 code row stride", "codes[(size_t)r * (cols / 4)", "codes[(size_t)r * (cols / 2)"),
+    ("q2 input stride", "x[(size_t)c * cols + j]", "x[(size_t)j * ncols + c]"),
+    ("q2 output stride", "y[(size_t)c * rows + r]", "y[(size_t)r * ncols + c]"),
+    ("q2 scale dropped", "return half_to_double(scale[(size_t)r * (cols / 64) + j / 64]) *", "return"),
     ("q8 down on bf16 path", "hc_oracle_down_q8(n, d, K, T, r_out, w_norm, Wd_q, Wd_scale, rs, lo);", "hc_oracle_down_q8(n, d, K, T, r_out, w_norm, Wd_q, Wu_scale, rs, lo);"),
 ]
 

@@ -40,3 +40,20 @@ def test_numpy_cross_check(orc):
     for name, want in (("lo", lo), ("u", u), ("out", out), ("mean", mean), ("rs", rs)):
         got = getattr(res, name)
         assert np.max(np.abs(got - want)) <= 1e-12 * np.max(np.abs(want)), name
+
+
+def test_q2_numpy_cross_check(orc):
+    """Supplementary: the Q2_0 product through a dense NumPy float64 matrix
+    (codes unpacked with np.unpackbits) agrees with the oracle.  (Not a pin:
+    it restates the definition.)"""
+    import synth
+    rows, cols, ncols = 1024, 2560, 4
+    m = synth.q2_0_matrix(rows, cols, j=3)
+    x = synth.q2_0_columns(cols, ncols, j=3)
+    bits = np.unpackbits(m.Wq[..., None], axis=-1, bitorder="little").reshape(rows, cols, 2)
+    codes = bits[..., 0].astype(np.int64) + 2 * bits[..., 1]
+    scale = m.Wscale.view(np.float16).astype(np.float64)
+    W = (codes - 2) * np.repeat(scale, 64, axis=1)
+    want = x.astype(np.float64) @ W.T
+    got = orc.q2_0_matvec(m.Wq, m.Wscale, x)
+    assert np.max(np.abs(got - want)) <= 1e-12 * np.max(np.abs(want))

@@ -79,3 +79,23 @@ def test_q8_quantizer():
     ws = synth.q8_weight_set(synth.Geometry(n=4, d=64, K=64, w_std=0.02), 0)
     assert ws.Wd_q.shape == (64, 256) and ws.Wd_scale.shape == (64, 8)
     assert ws.Wu_q.shape == (256, 64) and ws.Wu_scale.shape == (256, 2)
+
+
+def test_q2_quantization_recipe():
+    """quantize_q2: scale = binary16(max|w| / 2) per 64-value block, codes in
+    0..3 packed four to a byte, and dequantization within half a step."""
+    w = synth.normal_f32(5, synth.TID_Q2_W, 0.0, 0.02, (8, 256))
+    m = synth.quantize_q2(w)
+    assert m.Wq.shape == (8, 64) and m.Wq.dtype == np.uint8
+    assert m.Wscale.shape == (8, 4) and m.Wscale.dtype == np.uint16
+    scale = m.Wscale.view(np.float16).astype(np.float32)
+    want = (np.abs(w.reshape(8, 4, 64)).max(-1) / np.float32(2)).astype(np.float16).astype(np.float32)
+    assert np.array_equal(scale, want)
+    codes = np.stack([(m.Wq >> (2 * i)) & 3 for i in range(4)], -1).reshape(8, 256)
+    deq = (codes.astype(np.float32) - 2) * np.repeat(scale, 64, axis=1)
+    # inside the clamp range the error is at most half a step (plus the
+    # binary16 rounding of the scale); values above 1 step clamp to it
+    inside = w <= np.repeat(scale, 64, axis=1) * 1.5
+    err = np.abs(deq - w)[inside]
+    assert np.all(err <= 0.5 * np.repeat(scale, 64, axis=1)[inside] * 1.01)
+    assert np.array_equal(synth.pack_q2(codes), m.Wq)
