@@ -1,8 +1,9 @@
 """GB300 (sm_103a) hyper-connection read.
 
-The read runs only in the CUDA library ``libhcread.so`` (two hand-written
-kernels behind the C ABI of ``include/hc_read.h``).  This package is a thin
-ctypes binding with the same entry-point names; it has no CPU path.
+The read runs only in the CUDA library ``libhcread.so`` (hand-written kernels
+behind the C ABI of ``include/hc_read.h``), and so does the Q2_0
+matrix-vector product of ``include/hc_q2.h``.  This package is a thin ctypes
+binding with the same entry-point names; it has no CPU path.
 """
 
 from ._binding import (  # noqa: F401
@@ -21,6 +22,9 @@ from ._binding import (  # noqa: F401
     hc_graph_destroy,
     hc_graph_end,
     hc_graph_launch,
+    hc_q2_0_desc,
+    hc_q2_0_matvec,
+    hc_q2_0_matvec_batch,
     hc_read,
     hc_read_batch,
     hc_read_batch_groups,

@@ -17,7 +17,7 @@ HC_OK, HC_ERR_ARG, HC_ERR_ALIGN, HC_ERR_SHAPE, HC_ERR_CUDA, HC_ERR_TIMEOUT = 0, 
 HC_ERR_TOO_LARGE = -6
 HC_NOALLOC_MAX_T = 8
 
-# Every symbol the C header declares.
+# Every symbol the C headers (include/hc_read.h, include/hc_q2.h) declare.
 EXPORTS = (
     "hc_read_create", "hc_read", "hc_read_ex", "hc_read_check", "hc_read_reset",
     "hc_read_destroy", "hc_read_scratch_bytes", "hc_status_str",
@@ -25,6 +25,7 @@ EXPORTS = (
     "hc_read_noalloc", "hc_read_batch", "hc_read_batch_persistent", "hc_read_error_word",
     "hc_read_batch_plan", "hc_read_batch_groups", "hc_read_set_batch_lanes", "hc_read_q8",
     "hc_read_batch_q8", "hc_read_batch_q8_plan", "hc_read_batch_q8_groups",
+    "hc_q2_0_matvec", "hc_q2_0_matvec_batch",
 )
 
 
@@ -38,6 +39,11 @@ class hc_read_q8_desc(ctypes.Structure):
     """One Q8_0 read of hc_read_batch_q8 (field order of the C struct)."""
     _fields_ = [(name, ctypes.c_void_p) for name in (
         "R", "w_norm", "Wd_q", "Wd_scale", "Wu_q", "Wu_scale", "gate", "pending", "out", "mean", "lo")]
+
+
+class hc_q2_0_desc(ctypes.Structure):
+    """One product of hc_q2_0_matvec_batch (field order of the C struct)."""
+    _fields_ = [(name, ctypes.c_void_p) for name in ("Wq", "Wscale", "x", "y")]
 
 
 class HcError(RuntimeError):
@@ -115,6 +121,11 @@ def load(path: str | None = None):
                                             ctypes.POINTER(ctypes.c_int)]
     lib.hc_read_error_word.restype = ctypes.c_int64
     lib.hc_read_error_word.argtypes = [_vp]
+    lib.hc_q2_0_matvec.restype = ctypes.c_int
+    lib.hc_q2_0_matvec.argtypes = [_vp, _vp, ctypes.c_int, ctypes.c_int, _vp, ctypes.c_int, _vp, _vp]
+    lib.hc_q2_0_matvec_batch.restype = ctypes.c_int
+    lib.hc_q2_0_matvec_batch.argtypes = [ctypes.POINTER(hc_q2_0_desc), ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_int, ctypes.c_int, _vp]
     lib.hc_read_batch_persistent.restype = ctypes.c_int
     lib.hc_read_batch_persistent.argtypes = [_vp, ctypes.c_int]
     if path is None:
@@ -213,6 +224,41 @@ def hc_read_q8(h: int, geometry, R, w_norm, Wd_q, Wd_scale, Wu_q, Wu_scale, gate
         _ptr(r_out, "r_out", _F32, T * N), _ptr(rs, "rs", _F32, T * n), _stream_ptr(stream),
     )
     _check(load().hc_read_q8(*args), "hc_read_q8")
+
+def hc_q2_0_matvec(Wq, Wscale, x, y, rows: int | None = None, cols: int | None = None,
+                   ncols: int | None = None, stream=None) -> None:
+    """Enqueue y = W x over Q2_0 weights (see include/hc_q2.h): Wq uint8
+    [rows][cols/4], Wscale binary16 bits [rows][cols/64] (float16, int16 or
+    uint16), x float32 [ncols][cols], y float32 [ncols][rows].  Sizes come
+    from the tensors' shapes unless given (needed for raw pointers)."""
+    if rows is None:
+        rows = Wq.shape[0]
+    if cols is None:
+        cols = Wq.shape[-1] * 4
+    if ncols is None:
+        ncols = x.shape[0] if x.dim() == 2 else 1
+    args = (
+        _ptr(Wq, "Wq", ("uint8",), rows * cols // 4),
+        _ptr(Wscale, "Wscale", _HALF_BITS, rows * (cols // 64)),
+        rows, cols,
+        _ptr(x, "x", _F32, ncols * cols), ncols,
+        _ptr(y, "y", _F32, ncols * rows), _stream_ptr(stream),
+    )
+    _check(load().hc_q2_0_matvec(*args), "hc_q2_0_matvec")
+
+
+def hc_q2_0_matvec_batch(products, rows: int, cols: int, ncols: int, stream=None) -> None:
+    """Enqueue a batch of Q2_0 products of one shape (see include/hc_q2.h):
+    ``products`` is a list of (Wq, Wscale, x, y) tensors (or int pointers)."""
+    arr = (hc_q2_0_desc * max(1, len(products)))()
+    for j, (Wq, Ws, x, y) in enumerate(products):
+        arr[j] = hc_q2_0_desc(
+            _ptr(Wq, "Wq", ("uint8",), rows * cols // 4),
+            _ptr(Ws, "Wscale", _HALF_BITS, rows * (cols // 64)),
+            _ptr(x, "x", _F32, ncols * cols), _ptr(y, "y", _F32, ncols * rows))
+    _check(load().hc_q2_0_matvec_batch(arr, len(products), rows, cols, ncols, _stream_ptr(stream)),
+           "hc_q2_0_matvec_batch")
+
 
 def hc_read(h: int, geometry, R, w_norm, W_down, W_up, gate, pending, T: int,
             out, mean, lo, stream=None) -> None:

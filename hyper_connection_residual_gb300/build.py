@@ -1,6 +1,7 @@
 """Compile the CUDA library ``libhcread.so`` in-tree for sm_103a.
 
-One translation unit (host C ABI + kernels), one ``-gencode``:
+Two translation units (the read's host C ABI + kernels, and the Q2_0
+matrix-vector product's), one ``-gencode``:
 ``nvcc -gencode arch=compute_103a,code=sm_103a``.  The library links the
 CUDA runtime statically, so it only needs the driver at run time.
 """
@@ -16,10 +17,10 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libhcread.so")
-SOURCES = [os.path.join(CSRC, "hc_read.cu")]
+SOURCES = [os.path.join(CSRC, "hc_read.cu"), os.path.join(CSRC, "hc_q2.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, f) for f in (
     "hc_kernels.cuh", "hc_kernels_tc.cuh", "hc_kernels_umma.cuh", "hc_window.cuh", "hc_ptx.cuh")] + [
-    os.path.join(INCLUDE, "hc_read.h")]
+    os.path.join(INCLUDE, "hc_read.h"), os.path.join(INCLUDE, "hc_q2.h")]
 
 NVCC_FLAGS = [
     "-O3", "-std=c++17", "-lineinfo",
