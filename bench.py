@@ -558,7 +558,8 @@ def run_q2_sweep(torch, hc, dev, stream, steps: int = 5, warmup: int = 3, calls:
 
 
 def run_profile_q2_case():
-    """Q2_0 products (2560 -> 12288) at 1 and 4 columns, two of each, each
+    """Q2_0 products (2560 -> 12288): one at 1 column and one at 4 columns, then
+    one batch of 24 at 4 columns over 24 copies of the weights (212 MB), each
     after a 256 MB write that flushes L2; a small case for ncu."""
     import torch
     import hyper_connection_residual_gb300 as hc
@@ -567,12 +568,15 @@ def run_profile_q2_case():
     m = synth.q2_0_matrix(Q2_ROWS, Q2_COLS, j=0)
     Wq = torch.from_numpy(m.Wq).to(dev)
     Ws = torch.from_numpy(m.Wscale.view(np.int16)).to(dev)
+    copies = [(Wq.clone(), Ws.clone()) for _ in range(Q2_COPIES)]
     x = torch.from_numpy(synth.q2_0_columns(Q2_COLS, 4, j=0)).to(dev)
-    y = torch.empty(4, Q2_ROWS, device=dev)
+    ys = [torch.empty(4, Q2_ROWS, device=dev) for _ in range(Q2_COPIES)]
     flush = torch.empty(64 * 1024 * 1024, device=dev)
-    for ncols in (1, 1, 4, 4):
+    for ncols in (1, 4):
         flush.zero_()
-        hc.hc_q2_0_matvec(Wq, Ws, x[:ncols], y[:ncols])
+        hc.hc_q2_0_matvec(Wq, Ws, x[:ncols], ys[0][:ncols])
+    flush.zero_()
+    hc.hc_q2_0_matvec_batch([(*copies[i], x, ys[i]) for i in range(Q2_COPIES)], Q2_ROWS, Q2_COLS, 4)
     torch.cuda.synchronize()
     print("profile case done")
     return 0
