@@ -514,45 +514,46 @@ def q2_bytes(rows: int, cols: int, ncols: int) -> int:
     return rows * cols // 4 + rows * (cols // 64) * 2 + ncols * cols * 4 + ncols * rows * 4
 
 
-def run_q2_sweep(torch, hc, dev, stream, steps: int = 5, warmup: int = 3, calls: int = CALLS,
-                 batch: bool = True):
+def run_q2_sweep(torch, hc, dev, stream, steps: int = 5, warmup: int = 3, calls: int = CALLS):
     """The Q2_0 product of the decode windows' attn_q (2560 -> 12288) at 1..4
     columns, cold: 300 products per case rotated over 24 copies of the weights
     (212 MB, more than L2), one input, own outputs, captured once as a CUDA
-    graph and replayed; as one hc_q2_0_matvec_batch (products overlap) or as
-    300 hc_q2_0_matvec calls (each waits for the one before)."""
+    graph and replayed; as one hc_q2_0_matvec_batch (independent products
+    share a persistent launch) and as 300 hc_q2_0_matvec calls (each waits for
+    the one before).  Returns {mode: {ncols: (seconds per product, GB/s)}}."""
     m = synth.q2_0_matrix(Q2_ROWS, Q2_COLS, j=0)
     Wq0 = torch.from_numpy(m.Wq).to(dev)
     Ws0 = torch.from_numpy(m.Wscale.view(np.int16)).to(dev)
     copies = [(Wq0.clone(), Ws0.clone()) for _ in range(Q2_COPIES)]
     x = torch.from_numpy(synth.q2_0_columns(Q2_COLS, 4, j=0)).to(dev)
     ys = [torch.empty(4, Q2_ROWS, device=dev) for _ in range(Q2_COPIES)]
-    out = {}
-    for ncols in (1, 2, 3, 4):
-        xv = x[:ncols]
-        prods = [(*copies[i % Q2_COPIES], xv, ys[i % Q2_COPIES][:ncols]) for i in range(calls)]
-        torch.cuda.synchronize()
-        with torch.cuda.stream(stream):
-            hc.hc_graph_begin(stream)
-            if batch:
-                hc.hc_q2_0_matvec_batch(prods, Q2_ROWS, Q2_COLS, ncols, stream=stream)
-            else:
-                for p in prods:
-                    hc.hc_q2_0_matvec(*p, stream=stream)
-            graph = hc.hc_graph_end(stream)
-        for _ in range(warmup):
-            hc.hc_graph_launch(graph, stream)
-        stream.synchronize()
-        ea = torch.cuda.Event(enable_timing=True)
-        eb = torch.cuda.Event(enable_timing=True)
-        ea.record(stream)
-        for _ in range(steps):
-            hc.hc_graph_launch(graph, stream)
-        eb.record(stream)
-        eb.synchronize()
-        hc.hc_graph_destroy(graph)
-        sec = ea.elapsed_time(eb) / 1e3 / (steps * calls)
-        out[ncols] = (sec, q2_bytes(Q2_ROWS, Q2_COLS, ncols) / sec / 1e9)
+    out = {"batch": {}, "chained": {}}
+    for mode in out:
+        for ncols in (1, 2, 3, 4):
+            xv = x[:ncols]
+            prods = [(*copies[i % Q2_COPIES], xv, ys[i % Q2_COPIES][:ncols]) for i in range(calls)]
+            torch.cuda.synchronize()
+            with torch.cuda.stream(stream):
+                hc.hc_graph_begin(stream)
+                if mode == "batch":
+                    hc.hc_q2_0_matvec_batch(prods, Q2_ROWS, Q2_COLS, ncols, stream=stream)
+                else:
+                    for p in prods:
+                        hc.hc_q2_0_matvec(*p, stream=stream)
+                graph = hc.hc_graph_end(stream)
+            for _ in range(warmup):
+                hc.hc_graph_launch(graph, stream)
+            stream.synchronize()
+            ea = torch.cuda.Event(enable_timing=True)
+            eb = torch.cuda.Event(enable_timing=True)
+            ea.record(stream)
+            for _ in range(steps):
+                hc.hc_graph_launch(graph, stream)
+            eb.record(stream)
+            eb.synchronize()
+            hc.hc_graph_destroy(graph)
+            sec = ea.elapsed_time(eb) / 1e3 / (steps * calls)
+            out[mode][ncols] = (sec, q2_bytes(Q2_ROWS, Q2_COLS, ncols) / sec / 1e9)
     del copies, ys
     return out
 
@@ -684,16 +685,15 @@ def run_gpu(args):
             "GBps": sum(q8.bytes_per_replay(c) for c in q8.cases) * 5 / tq / 1e9}
         q8.close()
         q2 = run_q2_sweep(torch, hc, dev, stream)
-        q2s = run_q2_sweep(torch, hc, dev, stream, batch=False)
         hbm = measured_peaks()["hbm_gbs"]
         extra["q2_0_matvec_attn_q"] = {
             "note": "Q2_0 product 2560 -> 12288 (two-bit codes, one binary16 scale per 64 weights: "
                     "8,847,360 B of weights), 300 products per case rotated over 24 copies of the "
                     "weights (212 MB), one input, CUDA-graph replay; bytes = weights + x + y once",
-            "us_per_call": {f"ncols{n}": 1e6 * v[0] for n, v in q2.items()},
-            "GBps": {f"ncols{n}": v[1] for n, v in q2.items()},
-            "frac_of_measured_hbm": {f"ncols{n}": v[1] / hbm for n, v in q2.items()},
-            "us_per_call_chained": {f"ncols{n}": 1e6 * v[0] for n, v in q2s.items()},
+            "us_per_call": {f"ncols{n}": 1e6 * v[0] for n, v in q2["batch"].items()},
+            "GBps": {f"ncols{n}": v[1] for n, v in q2["batch"].items()},
+            "frac_of_measured_hbm": {f"ncols{n}": v[1] / hbm for n, v in q2["batch"].items()},
+            "us_per_call_chained": {f"ncols{n}": 1e6 * v[0] for n, v in q2["chained"].items()},
             "chained_note": "the same 300 products as single hc_q2_0_matvec calls: each waits for "
                             "the one before (the engine's case when x comes from the previous layer)",
             "pages_rtx2080ti_us": {"ncols1": 24.8, "ncols2": 31.4, "ncols3": 31.3, "ncols4": 36.6},
