@@ -84,7 +84,7 @@ struct Layout {
   int scale_pitch;  // bytes between rows of a scale tile
   int stage;        // bytes of one stage (codes, then scales)
   int scales, xs, kb, wmax, red, bytes;
-  __host__ __device__ Layout(int cols, int nc) {
+  __host__ __device__ Layout(int cols, int nc, int parts) {
     nb = cols / 64;
     // cols / 4 code bytes a row plus 16: the pitch in words is 4 * odd, so the
     // eight rows g of an MMA fragment fall on eight different groups of four
@@ -96,8 +96,8 @@ struct Layout {
     xs = kStages * stage;                  // [nb][2 halves][2 nc][4][16 B] binary16x2
     kb = xs + nb * 2 * (2 * nc) * 4 * 16;  // [nb][nc] float: accumulator seeds
     wmax = kb + nb * nc * 4;               // [8 warps][nc] float: max|x| per warp
-    red = wmax + kWarps * nc * 4;          // [4 quarters][32 rows][nc] float
-    bytes = red + 4 * kRows * nc * 4;
+    red = wmax + kWarps * nc * 4;          // [parts][32 rows][nc] float
+    bytes = red + parts * kRows * nc * 4;
   }
 };
 
@@ -183,10 +183,16 @@ struct Cursor {
   }
 };
 
-template <int NC>
-__global__ void __launch_bounds__(kThreads) hc_q2_matvec_kernel(const __grid_constant__ Args a) {
+// KPB > 0: the form for cols = 512 * KPB in which warp w takes both row
+// groups over the w-th eighth of the blocks (KPB blocks) and keeps that
+// eighth of x's B layout in registers for as long as x stays the same.
+// KPB = 0: any width; warp w takes one row group over a quarter of the
+// blocks and reads the B layout from shared memory.
+template <int NC, int KPB>
+__global__ void __launch_bounds__(kThreads, 2) hc_q2_matvec_kernel(const __grid_constant__ Args a) {
   extern __shared__ __align__(16) uint8_t smem[];
-  const Layout L(a.cols, NC);
+  constexpr int kParts = KPB > 0 ? kWarps : 4;  // partial sums per row
+  const Layout L(a.cols, NC, kParts);
   uint4* xs = reinterpret_cast<uint4*>(smem + L.xs);
   float* kb = reinterpret_cast<float*>(smem + L.kb);
   float* wmax = reinterpret_cast<float*>(smem + L.wmax);
@@ -225,9 +231,13 @@ __global__ void __launch_bounds__(kThreads) hc_q2_matvec_kernel(const __grid_con
   ptx::wait_prerequisites();
   ptx::launch_dependents();
 
-  // Warp w: rows 16 rg + g and + 8 of a tile, blocks [kq nq, (kq + 1) nq).
-  const int rg = warp & 1, kq = warp >> 1;
-  const int nq = nb / 4, b0 = kq * nq;
+  // Warp w: rows 16 rg + g and + 8 of a tile, blocks [kq nq, (kq + 1) nq)
+  // (KPB = 0); or all 32 rows, blocks [w KPB, (w + 1) KPB).
+  const int rg = KPB > 0 ? 0 : warp & 1, kq = KPB > 0 ? warp : warp >> 1;
+  const int nq = KPB > 0 ? KPB : nb / 4, b0 = kq * nq;
+  constexpr int kRegBlocks = KPB > 0 ? KPB : 1;
+  uint4 breg_l[kRegBlocks], breg_h[kRegBlocks];  // B fragments of this warp's blocks (KPB > 0)
+  float sreg[kRegBlocks];                         // their accumulator seeds
   const int co = (16 * rg + g) * L.code_pitch + 4 * t + 16 * b0;
   const int so = (16 * rg + g) * L.scale_pitch + 2 * b0;
   const bool has_b = g < 2 * NC;  // B columns past 2 NC are zero
@@ -311,51 +321,108 @@ __global__ void __launch_bounds__(kThreads) hc_q2_matvec_kernel(const __grid_con
       }
       staged = pr.x;
       __syncthreads();
+      if constexpr (KPB > 0) {
+#pragma unroll
+        for (int b = 0; b < KPB; ++b) {
+          breg_l[b] = has_b ? bp[(2 * b) * (8 * NC)] : make_uint4(0u, 0u, 0u, 0u);
+          breg_h[b] = has_b ? bp[(2 * b + 1) * (8 * NC)] : make_uint4(0u, 0u, 0u, 0u);
+          sreg[b] = t < NC ? kp[b * NC] : 0.f;
+        }
+      }
     }
 
     const uint8_t* st = smem + (k % kStages) * L.stage;
-    const uint8_t* c0 = st + co;
-    const uint8_t* c1 = c0 + 8 * L.code_pitch;
-    const __half* s0 = reinterpret_cast<const __half*>(st + L.scales + so);
-    const __half* s1 = reinterpret_cast<const __half*>(st + L.scales + so + 8 * L.scale_pitch);
-    float tot0 = 0.f, tot1 = 0.f;
-#pragma unroll 2
-    for (int b = 0; b < nq; ++b) {
-      const uint32_t w0 = *reinterpret_cast<const uint32_t*>(c0 + 16 * b);
-      const uint32_t w1 = *reinterpret_cast<const uint32_t*>(c1 + 16 * b);
-      uint4 bl = make_uint4(0u, 0u, 0u, 0u), bh = bl;
-      float seed = 0.f;
-      if (has_b) {
-        bl = bp[(2 * b) * (8 * NC)];
-        bh = bp[(2 * b + 1) * (8 * NC)];
+    if constexpr (KPB > 0) {
+      // rows g, g + 8 (chain 0) and 16 + g, 24 + g (chain 1)
+      const uint8_t* c0 = st + co;
+      const int sp = L.scale_pitch / 2;  // halves between scale rows
+      const __half* s0 = reinterpret_cast<const __half*>(st + L.scales + so);
+      float t0 = 0.f, t1 = 0.f, t2 = 0.f, t3 = 0.f;
+#pragma unroll
+      for (int b = 0; b < KPB; ++b) {
+        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(c0 + 16 * b);
+        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(c0 + 8 * L.code_pitch + 16 * b);
+        const uint32_t w2 = *reinterpret_cast<const uint32_t*>(c0 + 16 * L.code_pitch + 16 * b);
+        const uint32_t w3 = *reinterpret_cast<const uint32_t*>(c0 + 24 * L.code_pitch + 16 * b);
+        uint32_t p0[8], p1[8], p2[8], p3[8];
+        q2_decode(w0, p0);
+        q2_decode(w1, p1);
+        q2_decode(w2, p2);
+        q2_decode(w3, p3);
+        const uint4 bl = breg_l[b], bh = breg_h[b];
+        const float seed = sreg[b];
+        float d[4], e[4];
+        const uint32_t a0[4] = {p0[0], p1[0], p0[1], p1[1]};
+        const uint32_t f0[4] = {p2[0], p3[0], p2[1], p3[1]};
+        mma_f16(d, a0, bl.x, bl.y, seed, 0.f, seed, 0.f);
+        mma_f16(e, f0, bl.x, bl.y, seed, 0.f, seed, 0.f);
+        const uint32_t a1[4] = {p0[2], p1[2], p0[3], p1[3]};
+        const uint32_t f1[4] = {p2[2], p3[2], p2[3], p3[3]};
+        mma_f16(d, a1, bl.z, bl.w);
+        mma_f16(e, f1, bl.z, bl.w);
+        const uint32_t a2[4] = {p0[4], p1[4], p0[5], p1[5]};
+        const uint32_t f2[4] = {p2[4], p3[4], p2[5], p3[5]};
+        mma_f16(d, a2, bh.x, bh.y);
+        mma_f16(e, f2, bh.x, bh.y);
+        const uint32_t a3[4] = {p0[6], p1[6], p0[7], p1[7]};
+        const uint32_t f3[4] = {p2[6], p3[6], p2[7], p3[7]};
+        mma_f16(d, a3, bh.z, bh.w);
+        mma_f16(e, f3, bh.z, bh.w);
+        t0 = __fmaf_rn(__half2float(s0[b]), __fadd_rn(d[0], d[1]), t0);
+        t1 = __fmaf_rn(__half2float(s0[8 * sp + b]), __fadd_rn(d[2], d[3]), t1);
+        t2 = __fmaf_rn(__half2float(s0[16 * sp + b]), __fadd_rn(e[0], e[1]), t2);
+        t3 = __fmaf_rn(__half2float(s0[24 * sp + b]), __fadd_rn(e[2], e[3]), t3);
       }
-      if (t < NC) seed = kp[b * NC];
-      uint32_t p0[8], p1[8];
-      q2_decode(w0, p0);
-      q2_decode(w1, p1);
-      float d[4];
-      const uint32_t a0[4] = {p0[0], p1[0], p0[1], p1[1]};
-      mma_f16(d, a0, bl.x, bl.y, seed, 0.f, seed, 0.f);
-      const uint32_t a1[4] = {p0[2], p1[2], p0[3], p1[3]};
-      mma_f16(d, a1, bl.z, bl.w);
-      const uint32_t a2[4] = {p0[4], p1[4], p0[5], p1[5]};
-      mma_f16(d, a2, bh.x, bh.y);
-      const uint32_t a3[4] = {p0[6], p1[6], p0[7], p1[7]};
-      mma_f16(d, a3, bh.z, bh.w);
-      // d[0], d[1]: row g, column t (hi and lo terms); d[2], d[3]: row g + 8.
-      tot0 = __fmaf_rn(__half2float(s0[b]), __fadd_rn(d[0], d[1]), tot0);
-      tot1 = __fmaf_rn(__half2float(s1[b]), __fadd_rn(d[2], d[3]), tot1);
-    }
-    if (t < NC) {
-      red[(kq * kRows + 16 * rg + g) * NC + t] = tot0;
-      red[(kq * kRows + 16 * rg + g + 8) * NC + t] = tot1;
+      if (t < NC) {
+        red[(kq * kRows + g) * NC + t] = t0;
+        red[(kq * kRows + g + 8) * NC + t] = t1;
+        red[(kq * kRows + g + 16) * NC + t] = t2;
+        red[(kq * kRows + g + 24) * NC + t] = t3;
+      }
+    } else {
+      const uint8_t* c0 = st + co;
+      const uint8_t* c1 = c0 + 8 * L.code_pitch;
+      const __half* s0 = reinterpret_cast<const __half*>(st + L.scales + so);
+      const __half* s1 = reinterpret_cast<const __half*>(st + L.scales + so + 8 * L.scale_pitch);
+      float tot0 = 0.f, tot1 = 0.f;
+#pragma unroll 2
+      for (int b = 0; b < nq; ++b) {
+        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(c0 + 16 * b);
+        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(c1 + 16 * b);
+        uint4 bl = make_uint4(0u, 0u, 0u, 0u), bh = bl;
+        float seed = 0.f;
+        if (has_b) {
+          bl = bp[(2 * b) * (8 * NC)];
+          bh = bp[(2 * b + 1) * (8 * NC)];
+        }
+        if (t < NC) seed = kp[b * NC];
+        uint32_t p0[8], p1[8];
+        q2_decode(w0, p0);
+        q2_decode(w1, p1);
+        float d[4];
+        const uint32_t a0[4] = {p0[0], p1[0], p0[1], p1[1]};
+        mma_f16(d, a0, bl.x, bl.y, seed, 0.f, seed, 0.f);
+        const uint32_t a1[4] = {p0[2], p1[2], p0[3], p1[3]};
+        mma_f16(d, a1, bl.z, bl.w);
+        const uint32_t a2[4] = {p0[4], p1[4], p0[5], p1[5]};
+        mma_f16(d, a2, bh.x, bh.y);
+        const uint32_t a3[4] = {p0[6], p1[6], p0[7], p1[7]};
+        mma_f16(d, a3, bh.z, bh.w);
+        // d[0], d[1]: row g, column t (hi and lo terms); d[2], d[3]: row g + 8.
+        tot0 = __fmaf_rn(__half2float(s0[b]), __fadd_rn(d[0], d[1]), tot0);
+        tot1 = __fmaf_rn(__half2float(s1[b]), __fadd_rn(d[2], d[3]), tot1);
+      }
+      if (t < NC) {
+        red[(kq * kRows + 16 * rg + g) * NC + t] = tot0;
+        red[(kq * kRows + 16 * rg + g + 8) * NC + t] = tot1;
+      }
     }
     __syncthreads();
     if (tid < kRows * NC) {
       const int i = tid / NC, c = tid - i * NC;
       float s = red[i * NC + c];
 #pragma unroll
-      for (int m = 1; m < 4; ++m) s = __fadd_rn(s, red[(m * kRows + i) * NC + c]);
+      for (int m = 1; m < kParts; ++m) s = __fadd_rn(s, red[(m * kRows + i) * NC + c]);
       float u = unscale[0];
 #pragma unroll
       for (int cc = 1; cc < NC; ++cc) u = c == cc ? unscale[cc] : u;
@@ -369,7 +436,7 @@ __global__ void __launch_bounds__(kThreads) hc_q2_matvec_kernel(const __grid_con
 
 // CTAs of one launch: as many as can run at once (the kernel is persistent),
 // at most one per tile.
-template <int NC>
+template <int NC, int KPB>
 cudaError_t launch(const Args& a, cudaStream_t st) {
   static std::once_flag once[64];
   static cudaError_t configured[64];
@@ -380,18 +447,18 @@ cudaError_t launch(const Args& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::call_once(once[dev], [&] {
-    configured[dev] = cudaFuncSetAttribute(hc_q2_matvec_kernel<NC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           Layout(kMaxCols, NC).bytes);
+    configured[dev] = cudaFuncSetAttribute(hc_q2_matvec_kernel<NC, KPB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           Layout(kMaxCols, NC, KPB > 0 ? kWarps : 4).bytes);
     if (configured[dev] == cudaSuccess)
       configured[dev] = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
     for (int i = 0; i <= kMaxCols / kMinCols; ++i) per_sm[dev][i] = 0;
   });
   if (configured[dev] != cudaSuccess) return configured[dev];
-  const int smem = Layout(a.cols, NC).bytes;
+  const int smem = Layout(a.cols, NC, KPB > 0 ? kWarps : 4).bytes;
   int& n = per_sm[dev][a.cols / kMinCols];
   if (n == 0) {
     int v = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, hc_q2_matvec_kernel<NC>, kThreads, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, hc_q2_matvec_kernel<NC, KPB>, kThreads, smem);
     if (e != cudaSuccess) return e;
     if (v < 1) return cudaErrorInvalidConfiguration;
     n = v;
@@ -408,7 +475,7 @@ cudaError_t launch(const Args& a, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, hc_q2_matvec_kernel<NC>, a);
+  return cudaLaunchKernelEx(&cfg, hc_q2_matvec_kernel<NC, KPB>, a);
 }
 
 bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
@@ -444,12 +511,25 @@ int check_sizes(int rows, int cols, int ncols) {
   return HC_OK;
 }
 
+// The register form for the pages' width (2560 columns: 5 blocks a warp) at
+// 1..3 columns, the shared-memory form otherwise (measured on GB300, µs per
+// product in a cold batch at 1 / 2 / 3 / 4 columns: register form 3.14 /
+// 3.27 / 3.45 / 4.50, shared-memory form 3.51 / 3.59 / 3.82 / 3.58; at 4
+// columns the register form is at its 128-register limit).
+template <int NC>
+cudaError_t launch_nc(const Args& a, cudaStream_t st) {
+  if constexpr (NC < 4) {
+    if (a.cols == 2560) return launch<NC, 5>(a, st);
+  }
+  return launch<NC, 0>(a, st);
+}
+
 cudaError_t launch_any(const Args& a, int ncols, cudaStream_t st) {
   switch (ncols) {
-    case 1: return launch<1>(a, st);
-    case 2: return launch<2>(a, st);
-    case 3: return launch<3>(a, st);
-    default: return launch<4>(a, st);
+    case 1: return launch_nc<1>(a, st);
+    case 2: return launch_nc<2>(a, st);
+    case 3: return launch_nc<3>(a, st);
+    default: return launch_nc<4>(a, st);
   }
 }
 
