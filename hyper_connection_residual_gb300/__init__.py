@@ -25,6 +25,7 @@ from ._binding import (  # noqa: F401
     hc_q2_0_desc,
     hc_q2_0_matvec,
     hc_q2_0_matvec_batch,
+    hc_q2_0_matvec_batch_plan,
     hc_read,
     hc_read_batch,
     hc_read_batch_groups,

@@ -25,7 +25,7 @@ EXPORTS = (
     "hc_read_noalloc", "hc_read_batch", "hc_read_batch_persistent", "hc_read_error_word",
     "hc_read_batch_plan", "hc_read_batch_groups", "hc_read_set_batch_lanes", "hc_read_q8",
     "hc_read_batch_q8", "hc_read_batch_q8_plan", "hc_read_batch_q8_groups",
-    "hc_q2_0_matvec", "hc_q2_0_matvec_batch",
+    "hc_q2_0_matvec", "hc_q2_0_matvec_batch", "hc_q2_0_matvec_batch_plan",
 )
 
 
@@ -126,6 +126,9 @@ def load(path: str | None = None):
     lib.hc_q2_0_matvec_batch.restype = ctypes.c_int
     lib.hc_q2_0_matvec_batch.argtypes = [ctypes.POINTER(hc_q2_0_desc), ctypes.c_int, ctypes.c_int,
                                          ctypes.c_int, ctypes.c_int, _vp]
+    lib.hc_q2_0_matvec_batch_plan.restype = ctypes.c_int
+    lib.hc_q2_0_matvec_batch_plan.argtypes = [ctypes.POINTER(hc_q2_0_desc), ctypes.c_int, ctypes.c_int,
+                                              ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
     lib.hc_read_batch_persistent.restype = ctypes.c_int
     lib.hc_read_batch_persistent.argtypes = [_vp, ctypes.c_int]
     if path is None:
@@ -258,6 +261,20 @@ def hc_q2_0_matvec_batch(products, rows: int, cols: int, ncols: int, stream=None
             _ptr(x, "x", _F32, ncols * cols), _ptr(y, "y", _F32, ncols * rows))
     _check(load().hc_q2_0_matvec_batch(arr, len(products), rows, cols, ncols, _stream_ptr(stream)),
            "hc_q2_0_matvec_batch")
+
+
+def hc_q2_0_matvec_batch_plan(products, rows: int, cols: int, ncols: int) -> list[int]:
+    """The launch each product of a batch goes to (host logic; ``products`` as
+    for hc_q2_0_matvec_batch, or (Wq, Wscale, x, y) integer addresses)."""
+    n = len(products)
+    arr = (hc_q2_0_desc * max(1, n))()
+    for j, p in enumerate(products):
+        arr[j] = hc_q2_0_desc(*[v if isinstance(v, int) else v.data_ptr() for v in p])
+    out = (ctypes.c_int * max(1, n))()
+    rc = load().hc_q2_0_matvec_batch_plan(arr, n, rows, cols, ncols, out)
+    if rc < 0:
+        raise HcError(rc, "hc_q2_0_matvec_batch_plan")
+    return list(out[:n])
 
 
 def hc_read(h: int, geometry, R, w_norm, W_down, W_up, gate, pending, T: int,

@@ -43,6 +43,7 @@
 
 #include <cstdint>
 #include <mutex>
+#include <vector>
 
 #include "hc_ptx.cuh"
 #include "hc_q2.h"
@@ -543,6 +544,42 @@ HC_EXPORT int hc_q2_0_matvec(const uint8_t* Wq, const uint16_t* Wscale, int rows
   return hc_q2_0_matvec_batch(&d, 1, rows, cols, ncols, stream);
 }
 
+// Which launch each product of a batch goes to: a product joins the launch
+// being assembled unless that launch holds kLaunchProducts products already
+// or the product shares memory with one of them (reads an earlier y, or
+// writes over an earlier operand).  Returns the number of launches.
+static int plan_launches(const hc_q2_0_desc* descs, int count, const hc::q2::Ranges& b, int* launch) {
+  using namespace hc::q2;
+  int launches = 0, first = 0, in_launch = 0;
+  for (int j = 0; j < count; ++j) {
+    bool flush = in_launch == kLaunchProducts;
+    for (int i = first; i < j && !flush; ++i) {
+      const hc_q2_0_desc& d = descs[j];
+      const hc_q2_0_desc& e = descs[i];
+      flush = overlaps(d.x, b.x, e.y, b.y) || overlaps(d.Wq, b.wq, e.y, b.y) || overlaps(d.Wscale, b.ws, e.y, b.y) ||
+              overlaps(d.y, b.y, e.y, b.y) || overlaps(d.y, b.y, e.x, b.x) || overlaps(d.y, b.y, e.Wq, b.wq) ||
+              overlaps(d.y, b.y, e.Wscale, b.ws);
+    }
+    if (j == 0 || flush) {
+      ++launches;
+      first = j;
+      in_launch = 0;
+    }
+    launch[j] = launches - 1;
+    ++in_launch;
+  }
+  return launches;
+}
+
+HC_EXPORT int hc_q2_0_matvec_batch_plan(const hc_q2_0_desc* descs, int count, int rows, int cols, int ncols,
+                                        int* launch) {
+  using namespace hc::q2;
+  if (!descs || !launch || count < 1) return HC_ERR_ARG;
+  const int rc = check_sizes(rows, cols, ncols);
+  if (rc != HC_OK) return rc;
+  return plan_launches(descs, count, Ranges(rows, cols, ncols), launch);
+}
+
 HC_EXPORT int hc_q2_0_matvec_batch(const hc_q2_0_desc* descs, int count, int rows, int cols, int ncols,
                                    hc_stream_t stream) {
   using namespace hc::q2;
@@ -554,30 +591,20 @@ HC_EXPORT int hc_q2_0_matvec_batch(const hc_q2_0_desc* descs, int count, int row
     rc = check_product(descs[j].Wq, descs[j].Wscale, descs[j].x, descs[j].y, b);
     if (rc != HC_OK) return rc;
   }
+  std::vector<int> launch(static_cast<size_t>(count));
+  plan_launches(descs, count, b, launch.data());
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   Args a;
   a.rows = rows;
   a.cols = cols;
   a.tiles = (rows + kRows - 1) / kRows;
   a.count = 0;
-  int first = 0;  // first product of the launch being assembled
-  for (int j = 0; j <= count; ++j) {
-    bool flush = j == count || a.count == kLaunchProducts;
-    for (int i = first; i < j && !flush; ++i) {
-      // a product that reads an earlier output of its launch, or writes over
-      // an operand of one, starts a new launch (which waits for the last)
-      const hc_q2_0_desc& d = descs[j];
-      const hc_q2_0_desc& e = descs[i];
-      flush = overlaps(d.x, b.x, e.y, b.y) || overlaps(d.Wq, b.wq, e.y, b.y) || overlaps(d.Wscale, b.ws, e.y, b.y) ||
-              overlaps(d.y, b.y, e.y, b.y) || overlaps(d.y, b.y, e.x, b.x) || overlaps(d.y, b.y, e.Wq, b.wq) ||
-              overlaps(d.y, b.y, e.Wscale, b.ws);
-    }
-    if (flush && a.count > 0) {
+  for (int j = 0; j < count; ++j) {
+    a.p[a.count++] = Product{descs[j].Wq, descs[j].Wscale, descs[j].x, descs[j].y};
+    if (j + 1 == count || launch[j + 1] != launch[j]) {
       if (launch_any(a, ncols, st) != cudaSuccess) return HC_ERR_CUDA;
       a.count = 0;
-      first = j;
     }
-    if (j < count) a.p[a.count++] = Product{descs[j].Wq, descs[j].Wscale, descs[j].x, descs[j].y};
   }
   return HC_OK;
 }

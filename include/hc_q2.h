@@ -93,6 +93,16 @@ typedef struct {
 int hc_q2_0_matvec_batch(const hc_q2_0_desc* descs, int count, int rows, int cols, int ncols,
                          hc_stream_t stream);
 
+/* How hc_q2_0_matvec_batch would split this batch (same arguments): writes
+ * launch[j], the launch product j goes to (0, 1, ... in order), and returns
+ * the number of launches; HC_ERR_ARG for NULL pointers or no products,
+ * HC_ERR_SHAPE / HC_ERR_ARG for sizes as hc_q2_0_matvec.  A product joins
+ * the launch being assembled unless it holds 120 products already or the
+ * product shares memory with one of them.  Host logic only: the pointers
+ * are compared, never dereferenced, and no device is needed. */
+int hc_q2_0_matvec_batch_plan(const hc_q2_0_desc* descs, int count, int rows, int cols, int ncols,
+                              int* launch);
+
 #ifdef __cplusplus
 }
 #endif
