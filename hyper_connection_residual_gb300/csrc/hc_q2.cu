@@ -57,7 +57,7 @@ constexpr int kThreads = 256;         // 8 warps: 2 row groups of 16 rows x 4 qu
 constexpr int kWarps = kThreads / 32;
 constexpr int kRows = 32;             // rows of one tile
 constexpr int kStages = 3;            // tiles in flight per CTA (one computed, two loading)
-constexpr int kMinCols = 512;         // a quarter holds an even number of 64-value blocks
+constexpr int kMinCols = 512;         // a quarter of a row is an even number of 64-value blocks
 constexpr int kMaxCols = 4096;
 constexpr int kMaxNcols = 4;
 constexpr int kLaunchProducts = 120;  // products per launch (kernel parameters under 4 KB)
