@@ -53,7 +53,7 @@
 namespace hc {
 namespace q2 {
 
-constexpr int kThreads = 256;         // 8 warps: 2 row groups of 16 rows x 4 quarters of the blocks
+constexpr int kThreads = 256;         // 8 warps (their split of a tile: the KPB template below)
 constexpr int kWarps = kThreads / 32;
 constexpr int kRows = 32;             // rows of one tile
 constexpr int kStages = 3;            // tiles in flight per CTA (one computed, two loading)
