@@ -60,6 +60,7 @@ constexpr int kStages = 3;            // tiles in flight per CTA (one computed, 
 constexpr int kMinCols = 512;         // a quarter of a row is an even number of 64-value blocks
 constexpr int kMaxCols = 4096;
 constexpr int kMaxNcols = 4;
+constexpr int kMaxRows = 1 << 24;
 constexpr int kLaunchProducts = 120;  // products per launch (kernel parameters under 4 KB)
 constexpr int kTarget = 13;           // x is scaled so that max|x| lies in [2^13, 2^14)
 
@@ -507,7 +508,9 @@ int check_product(const uint8_t* Wq, const uint16_t* Wscale, const float* x, flo
 }
 
 int check_sizes(int rows, int cols, int ncols) {
-  if (rows < 1 || ncols < 1 || ncols > kMaxNcols) return HC_ERR_ARG;
+  // rows <= 2^24 keeps the tile counts of a launch (products x rows / 32)
+  // inside int
+  if (rows < 1 || rows > kMaxRows || ncols < 1 || ncols > kMaxNcols) return HC_ERR_ARG;
   if (cols < kMinCols || cols > kMaxCols || cols % kMinCols != 0) return HC_ERR_SHAPE;
   return HC_OK;
 }

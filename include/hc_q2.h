@@ -22,7 +22,7 @@
  *   x      : float  [ncols][cols]
  *   y      : float  [ncols][rows]
  *
- * Sizes: rows >= 1; cols a multiple of 512, 512 <= cols <= 4096;
+ * Sizes: 1 <= rows <= 2^24; cols a multiple of 512, 512 <= cols <= 4096;
  * 1 <= ncols <= 4.
  *
  * Arithmetic: each weight is decoded exactly; x is scaled per column by a
@@ -46,8 +46,8 @@
  * triggers its dependents early (kernels that do not use programmatic
  * completion, copies and memsets are always waited for in full).
  *
- * Errors (hc_status of hc_read.h): HC_ERR_ARG for a NULL pointer, rows < 1,
- * ncols outside 1..4, y overlapping an input, or a batch without products;
+ * Errors (hc_status of hc_read.h): HC_ERR_ARG for a NULL pointer, rows
+ * outside 1..2^24, ncols outside 1..4, y overlapping an input, or a batch without products;
  * HC_ERR_SHAPE for cols not supported; HC_ERR_ALIGN for a pointer that is
  * not 16-byte aligned; HC_ERR_CUDA for a launch error.  Nothing is enqueued
  * on an error.  The kernel has no waits of its own.

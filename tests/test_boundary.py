@@ -78,6 +78,7 @@ def test_q2_matvec_rejects_bad_arguments(lib):
     assert f(Wq, Ws, rows, cols, None, ncols, y, None) == hc.HC_ERR_ARG
     assert f(Wq, Ws, rows, cols, x, ncols, None, None) == hc.HC_ERR_ARG
     assert f(Wq, Ws, 0, cols, x, ncols, y, None) == hc.HC_ERR_ARG
+    assert f(Wq, Ws, (1 << 24) + 1, cols, x, ncols, y, None) == hc.HC_ERR_ARG
     for bad in (0, 5, -1):
         assert f(Wq, Ws, rows, cols, x, bad, y, None) == hc.HC_ERR_ARG
     for bad in (256, 2560 + 64, 2560 + 256, 4096 + 512, 16384, 0, -512):
