@@ -47,10 +47,10 @@
  * completion, copies and memsets are always waited for in full).
  *
  * Errors (hc_status of hc_read.h): HC_ERR_ARG for a NULL pointer, rows
- * outside 1..2^24, ncols outside 1..4, y overlapping an input, or a batch without products;
- * HC_ERR_SHAPE for cols not supported; HC_ERR_ALIGN for a pointer that is
- * not 16-byte aligned; HC_ERR_CUDA for a launch error.  Nothing is enqueued
- * on an error.  The kernel has no waits of its own.
+ * outside 1..2^24, ncols outside 1..4, y overlapping an input, or a batch
+ * without products; HC_ERR_SHAPE for cols not supported; HC_ERR_ALIGN for a
+ * pointer that is not 16-byte aligned; HC_ERR_CUDA for a launch error.
+ * Nothing is enqueued on an error.  The kernel has no waits of its own.
  */
 #ifndef HC_Q2_H
 #define HC_Q2_H
