@@ -231,7 +231,7 @@ __device__ __forceinline__ void st_async(uint32_t addr, uint32_t v, uint32_t bar
                : "memory");
 }
 
-// Self-tagged exchange words: fp32 bits with the two low mantissa bits
+// Self-tagged exchange words: fp32 bits with the three low mantissa bits
 // replaced by the epoch modulo 8.
 __device__ __forceinline__ uint32_t tag_word(float v, uint32_t epoch) {
   return (__float_as_uint(v) & ~7u) | (epoch & 7u);
