@@ -43,6 +43,9 @@ from ._binding import (  # noqa: F401
     hc_read_error_word,
     hc_read_ex,
     hc_read_noalloc,
+    hc_read_noalloc_check,
+    hc_read_set_overlap,
+    hc_read_set_wait_limit,
     hc_read_reset,
     hc_read_scratch_bytes,
     library_path,

@@ -26,6 +26,7 @@ EXPORTS = (
     "hc_read_batch_plan", "hc_read_batch_groups", "hc_read_set_batch_lanes", "hc_read_q8",
     "hc_read_batch_q8", "hc_read_batch_q8_plan", "hc_read_batch_q8_groups",
     "hc_q2_0_matvec", "hc_q2_0_matvec_batch", "hc_q2_0_matvec_batch_plan",
+    "hc_read_set_wait_limit", "hc_read_set_overlap", "hc_read_noalloc_check",
 )
 
 
@@ -131,6 +132,12 @@ def load(path: str | None = None):
                                               ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
     lib.hc_read_batch_persistent.restype = ctypes.c_int
     lib.hc_read_batch_persistent.argtypes = [_vp, ctypes.c_int]
+    lib.hc_read_set_wait_limit.restype = ctypes.c_int
+    lib.hc_read_set_wait_limit.argtypes = [_vp, ctypes.c_uint64]
+    lib.hc_read_set_overlap.restype = ctypes.c_int
+    lib.hc_read_set_overlap.argtypes = [_vp, ctypes.c_int]
+    lib.hc_read_noalloc_check.restype = ctypes.c_int
+    lib.hc_read_noalloc_check.argtypes = []
     if path is None:
         _lib = lib
     return lib
@@ -309,6 +316,30 @@ def hc_read_noalloc(geometry, eps, R, w_norm, W_down, W_up, gate, pending, T: in
             _ptr(lo, "lo", _F32, T * K))
     _check(load().hc_read_noalloc(n, d, K, eps, *args, T, *outs, _stream_ptr(stream)),
            "hc_read_noalloc")
+
+
+def hc_read_noalloc_check() -> int:
+    """HC_OK or HC_ERR_TIMEOUT for the hc_read_noalloc calls on the current
+    device since the last check (synchronises the device, clears the record)."""
+    st = load().hc_read_noalloc_check()
+    if st not in (HC_OK, HC_ERR_TIMEOUT):
+        _check(st, "hc_read_noalloc_check")
+    return st
+
+
+def hc_read_set_wait_limit(h: int, ns: int) -> None:
+    """Limit (ns from the kernel's start) of the down kernels' first bulk-copy
+    wait for later reads on the handle; 0 restores the default (1 s)."""
+    _check(load().hc_read_set_wait_limit(h, ns), "hc_read_set_wait_limit")
+
+
+def hc_read_set_overlap(h: int, enabled: bool) -> bool:
+    """Whether reads on the handle may overlap their predecessor; returns the
+    previous setting."""
+    st = load().hc_read_set_overlap(h, 1 if enabled else 0)
+    if st < 0:
+        _check(st, "hc_read_set_overlap")
+    return st == 1
 
 
 def _descs(geometry, reads, T: int):
@@ -498,6 +529,12 @@ class Read:
 
     def check(self) -> int:
         return hc_read_check(self.h)
+
+    def set_wait_limit(self, ns: int) -> None:
+        hc_read_set_wait_limit(self.h, ns)
+
+    def set_overlap(self, enabled: bool) -> bool:
+        return hc_read_set_overlap(self.h, enabled)
 
     def error_word(self) -> int:
         return hc_read_error_word(self.h)

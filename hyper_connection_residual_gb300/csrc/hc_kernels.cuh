@@ -158,6 +158,7 @@ struct DownArgs {
   float eps;
   int independent;         // 1: no read in flight writes R or P (see below)
   int late_launch;         // 1: the read runs among others on the batch lanes (see hc_down_kernel)
+  unsigned long long wait_ns;  // limit of the first bulk-copy wait from the kernel's start (0: kWaitNs)
 };
 
 struct UpArgs {
@@ -230,6 +231,25 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, unsigne
   return true;
 }
 
+// The first bulk-copy wait of a down kernel: gives up once `limit` ns have
+// passed since `t0` (the kernel's start), checked before every probe, so a
+// limit shorter than the kernel's start-up gives up whether or not the copy
+// has landed (the timeout path of a read can be exercised on purpose: see
+// hc_read_set_wait_limit).  The copy itself still lands and is drained.
+__device__ __forceinline__ bool wait_bar_from(uint64_t* bar, uint32_t parity, unsigned* err, unsigned code,
+                                              uint64_t t0, uint64_t limit) {
+  for (;;) {
+    if (ptx::globaltimer_ns() - t0 >= limit) {
+      atomicOr(err, code);
+      return false;
+    }
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+  }
+}
+__device__ __forceinline__ uint64_t first_wait_limit(unsigned long long wait_ns) {
+  return wait_ns != 0ull && wait_ns < kWaitNs ? wait_ns : kWaitNs;
+}
+
 // Before a CTA whose wait timed out exits: wait (bounded again) for copies
 // still in flight into its shared memory.
 __device__ __forceinline__ void drain(uint64_t* bar, uint32_t parity) {
@@ -264,6 +284,7 @@ __global__ void __launch_bounds__(kThreads, D == 2560 ? 3 : 2) hc_down_kernel(co
   const int row0 = rg * G::DN_ROWS;
   const int T = a.T;
 
+  const uint64_t t_entry = ptx::globaltimer_ns();
   cg::cluster_group cluster = cg::this_cluster();
   const unsigned rank = cluster.block_rank();  // = slab within the stream
   // The leader's receive area: [4][T] sums of squares, then [4][T][32] partials.
@@ -335,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, D == 2560 ? 3 : 2) hc_down_kernel(co
       }
     }
     // w_norm is waited for only now, with this group's R and P loads in flight.
-    if (t0 == 0) ok = wait_bar(bar_n, 0, a.err, kErrDownNorm) && ok;
+    if (t0 == 0) ok = wait_bar_from(bar_n, 0, a.err, kErrDownNorm, t_entry, first_wait_limit(a.wait_ns)) && ok;
     float ssl[TT];
 #pragma unroll
     for (int t = 0; t < TT; ++t) {

@@ -246,6 +246,7 @@ __global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_down_tc_k
   const int mt = warp & 1;    // m16 tile: rows 16 mt .. 16 mt + 15
   const int kp = warp >> 1;   // K-part: columns kp * KPART .. + KPART
 
+  const uint64_t t_entry = ptx::globaltimer_ns();
   cg::cluster_group cluster = cg::this_cluster();
   const unsigned rank = cluster.block_rank();
   float* recv_ss = cluster.map_shared_rank(reinterpret_cast<float*>(smem + S::RECV), 0);
@@ -359,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_down_tc_k
       if (lane == 0) ssw_s[warp * TG + t] = v;
     }
     if (t0 == 0) {
-      ok = wait_bar(bar_w, 0, a.err, kErrDownWeights) && ok;
+      ok = wait_bar_from(bar_w, 0, a.err, kErrDownWeights, t_entry, first_wait_limit(a.wait_ns)) && ok;
       if constexpr (Q8 != 0) ptx::cp_async_wait_all();
       if constexpr (Q8 == 2) q8_widen_rows<G::DN_ROWS, G::SLAB, 32>(w_s, S::WPITCH, S::Q8_OFF, warp, lane);
     }

@@ -115,6 +115,7 @@ __global__ void __launch_bounds__(UGeo<D, KD>::THREADS, 4) hc_down_u_kernel(cons
   float* rpr = reinterpret_cast<float*>(smem + U::DN_RP);
   float* rs_s = reinterpret_cast<float*>(smem + U::DN_RS);
 
+  const uint64_t t_entry = ptx::globaltimer_ns();
   const int chunk = blockIdx.x;
   const int stream = chunk / U::CPS;
   const int rg = blockIdx.y;
@@ -202,7 +203,7 @@ __global__ void __launch_bounds__(UGeo<D, KD>::THREADS, 4) hc_down_u_kernel(cons
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     if (lane == 0) ssw[warp * U::TMAX + t] = v;
   }
-  const bool ok = wait_bar(bar_w, 0, a.err, kErrDownWeights);
+  const bool ok = wait_bar_from(bar_w, 0, a.err, kErrDownWeights, t_entry, first_wait_limit(a.wait_ns));
   ptx::fence_proxy_async_smem();  // this thread's x stores, visible to the tensor cores
   ptx::tc_fence_before();
   __syncthreads();

@@ -118,6 +118,19 @@ __device__ __forceinline__ void cluster_wait_any() {
   asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
 }
 
+// This CTA's rank in its cluster and the number of CTAs in the cluster (1
+// when the launch has no clusters).
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+
 // ldmatrix: four (or two) 8x8 b16 matrices from shared memory; lane i
 // supplies the row address of matrix i/8.
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,

@@ -26,15 +26,20 @@
 // streams 2.60 / 2.52 / 2.51 us; at T = 8 6.9 -> 3.88 / 3.79 / 3.82 us.
 constexpr int kBatchLanes = 6;
 
-// The tensor maps of the W_down matrices a handle has seen (boxes of 64
-// columns x 64 rows, for the tensor-memory down kernel), by address: a map
-// holds only the address, sizes and strides, so an entry stays valid for
-// the handle's geometry whatever the memory holds.
+// Reads of at least this many tokens (d = 2560) take the wide tensor-memory
+// pair (hc_kernels_wide.cuh).
+constexpr int kWideMinT = 9;
+
+// The tensor maps of the weight matrices a handle has seen, by address:
+// W_down in boxes of 64 columns x 64 rows (the tensor-memory down kernels),
+// W_up in boxes of 64 columns x 16 rows (the wide up kernel).  A map holds
+// only the address, sizes and strides, so an entry stays valid for the
+// handle's geometry whatever the memory holds.
 struct MapCache {
   static constexpr int kSlots = 64;
-  const void* down[kSlots];
-  CUtensorMap maps[kSlots];
-  unsigned next;
+  const void* base[2][kSlots];  // [0] W_down, [1] W_up
+  CUtensorMap maps[2][kSlots];
+  unsigned next[2];
 };
 
 struct hc_read_s {
@@ -64,6 +69,8 @@ struct hc_read_s {
     int parity;
   } lanes[kBatchLanes];
   MapCache* map_cache;  // created on first use
+  unsigned long long wait_ns;  // limit of the down kernels' first bulk-copy wait (0: the default)
+  bool overlap;       // reads may overlap their predecessor (independent mode), hc_read_set_overlap
   int nlanes;         // lanes created (0: batches run on the caller's stream only)
   int batch_lanes;    // most lanes a batch may use (hc_read_set_batch_lanes)
   cudaEvent_t fork;
@@ -264,10 +271,10 @@ cudaError_t launch_pair_u(const DownArgs& da, const UpArgs& ua, const CUtensorMa
 // stay faster from T = 5 (8.5 against 9.0 us).
 template <int D, int KD>
 cudaError_t launch_geometry(int T, const DownArgs& da, const UpArgs& ua, cudaStream_t st,
-                            const CUtensorMap* w_down) {
+                            const CUtensorMap* w_down, const CUtensorMap* w_up = nullptr) {
   if (T == 1) return launch_pair<D, KD, 1>(da, ua, st);
   if constexpr (D == 2560) {
-    if (w_down != nullptr) return launch_pair_u<D, KD>(da, ua, *w_down, st);
+    if (w_down != nullptr && T <= hc::UGeo<D, KD>::TMAX) return launch_pair_u<D, KD>(da, ua, *w_down, st);
   }
   constexpr int kOneGroupMaxT = D == 2560 ? 8 : 4;
   return T <= kOneGroupMaxT ? launch_pair_tc<D, KD, 1>(da, ua, st) : launch_pair_tc<D, KD, 2>(da, ua, st);
@@ -492,6 +499,8 @@ HC_EXPORT int hc_read_create(hc_read_t* out, int n, int d, int K, int T_max, flo
     h->T_max = T_max;
     h->device = device;
     h->eps = eps;
+    h->wait_ns = 0;
+    h->overlap = true;
     const size_t part_b = round_up((size_t)n * T_max * K * sizeof(float), 256);
     const size_t err_b = 256;
     h->window = d == 2560 && window_fits();
@@ -548,28 +557,45 @@ HC_EXPORT int hc_read_create(hc_read_t* out, int n, int d, int K, int T_max, flo
 
 namespace {
 
-// Whether a BF16 read takes the tensor-memory down kernel: d = 2560 and
-// 5 <= T <= 8.
+// Whether a BF16 read takes a tensor-memory down kernel: d = 2560 and
+// 5 <= T <= 8 (hc_down_u_kernel) or T >= kWideMinT (the wide pair, whose up
+// kernel also takes a W_up map).
 bool takes_umma(int d, int T) { return d == 2560 && T > 4 && T <= hc::UGeo<2560, 320>::TMAX; }
+bool takes_wide(int d, int T) { return d == 2560 && T >= kWideMinT; }
 
-// The W_down tensor map of a read that takes the tensor-memory down kernel,
-// from the handle's cache; null: the read takes the mma.sync kernels (also
-// when the driver offers no tensor-map encoder).
-const CUtensorMap* down_map_for(hc_read_t h, const ReadDesc& q, int T) {
-  if (q.is_q8() || !takes_umma(h->d, T)) return nullptr;
+// A weight map from the handle's cache (which = 0: W_down [K][N] in boxes of
+// 64 x 64; 1: W_up [N][K] in boxes of 64 x 16); null when the driver offers
+// no tensor-map encoder.
+const CUtensorMap* weight_map(hc_read_t h, int which, const void* base) {
   MapCache* c = h->map_cache;
   if (c == nullptr) {
     c = h->map_cache = new (std::nothrow) MapCache();
     if (c == nullptr) return nullptr;
   }
   for (int i = 0; i < MapCache::kSlots; ++i) {
-    if (c->down[i] == q.W_down) return &c->maps[i];
+    if (c->base[which][i] == base) return &c->maps[which][i];
   }
-  const int i = (int)(c->next++ % MapCache::kSlots);
-  c->down[i] = nullptr;
-  if (!encode_bf16_tiles(&c->maps[i], q.W_down, h->K, (uint64_t)h->n * h->d, 64)) return nullptr;
-  c->down[i] = q.W_down;
-  return &c->maps[i];
+  const int i = (int)(c->next[which]++ % MapCache::kSlots);
+  c->base[which][i] = nullptr;
+  const uint64_t N = (uint64_t)h->n * h->d;
+  const bool done = which == 0 ? encode_bf16_tiles(&c->maps[which][i], base, h->K, N, 64)
+                               : encode_bf16_tiles(&c->maps[which][i], base, N, h->K, 16);
+  if (!done) return nullptr;
+  c->base[which][i] = base;
+  return &c->maps[which][i];
+}
+
+// The W_down tensor map of a read that takes a tensor-memory down kernel;
+// null: the read takes the mma.sync kernels.
+const CUtensorMap* down_map_for(hc_read_t h, const ReadDesc& q, int T) {
+  if (q.is_q8() || !takes_umma(h->d, T)) return nullptr;
+  return weight_map(h, 0, q.W_down);
+}
+
+// The W_up tensor map of a read that takes the wide pair (else null).
+const CUtensorMap* up_map_for(hc_read_t h, const ReadDesc& q, int T) {
+  if (q.is_q8() || !takes_wide(h->d, T)) return nullptr;
+  return weight_map(h, 1, q.W_up);
 }
 
 // Enqueues one validated read on `st` with partial-sum slot `part` (the two
@@ -582,7 +608,7 @@ int enqueue_read(hc_read_t h, float* part, int device, const ReadDesc& q, int T,
   const Range outs[5] = {range_of(q.out, T * N * 4),  range_of(q.mean, (size_t)T * h->d * 4),
                          range_of(q.lo, (size_t)T * h->K * 4), range_of(r_out, T * N * 4),
                          range_of(rs, (size_t)T * h->n * 4)};
-  const int independent = record_and_check(device, st, ins, outs) ? 1 : 0;
+  const int independent = (record_and_check(device, st, ins, outs) && h->overlap) ? 1 : 0;
 
   DownArgs da{};
   da.R = q.R;
@@ -599,6 +625,7 @@ int enqueue_read(hc_read_t h, float* part, int device, const ReadDesc& q, int T,
   da.independent = independent;
   da.late_launch = on_lanes ? 1 : 0;
   da.eps = h->eps;
+  da.wait_ns = h->wait_ns;
 
   UpArgs ua{};
   ua.R = q.R;
@@ -621,7 +648,7 @@ int enqueue_read(hc_read_t h, float* part, int device, const ReadDesc& q, int T,
   if (q.is_q8()) {
     e = (h->d == 2560) ? launch_geometry_q8<2560, 320>(T, da, ua, st) : launch_geometry_q8<4096, 512>(T, da, ua, st);
   } else {
-    e = (h->d == 2560) ? launch_geometry<2560, 320>(T, da, ua, st, down_map_for(h, q, T))
+    e = (h->d == 2560) ? launch_geometry<2560, 320>(T, da, ua, st, down_map_for(h, q, T), up_map_for(h, q, T))
                        : launch_geometry<4096, 512>(T, da, ua, st, nullptr);
   }
   if (e != cudaSuccess) {
@@ -1020,6 +1047,19 @@ HC_EXPORT void hc_read_destroy(hc_read_t h) {
   delete h;
 }
 
+HC_EXPORT int hc_read_set_wait_limit(hc_read_t h, uint64_t ns) {
+  if (h == nullptr) return HC_ERR_ARG;
+  h->wait_ns = ns;
+  return HC_OK;
+}
+
+HC_EXPORT int hc_read_set_overlap(hc_read_t h, int enabled) {
+  if (h == nullptr || enabled < 0 || enabled > 1) return HC_ERR_ARG;
+  const int prev = h->overlap ? 1 : 0;
+  h->overlap = enabled != 0;
+  return prev;
+}
+
 HC_EXPORT int64_t hc_read_scratch_bytes(hc_read_t h) {
   return h == nullptr ? -1 : static_cast<int64_t>(h->scratch_bytes);
 }
@@ -1127,12 +1167,11 @@ HC_EXPORT int hc_read_noalloc(int n, int d, int K, float eps, const float* R, co
 
   char* b = static_cast<char*>(base);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // The error word collects the calls' bounded-wait failures until
+  // hc_read_noalloc_check reads and clears it (it starts at zero: the array
+  // is zero-initialised when the library is loaded).  The partial-sum slot
+  // needs no clearing: every call writes the part it reads.
   unsigned* err = reinterpret_cast<unsigned*>(b + kNoallocPartBytes);
-  // The error word must start at zero.
-  if (cudaMemsetAsync(err, 0, kNoallocTailBytes, st) != cudaSuccess) {
-    cudaGetLastError();
-    return HC_ERR_CUDA;
-  }
   // Keep this stream's record of the last read current, so that a later read
   // that consumes these outputs waits for them.  (This path has one scratch
   // slot and always waits for the previous kernel before it computes.)
@@ -1183,4 +1222,25 @@ HC_EXPORT int hc_read_noalloc(int n, int d, int K, float eps, const float* R, co
     return HC_ERR_CUDA;
   }
   return HC_OK;
+}
+
+HC_EXPORT int hc_read_noalloc_check(void) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return HC_ERR_CUDA;
+  void* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    base = g_noalloc_scratch_addr[dev];
+  }
+  if (base == nullptr) return HC_OK;  // no call has run on this device
+  unsigned* err = reinterpret_cast<unsigned*>(static_cast<char*>(base) + kNoallocPartBytes);
+  unsigned word = 0;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(&word, err, sizeof word, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && word != 0u) e = cudaMemset(err, 0, sizeof word);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return HC_ERR_CUDA;
+  }
+  return word == 0u ? HC_OK : HC_ERR_TIMEOUT;
 }

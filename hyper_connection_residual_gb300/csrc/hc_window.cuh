@@ -46,10 +46,25 @@
 // again.
 //
 // Every sum runs in a fixed order, so repeated launches and graph replays give
-// identical bits.  All waits are bounded (kWaitNs) and also give up once any
-// CTA has raised the launch's abort word; a CTA that gives up records an error
-// bit, stops issuing work and leaves with its cluster (leave_cluster).  The
-// 128 CTAs must be co-resident (the host launches cooperatively).
+// identical bits.  All waits are bounded.  Two kinds:
+//   * waits across clusters (the global exchange, the stream-mean tiles)
+//     depend on CTAs that the hardware does not co-schedule with this one;
+//     they give up after kWaitNs, or at once when any CTA has raised the
+//     launch's abort word, and from then on this CTA skips them (its results
+//     are void and the error word says so);
+//   * waits inside the CTA or its cluster (the weight ring, the cluster
+//     exchanges) depend only on this CTA's own copies and on its cluster
+//     peers, which run at the same time and never skip a send.  They ignore
+//     the abort word, so every byte a peer sends is waited for by its
+//     receiver, every transaction count returns to zero, and no CTA leaves
+//     while a copy or a peer's store into it is in flight.  Their limit
+//     (kLocalWaitNs) is longer than the global one: a peer stuck in a global
+//     wait gives up first.
+// The kernel checks its launch shape (grid, block and 4-CTA clusters) before
+// it touches a peer, and records kErrWinLaunch instead of running when the
+// shape is wrong.  The 128 CTAs must be co-resident (the host launches
+// cooperatively); if they are not, the global waits give up and the launch
+// reports HC_ERR_TIMEOUT.
 //
 // Design ancestors: the down and up kernels of "#2812 sycl: STRATA_GR_FUSED=1,
 // the two-kernel BF16 hyper-connection read (opt-in)", section "What changed"
@@ -74,6 +89,10 @@ constexpr unsigned kErrWinFull = 16u;      // weight tiles did not land
 constexpr unsigned kErrWinEmpty = 32u;     // producer: ring entry never released
 constexpr unsigned kErrWinCluster = 64u;   // cluster exchange did not complete
 constexpr unsigned kErrWinGlobal = 128u;   // global exchange did not complete
+constexpr unsigned kErrWinLaunch = 256u;   // launched with a grid, block or cluster shape it was not built for
+// Waits inside a CTA or its cluster give up only after this long (longer than
+// kWaitNs, the limit of the waits across clusters that they may wait behind).
+constexpr uint64_t kLocalWaitNs = 4 * kWaitNs;
 
 struct WinRead {
   const float* R;          // [T][N]
@@ -268,57 +287,34 @@ __device__ __forceinline__ void raise_abort(unsigned* f, unsigned* err, unsigned
 }
 
 // Exit of a CTA of a CL-CTA cluster whose CTAs store into one another's
-// shared memory (st.async), called by every thread after the CTA's last
-// store was issued.  Normally every byte sent was waited for by its
-// receiver, so nothing is in flight.  After an abort, receivers stop waiting:
-// stores a peer issued earlier may still be on their way, and no CTA may
-// leave before they land.  The CTAs first meet (nobody sends any more), then
-// each posts its reading of the abort word to every peer; all see the same
-// CL readings, so all take the same decision: if any saw the abort, all wait
-// 50 us and meet once more before leaving.
-template <int CL>
-__device__ __forceinline__ void leave_cluster(const unsigned* abort_flag, uint32_t rank, int tid) {
-  __shared__ unsigned votes[CL];
+// shared memory (st.async), called by every thread, converged, after the
+// CTA's last store was issued.  Every byte a peer sent was waited for by its
+// receiver (local waits never skip), so nothing is in flight any more; the
+// cluster barrier keeps every CTA resident until all have passed their last
+// wait on a peer's stores.
+__device__ __forceinline__ void leave_cluster() {
   ptx::cluster_arrive_release();
   ptx::cluster_wait();
-  if (tid == 0) {
-    const unsigned mine = load_abort(abort_flag);
-    const uint32_t at = ptx::smem_u32(&votes[rank]);
-    for (uint32_t peer = 0; peer < (uint32_t)CL; ++peer) {
-      asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(mapa(at, peer)), "r"(mine) : "memory");
-    }
-  }
-  __syncwarp();
-  ptx::cluster_arrive_release();
-  ptx::cluster_wait();
-  unsigned any = 0u;
-#pragma unroll
-  for (int r = 0; r < CL; ++r) any |= votes[r];
-  if (any != 0u) {
-    if (tid == 0) {
-      const uint64_t t0 = ptx::globaltimer_ns();
-      while (ptx::globaltimer_ns() - t0 < 50000u) {
-      }
-    }
-    __syncwarp();
-    __syncthreads();
-    ptx::cluster_arrive_release();
-    ptx::cluster_wait();
-  }
 }
 
-// Bounded mbarrier wait; gives up after kWaitNs or once the launch is aborted.
+// Bounded wait on a phase of an mbarrier of this CTA that only this CTA's
+// copies or its cluster peers complete (see the header: such waits ignore the
+// abort word).  After kLocalWaitNs the thread records `code`, raises the
+// abort word and marks the CTA broken (*broken, shared memory), which makes
+// every later local wait of the CTA return at once: the protocol cannot be
+// kept any more, and the kernel only runs to its end.
 template <bool kCluster>
-__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, unsigned* abort_flag,
-                                           unsigned* err, unsigned code) {
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile unsigned* broken,
+                                           unsigned* abort_flag, unsigned* err, unsigned code) {
   auto probe = [&]() { return kCluster ? mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity); };
   if (probe()) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   for (unsigned n = 1;; ++n) {
     if (probe()) return true;
     if ((n & 31u) == 0u) {
-      if (load_abort(abort_flag) != 0u) return false;
-      if (ptx::globaltimer_ns() - t0 > kWaitNs) {
+      if (*broken != 0u) return false;
+      if (ptx::globaltimer_ns() - t0 > kLocalWaitNs) {
+        *broken = 1u;
         raise_abort(abort_flag, err, code);
         return false;
       }
@@ -441,8 +437,18 @@ __global__ void __launch_bounds__(WinGeo<D, KD, NT>::THREADS, 1)
   const uint32_t rank = b % G::CL;      // rank in the cluster (1-D clusters along x)
   const int col0 = s * D + j * G::W;    // first column of W_down / row of W_up
   const int T = a.T;
+  __shared__ unsigned broken;  // a local wait of this CTA ran out (see wait_phase)
+
+  // The launch shape the CTA numbering above assumes: every CTA of a launch
+  // sees the same shape, so either all return here or none does.
+  if (ptx::cluster_nctarank() != (uint32_t)G::CL || ptx::cluster_ctarank() != rank ||
+      gridDim.x != (unsigned)kWinCtas || gridDim.y != 1u || gridDim.z != 1u || blockDim.x != (unsigned)G::THREADS) {
+    if (tid == 0) atomicOr(a.err, kErrWinLaunch);
+    return;
+  }
 
   if (tid == 0) {
+    broken = 0u;
     for (int e = 0; e < 2; ++e) {
       ptx::mbar_init(&full_d[e], G::PT);
       ptx::mbar_init(&full_u[e], G::PT);
@@ -473,7 +479,7 @@ __global__ void __launch_bounds__(WinGeo<D, KD, NT>::THREADS, 1)
       const WinRead& rd = a.rd[i];
       unsigned char* ent = smem + G::ENT + e * G::ENT_BYTES;
       // Entry e was last used by read i - 2.
-      if (i >= 2 && !win::wait_phase<false>(&empty_d[e], ((i >> 1) + 1) & 1, a.abort_flag, a.err, kErrWinEmpty)) break;
+      if (i >= 2 && !win::wait_phase<false>(&empty_d[e], ((i >> 1) + 1) & 1, &broken, a.abort_flag, a.err, kErrWinEmpty)) break;
       for (int idx = pt; idx < KD * G::WD_CH; idx += G::PT) {
         const int r = idx / G::WD_CH, c = idx - r * G::WD_CH;
         win::cp_async16(ent + G::E_WD + win::wd_off(r, c, G::WD_ROWB), rd.W_down + (size_t)r * G::N + col0 + c * 8,
@@ -497,7 +503,7 @@ __global__ void __launch_bounds__(WinGeo<D, KD, NT>::THREADS, 1)
         }
       }
       win::cp_async_arrive(&full_d[e]);
-      if (i >= 2 && !win::wait_phase<false>(&empty_u[e], ((i >> 1) + 1) & 1, a.abort_flag, a.err, kErrWinEmpty)) break;
+      if (i >= 2 && !win::wait_phase<false>(&empty_u[e], ((i >> 1) + 1) & 1, &broken, a.abort_flag, a.err, kErrWinEmpty)) break;
       for (int idx = pt; idx < G::W * G::WU_CH; idx += G::PT) {
         const int r = idx / G::WU_CH, c = idx - r * G::WU_CH;
         win::cp_async16(ent + G::E_WU + win::wu_off(r, c, G::WU_ROWB), rd.W_up + (size_t)(col0 + r) * KD + c * 8,
@@ -536,7 +542,7 @@ __global__ void __launch_bounds__(WinGeo<D, KD, NT>::THREADS, 1)
       unsigned char* ent = smem + G::ENT + e * G::ENT_BYTES;
 
       // (1) down part of the entry: W_down tile, w_norm, R, P.
-      ok = win::wait_phase<false>(&full_d[e], ph, a.abort_flag, a.err, kErrWinFull) && ok;
+      ok = win::wait_phase<false>(&full_d[e], ph, &broken, a.abort_flag, a.err, kErrWinFull) && ok;
       // (2) staging, one warp per token: R' = R + P (or the previous read's
       // out + P), x = R' * w_norm split into hi/lo B rows, sums of squares.
       if (warp < T) {
@@ -575,6 +581,9 @@ __global__ void __launch_bounds__(WinGeo<D, KD, NT>::THREADS, 1)
       win::compute_sync<G::CT>();  // x rows complete
 
       // (3) down projection: warp w owns W_down rows 16 * (DN_MPW w + m) ...
+      // The warp's lanes left the waits above one by one and the named
+      // barrier does not reconverge them: ldmatrix and mma are .aligned.
+      __syncwarp();
       {
         float acc[G::DN_MPW][NT][4];
 #pragma unroll
@@ -625,7 +634,7 @@ __global__ void __launch_bounds__(WinGeo<D, KD, NT>::THREADS, 1)
       {
         // Arm the next read only once this phase has completed: arming an
         // incomplete phase would take its arrival count below zero.
-        const bool got = win::wait_phase<true>(bar_rs, xp, a.abort_flag, a.err, kErrWinCluster);
+        const bool got = win::wait_phase<true>(bar_rs, xp, &broken, a.abort_flag, a.err, kErrWinCluster);
         ok = got && ok;
         if (tid == 0 && got) ptx::mbar_arrive_expect_tx(bar_rs, G::rs_bytes(T));
       }
@@ -762,9 +771,9 @@ __global__ void __launch_bounds__(WinGeo<D, KD, NT>::THREADS, 1)
       }
 
       // (7) up part of the entry.
-      ok = win::wait_phase<false>(&full_u[e], ph, a.abort_flag, a.err, kErrWinFull) && ok;
+      ok = win::wait_phase<false>(&full_u[e], ph, &broken, a.abort_flag, a.err, kErrWinFull) && ok;
       {
-        const bool got = win::wait_phase<true>(bar_lo, xp, a.abort_flag, a.err, kErrWinCluster);
+        const bool got = win::wait_phase<true>(bar_lo, xp, &broken, a.abort_flag, a.err, kErrWinCluster);
         ok = got && ok;
         if (tid == 0 && got) ptx::mbar_arrive_expect_tx(bar_lo, G::lo_bytes(T));  // arm the next read
       }
@@ -846,7 +855,7 @@ __global__ void __launch_bounds__(WinGeo<D, KD, NT>::THREADS, 1)
   }
   __syncwarp();
   __syncthreads();
-  win::leave_cluster<G::CL>(a.abort_flag, rank, tid);
+  win::leave_cluster();
 }
 
 }  // namespace hc

@@ -51,7 +51,8 @@
  * read's.  The inputs of a read must therefore not be written by a kernel
  * that immediately precedes it on the stream and itself triggers its
  * dependents early (kernels that do not use programmatic completion, copies
- * and memsets are always waited for in full).
+ * and memsets are always waited for in full); callers whose own kernels do
+ * that switch the overlap off per handle with hc_read_set_overlap.
  *
  * Errors: every entry point returns an hc_status (0 = HC_OK).  Argument errors
  * are detected on the host before anything is enqueued.  HC_ERR_CUDA reports
@@ -256,6 +257,30 @@ void hc_read_destroy(hc_read_t h);
 /* Bytes of device scratch a handle holds (for accounting). */
 int64_t hc_read_scratch_bytes(hc_read_t h);
 
+/* Limit, in nanoseconds counted from the kernel's start, of the first
+ * bulk-copy wait of the down kernel of every later read enqueued through this
+ * handle (hc_read, hc_read_ex, hc_read_q8 and the reads of batches that run
+ * on the internal streams).  0 restores the default, which is also the
+ * largest value taken: 1 s.  A read whose down kernel reaches that wait after
+ * the limit gives up on it whether or not the copy has landed: its results
+ * are void, the copy is still drained before the kernel exits, and
+ * hc_read_check reports HC_ERR_TIMEOUT (bit 1 or 2 of hc_read_error_word)
+ * until hc_read_reset.  This is how the timeout path is exercised on purpose
+ * (a limit of a few nanoseconds); no other wait takes the setting.  Not
+ * thread-safe against a concurrent read on the same handle.  HC_ERR_ARG for
+ * a NULL handle. */
+int hc_read_set_wait_limit(hc_read_t h, uint64_t ns);
+
+/* Whether reads on this handle may overlap the read enqueued before them on
+ * the same stream (1, the default) or always wait for it in full (0).  With
+ * 1, a read that takes nothing the previous read wrote reads R and pending
+ * and computes before its dependency wait (see "Asynchrony" above); callers
+ * whose own kernels trigger their dependents early and write a read's inputs
+ * just before it should pass 0.  Returns the previous setting, or HC_ERR_ARG
+ * for a NULL handle or a value other than 0 or 1.  Not thread-safe against a
+ * concurrent read on the same handle. */
+int hc_read_set_overlap(hc_read_t h, int enabled);
+
 /* hc_read without a handle and without any device allocation.
  *
  * The pages have no counterpart of this entry point; it exists for callers
@@ -277,14 +302,26 @@ int64_t hc_read_scratch_bytes(hc_read_t h);
  * array's device address and sets kernel attributes); make that first call
  * before any stream capture.  Every call on a device shares the one scratch
  * array: calls that overlap on the GPU (two streams, or two threads) race and
- * give wrong results, so serialise them.  Each call clears the parts of the
- * scratch that must start at zero on `stream` before its kernels run. */
+ * give wrong results, so serialise them.  The array keeps what the last call
+ * left there: the partial sums need no clearing (each call writes all it
+ * reads), and the error word, which starts at zero when the library is
+ * loaded, collects the calls' bounded-wait failures until
+ * hc_read_noalloc_check reads and clears it.  No call runs every read in
+ * independent mode: each waits for the kernel before it in full. */
 #define HC_NOALLOC_MAX_T 8
 #define HC_NOALLOC_SCRATCH_BYTES (4 * HC_NOALLOC_MAX_T * 512 * 4 + 256)
 int hc_read_noalloc(int n, int d, int K, float eps, const float* R, const float* w_norm,
                     const uint16_t* W_down, const uint16_t* W_up, const float* gate,
                     const float* pending, int T, float* out, float* mean, float* lo,
                     hc_stream_t stream);
+
+/* The no-allocation entry point's counterpart of hc_read_check, for the
+ * current device: synchronises the device, then returns HC_ERR_TIMEOUT if a
+ * kernel of an hc_read_noalloc call gave up on a bounded wait since the last
+ * hc_read_noalloc_check (and clears that record), HC_OK if none did or no
+ * call has run on the device, HC_ERR_CUDA on a runtime error.  Allocates
+ * nothing. */
+int hc_read_noalloc_check(void);
 
 /* Static text for a status code. */
 const char* hc_status_str(int status);

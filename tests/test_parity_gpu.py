@@ -345,3 +345,33 @@ def test_mixed_dependent_and_independent_sequence(dev, orc, rd1):
         if k == 0:
             continue  # its output buffer was rewritten by read 3
         assert_parity(o, ref, T, f"read {k} (T={T})")
+
+
+@pytest.mark.parametrize("T", [1, 4, 8])
+def test_overlap_switched_off_gives_the_same_bits(dev, orc, T):
+    """hc_read_set_overlap(0): every read waits for its predecessor in full
+    instead of computing before the wait; the results are the same bits as
+    with the overlap on (the kernels and their summation order do not change),
+    and match the oracle."""
+    g = synth.G1
+    n_reads = 3
+    sets = [synth.weight_set(g, 80 + i) for i in range(n_reads)]
+    w = [dev_weights(ws, dev) for ws in sets]
+    act = synth.activations(g, T, True, s0=81)
+    a = dev_act(act, dev)
+    got = {}
+    for overlap in (True, False):
+        with hc.Read(g.n, g.d, g.K, T_max=8, eps=EPS) as rd:
+            assert rd.set_overlap(overlap) is True  # the default is on
+            outs = [outputs(g, T, dev) for _ in range(n_reads)]
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                for i in range(n_reads):
+                    run(rd, w[i], a, T, outs[i], stream=s)
+            s.synchronize()
+            assert rd.check() == hc.HC_OK
+            got[overlap] = outs
+    for i in range(n_reads):
+        for name in ("out", "mean", "lo", "r_out", "rs"):
+            assert np.array_equal(bits(got[True][i][name]), bits(got[False][i][name])), f"read {i} {name}"
+        assert_parity(got[False][i], oracle_read(orc, g, sets[i], act), T, f"read {i}")

@@ -65,6 +65,49 @@ def test_noalloc_matches_handle_read_twice():
                 _close(x, y, f"T={T} {name}")
 
 
+NOALLOC_CASES = [(synth.G1, 1), (synth.G1, 4), (synth.G1, 8), (synth.G2, 1), (synth.G2, 5), (synth.G2, 8)]
+
+
+@pytest.mark.parametrize("g,T", NOALLOC_CASES, ids=[f"d{g.d}_T{T}" for g, T in NOALLOC_CASES])
+def test_noalloc_matches_oracle_twice(g, T):
+    """Two calls in a row (the second over other inputs, pending write on),
+    each against the FP64 oracle at the parity bar: the CUDA-core kernels at
+    T = 1, the tensor-core ones above, and d = 4096, K = 512, whose partial
+    sums fill the whole fixed array at T = 8.  The first call goes through the
+    Python wrapper, the second through the C ABI.  hc_read_noalloc_check then
+    reports that no bounded wait ran out."""
+    import oracle
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    lib = hc.load()
+    for call, (j, pending) in enumerate(((5, False), (6, True))):
+        ws = synth.weight_set(g, j)
+        act = synth.activations(g, T, pending, s0=60 + 7 * j + T)
+        w = dev_weights(ws, dev)
+        a = dev_act(act, dev)
+        got = _outs(g, T, dev)
+        if call == 0:
+            hc.hc_read_noalloc((g.n, g.d, g.K), EPS, a["R"], w["w_norm"], w["W_down"], w["W_up"], w["gate"],
+                               a["P"], T, *got)
+        else:
+            p = [a["R"].data_ptr(), w["w_norm"].data_ptr(), w["W_down"].data_ptr(), w["W_up"].data_ptr(),
+                 w["gate"].data_ptr(), a["P"].data_ptr() if a["P"] is not None else None]
+            status = lib.hc_read_noalloc(g.n, g.d, g.K, ctypes.c_float(EPS), *p, T,
+                                         *[t.data_ptr() for t in got],
+                                         torch.cuda.current_stream().cuda_stream or None)
+            assert status == hc.HC_OK, hc.status_str(status)
+        torch.cuda.synchronize()
+        ref = oracle.default().read(g.n, g.d, g.K, R=act.R, P=act.P, w_norm=ws.w_norm, W_down=ws.W_down,
+                                    W_up=ws.W_up, gate=ws.gate, eps=EPS)
+        for name, x, want in zip(("out", "mean", "lo"), got, (ref.out, ref.mean, ref.lo)):
+            err = float(np.max(np.abs(x.double().cpu().numpy() - want)))
+            bound = TOL * float(np.max(np.abs(want)))
+            assert err <= bound, f"d={g.d} T={T} call {call} {name}: max err {err:.3e} > {bound:.3e}"
+    assert hc.hc_read_noalloc_check() == hc.HC_OK
+
+
 def test_noalloc_rejects_t_above_its_maximum():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
