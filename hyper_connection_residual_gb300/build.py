@@ -19,7 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libhcread.so")
 SOURCES = [os.path.join(CSRC, "hc_read.cu"), os.path.join(CSRC, "hc_q2.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, f) for f in (
-    "hc_kernels.cuh", "hc_kernels_tc.cuh", "hc_kernels_umma.cuh", "hc_window.cuh", "hc_ptx.cuh")] + [
+    "hc_kernels.cuh", "hc_kernels_tc.cuh", "hc_kernels_umma.cuh", "hc_kernels_wide.cuh", "hc_window.cuh",
+    "hc_ptx.cuh")] + [
     os.path.join(INCLUDE, "hc_read.h"), os.path.join(INCLUDE, "hc_q2.h")]
 
 NVCC_FLAGS = [

@@ -84,6 +84,21 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+// Shared -> shared bulk copy on the TMA engine from this CTA into the
+// shared memory of cluster CTA `rank` (dst and bar given as this CTA's
+// shared addresses of the same variables there); completion is reported to
+// the peer's barrier as `bytes` transactions.  Both addresses 16-byte
+// aligned, bytes % 16 == 0.
+__device__ __forceinline__ void bulk_s2peer(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar, uint32_t rank) {
+  uint32_t rdst, rbar;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rdst) : "r"(dst), "r"(rank));
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rbar) : "r"(bar), "r"(rank));
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   rdst),
+               "r"(src), "r"(bytes), "r"(rbar)
+               : "memory");
+}
+
 // Programmatic dependent launch: let the next kernel in the stream start.
 __device__ __forceinline__ void launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

@@ -16,6 +16,7 @@
 #include "hc_kernels.cuh"
 #include "hc_kernels_tc.cuh"
 #include "hc_kernels_umma.cuh"
+#include "hc_kernels_wide.cuh"
 #include "hc_read.h"
 #include "hc_window.cuh"
 
@@ -165,10 +166,28 @@ cudaError_t configure_umma() {
 }
 
 template <int D, int KD>
+cudaError_t configure_wide() {
+  using W = hc::WGeo<D, KD>;
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(hc::hc_down_w_kernel<D, KD, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                W::dn_bytes(W::TP))) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(hc::hc_up_w_kernel<D, KD, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                W::up_bytes(W::TP))) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(hc::hc_down_w_kernel<D, KD, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                W::DN_BYTES_MAX)) != cudaSuccess)
+    return e;
+  return cudaFuncSetAttribute(hc::hc_up_w_kernel<D, KD, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              W::up_bytes(W::TW));
+}
+
+template <int D, int KD>
 cudaError_t configure_geometry() {
   cudaError_t e;
   if constexpr (D == 2560) {
     if ((e = configure_umma<D, KD>()) != cudaSuccess) return e;
+    if ((e = configure_wide<D, KD>()) != cudaSuccess) return e;
   }
   if ((e = configure_one<D, KD, 1>()) != cudaSuccess) return e;
   if ((e = configure_tc<D, KD, 1, 0>()) != cudaSuccess) return e;
@@ -261,6 +280,33 @@ cudaError_t launch_pair_u(const DownArgs& da, const UpArgs& ua, const CUtensorMa
   return cudaLaunchKernelEx(&c2, hc::hc_up_tc_kernel<D, KD, 1>, ua);
 }
 
+// The wide tensor-memory pair (d = 2560, K = 320, T >= kWideMinT): both
+// projections on tcgen05 with every weight byte read once for all T tokens,
+// tokens in passes of 16, the up kernel's lo combined once per cluster;
+// shared memory sized by T, three CTAs per SM.
+template <int D, int KD>
+cudaError_t launch_pair_w(const DownArgs& da, const UpArgs& ua, const CUtensorMap& w_down, const CUtensorMap& w_up,
+                          cudaStream_t st) {
+  using W = hc::WGeo<D, KD>;
+  hc::DownUArgs dargs;
+  dargs.w = w_down;
+  dargs.a = da;
+  cudaLaunchAttribute attr[2];
+  // T <= 16: the single-pass instantiations.
+  const bool multi = da.T > W::TP;
+  cudaLaunchConfig_t c1 = pdl_config(dim3(W::CHUNKS, W::ROW_GROUPS), W::dn_bytes(da.T), st, attr, W::CPS, W::THREADS);
+  cudaError_t e = multi ? cudaLaunchKernelEx(&c1, hc::hc_down_w_kernel<D, KD, true>, dargs)
+                        : cudaLaunchKernelEx(&c1, hc::hc_down_w_kernel<D, KD, false>, dargs);
+  if (e != cudaSuccess) return e;
+  hc::UpWArgs uargs;
+  uargs.w = w_up;
+  uargs.a = ua;
+  cudaLaunchAttribute attr2[2];
+  cudaLaunchConfig_t c2 = pdl_config(dim3(W::UP_CTAS), W::up_bytes(ua.T), st, attr2, W::UCL, W::THREADS);
+  return multi ? cudaLaunchKernelEx(&c2, hc::hc_up_w_kernel<D, KD, true>, uargs)
+               : cudaLaunchKernelEx(&c2, hc::hc_up_w_kernel<D, KD, false>, uargs);
+}
+
 // From T = 2 on the tensor-core kernels are faster on GB300 (measured: T=2
 // 6.1 vs 6.7 us, T=8 7.9 vs 11.1 us per read); at T = 1 the CUDA-core kernels
 // are (5.2 vs 6.0 us): the MMA path stages four tokens there.  At d = 2560,
@@ -274,6 +320,7 @@ cudaError_t launch_geometry(int T, const DownArgs& da, const UpArgs& ua, cudaStr
                             const CUtensorMap* w_down, const CUtensorMap* w_up = nullptr) {
   if (T == 1) return launch_pair<D, KD, 1>(da, ua, st);
   if constexpr (D == 2560) {
+    if (w_down != nullptr && w_up != nullptr && T >= kWideMinT) return launch_pair_w<D, KD>(da, ua, *w_down, *w_up, st);
     if (w_down != nullptr && T <= hc::UGeo<D, KD>::TMAX) return launch_pair_u<D, KD>(da, ua, *w_down, st);
   }
   constexpr int kOneGroupMaxT = D == 2560 ? 8 : 4;
@@ -560,7 +607,7 @@ namespace {
 // Whether a BF16 read takes a tensor-memory down kernel: d = 2560 and
 // 5 <= T <= 8 (hc_down_u_kernel) or T >= kWideMinT (the wide pair, whose up
 // kernel also takes a W_up map).
-bool takes_umma(int d, int T) { return d == 2560 && T > 4 && T <= hc::UGeo<2560, 320>::TMAX; }
+bool takes_umma(int d, int T) { return d == 2560 && T > 4 && (T <= hc::UGeo<2560, 320>::TMAX || T >= kWideMinT); }
 bool takes_wide(int d, int T) { return d == 2560 && T >= kWideMinT; }
 
 // A weight map from the handle's cache (which = 0: W_down [K][N] in boxes of
