@@ -277,9 +277,12 @@ def run_reference(args):
 class Sweep:
     """Device-resident inputs and one captured graph per case.
 
-    batch=True: the case's reads are one hc_read_batch, every read with its
-    own out, mean and lo.  batch=False: one hc_read call per read on the
-    stream, all into one set of output buffers."""
+    Every read has its own R and P (distinct buffers: a read's activations are
+    never another read's, as in a verify window) and, with batch=True, its own
+    out, mean and lo; per T they are one contiguous block of `calls` reads
+    ([calls][T][...]), which the end-to-end leg copies in and out whole.
+    batch=True: the case's reads are one hc_read_batch.  batch=False: one
+    hc_read call per read on the stream, all into one set of output buffers."""
 
     def __init__(self, hc, torch, dev, g: synth.Geometry, Ts, pendings, sets: int, calls: int,
                  stream, batch: bool = True, q8: bool = False):
@@ -300,11 +303,18 @@ class Sweep:
                 w_norm=torch.from_numpy(w.w_norm).to(dev), gate=torch.from_numpy(w.gate).to(dev),
                 W_down=torch.from_numpy(w.W_down.view(np.int16)).to(dev),
                 W_up=torch.from_numpy(w.W_up.view(np.int16)).to(dev)))
-        act = synth.activations(g, Tmax, True)
-        self.R = torch.from_numpy(act.R).to(dev)
-        self.P = torch.from_numpy(act.P).to(dev)
-        self.outs = [dict(out=torch.empty(Tmax, g.N, device=dev), mean=torch.empty(Tmax, g.d, device=dev),
-                          lo=torch.empty(Tmax, g.K, device=dev)) for _ in range(calls if batch else 1)]
+        # One activation draw per T, copied into every read's own buffers.
+        self.act = {}
+        nout = calls if batch else 1
+        for T in sorted(set(Ts)):
+            a = synth.activations(g, T, True)
+            R1 = torch.from_numpy(a.R).to(dev)
+            blk = dict(R=R1.unsqueeze(0).repeat(calls, 1, 1).contiguous(),
+                       out=torch.empty(nout, T, g.N, device=dev), mean=torch.empty(nout, T, g.d, device=dev),
+                       lo=torch.empty(nout, T, g.K, device=dev))
+            if True in pendings:
+                blk["P"] = torch.from_numpy(a.P).to(dev).unsqueeze(0).repeat(calls, 1, 1).contiguous()
+            self.act[T] = blk
         self.rd = hc.Read(g.n, g.d, g.K, T_max=max(8, Tmax), eps=EPS)
         self.cases = [(T, p) for T in Ts for p in pendings]
         self.graphs = {}
@@ -312,9 +322,10 @@ class Sweep:
             self.graphs[case] = self._capture(*case)
 
     def _desc(self, T, pending, j):
-        o = self.outs[j if self.batch else 0]
-        return dict(R=self.R, P=self.P if pending else None, out=o["out"][:T], mean=o["mean"][:T],
-                    lo=o["lo"][:T], **self.ws[j % len(self.ws)])
+        a = self.act[T]
+        o = j if self.batch else 0
+        return dict(R=a["R"][j], P=a["P"][j] if pending else None, out=a["out"][o], mean=a["mean"][o],
+                    lo=a["lo"][o], **self.ws[j % len(self.ws)])
 
     def _capture(self, T, pending):
         hc = self.hc
@@ -338,9 +349,9 @@ class Sweep:
         descs = [self._desc(T, pending, j) for j in range(self.calls)]
         return (self.rd.batch_q8_plan if self.q8 else self.rd.batch_plan)(descs, T)
 
-    def result(self):
-        """The output buffers of the last read of a case."""
-        return self.outs[-1]
+    def block(self, T):
+        """The case's device buffers: R, P, out, mean, lo, each [calls][T][...]."""
+        return self.act[T]
 
     def replay(self, case):
         self.hc.hc_graph_launch(self.graphs[case], self.stream)
@@ -459,6 +470,38 @@ def run_profile_case():
             for w in ws:
                 flush.zero_()
                 rd(R, w["w_norm"], w["W_down"], w["W_up"], w["gate"], P, T, out, mean, lo)
+        torch.cuda.synchronize()
+        assert rd.check() == hc.HC_OK
+    print("profile case done")
+    return 0
+
+
+def run_profile_wide_case():
+    """Cold reads on the wide tensor-memory pair, each after a 256 MB write that
+    flushes L2: three at T=16 (one pass), three at T=64 (four passes), pending
+    off; a small case for ncu captures."""
+    import torch
+    import hyper_connection_residual_gb300 as hc
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    g = synth.G1
+    ws = []
+    for j in range(3):
+        w = synth.weight_set(g, j)
+        ws.append(dict(w_norm=torch.from_numpy(w.w_norm).to(dev), gate=torch.from_numpy(w.gate).to(dev),
+                       W_down=torch.from_numpy(w.W_down.view(np.int16)).to(dev),
+                       W_up=torch.from_numpy(w.W_up.view(np.int16)).to(dev)))
+    act = synth.activations(g, 64, False)
+    R = torch.from_numpy(act.R).to(dev)
+    out = torch.empty(64, g.N, device=dev)
+    mean = torch.empty(64, g.d, device=dev)
+    lo = torch.empty(64, g.K, device=dev)
+    flush = torch.empty(64 * 1024 * 1024, device=dev)
+    with hc.Read(g.n, g.d, g.K, T_max=64, eps=EPS) as rd:
+        for T in (16, 64):
+            for w in ws:
+                flush.zero_()
+                rd(R, w["w_norm"], w["W_down"], w["W_up"], w["gate"], None, T, out, mean, lo)
         torch.cuda.synchronize()
         assert rd.check() == hc.HC_OK
     print("profile case done")
@@ -623,13 +666,16 @@ def run_gpu(args):
                     read_bytes(g, T, p) * args.steps * calls / per_case[(T, p)] / 1e9
                     for (T, p) in sweep.cases}
 
-    # ---- end to end: pinned host inputs in, results out, every step
-    pin_R = torch.from_numpy(synth.activations(g, max(SWEEP_T), True).R).pin_memory()
-    pin_P = torch.from_numpy(synth.activations(g, max(SWEEP_T), True).P).pin_memory()
-    host_out = torch.empty(max(SWEEP_T), g.N).pin_memory()
-    host_mean = torch.empty(max(SWEEP_T), g.d).pin_memory()
-    h2d = sum(T * g.N * 4 * (2 if p else 1) for (T, p) in sweep.cases)
-    d2h = sum(T * (g.N + g.d) * 4 for (T, p) in sweep.cases)
+    # ---- end to end: every read's R (and P) in from pinned host memory and
+    # every read's out and mean back, every step
+    host = {}
+    for T in SWEEP_T:
+        b = sweep.block(T)
+        host[T] = {k: torch.empty(b[k].shape, dtype=b[k].dtype).pin_memory() for k in ("R", "P", "out", "mean")}
+        host[T]["R"].copy_(b["R"])
+        host[T]["P"].copy_(b["P"])
+    h2d = sum(calls * T * g.N * 4 * (2 if p else 1) for (T, p) in sweep.cases)
+    d2h = sum(calls * T * (g.N + g.d) * 4 for (T, p) in sweep.cases)
     e2e_steps = max(3, min(args.steps, 20))
     if pg:
         pg.barrier()
@@ -639,20 +685,22 @@ def run_gpu(args):
     ea.record(stream)
     for _ in range(e2e_steps):
         for (T, p) in sweep.cases:
+            b, hb = sweep.block(T), host[T]
             with torch.cuda.stream(stream):
-                sweep.R[:T].copy_(pin_R[:T], non_blocking=True)
+                b["R"].copy_(hb["R"], non_blocking=True)
                 if p:
-                    sweep.P[:T].copy_(pin_P[:T], non_blocking=True)
+                    b["P"].copy_(hb["P"], non_blocking=True)
             sweep.replay((T, p))
             with torch.cuda.stream(stream):
-                host_out[:T].copy_(sweep.result()["out"][:T], non_blocking=True)
-                host_mean[:T].copy_(sweep.result()["mean"][:T], non_blocking=True)
+                hb["out"].copy_(b["out"], non_blocking=True)
+                hb["mean"].copy_(b["mean"], non_blocking=True)
     eb.record(stream)
     eb.synchronize()
     e2e_sec = ea.elapsed_time(eb) / 1e3
     e2e_sec = max_over_ranks(pg, e2e_sec, dev)
     e2e_value = whole_job_gbs(world, step_bytes, e2e_steps, e2e_sec)
     sweep.close()
+    del host
 
     extra = {}
     if not args.quick:
@@ -741,15 +789,17 @@ def run_gpu(args):
         "dtype": "f32 (bf16 weights)", "data": "synthetic",
         "config": {"workload": "cold read sweep: n=4 streams, d=2560, K=320, T in (1,2,3,4,5,6,8), "
                                "pending write off and on, 300 independent reads per case rotated over "
-                               "16 weight sets, own outputs per read, one hc_read_batch per case, "
-                               "CUDA-graph replay",
+                               "16 weight sets, own inputs and outputs per read, one hc_read_batch per "
+                               "case, CUDA-graph replay",
                    "batch_plan": sorted(plans),
                    "l2": "inputs larger than L2 (16 x 13.1 MB weight sets rotated)",
                    "parallelism": f"replicas x{world}"},
         "us_per_read": us_per_read, "GBps_per_case": gbs_per_case,
         "roofline": roofline, "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "note": "per step, every read's own R (and P) copied in from pinned host memory and "
+                        "every read's out and mean copied back, around the same graph replays"},
         "gpu_launches": 2 * calls * len(sweep_cases()) * args.steps,
         "clocks": clocks.summary(),
         "extra": extra,
@@ -777,6 +827,9 @@ def main(argv=None):
                          "before each), a small case for ncu captures")
     ap.add_argument("--profile-q2", action="store_true",
                     help="run the small Q2_0 product case used for ncu captures and exit")
+    ap.add_argument("--profile-wide", action="store_true",
+                    help="no timing: cold direct reads at T=16 and T=64 on the wide tensor-memory "
+                         "pair, a small case for ncu captures")
     ap.add_argument("--profile-q8", action="store_true",
                     help="no timing: cold direct reads, BF16 and Q8_0 at T=4, Q8_0 at T=1 and T=8, "
                          "a small case for ncu captures")
@@ -788,6 +841,8 @@ def main(argv=None):
         return run_profile_case()
     if args.profile_q8:
         return run_profile_q8_case()
+    if args.profile_wide:
+        return run_profile_wide_case()
     if args.profile_q2:
         return run_profile_q2_case()
     return run_gpu(args)
