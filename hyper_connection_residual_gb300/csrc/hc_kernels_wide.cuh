@@ -8,8 +8,9 @@
 //
 // Both kernels hold a 64-row weight tile (M = 64) in shared memory, brought
 // by 2-D TMA boxes of 64 columns in the 128-byte swizzle layout, and run the
-// tokens in passes of 16: the FP32 activations of a pass are split into two
-// BF16 terms (hi = bf16(x), lo = bf16(x - hi), the split of
+// tokens in passes of 16 (the up kernel; the down kernel of T > 16 runs
+// all tokens in one pass, below): the FP32 activations of a pass are split
+// into two BF16 terms (hi = bf16(x), lo = bf16(x - hi), the split of
 // hc_kernels_tc.cuh) as 2 x 16 rows of the B operand, also in the 128-byte
 // swizzle layout (threads running along the columns of one token then store
 // with at most two-way bank conflicts), and 20 tcgen05.mma (K = 16 each) of
@@ -17,18 +18,24 @@
 // accumulator in tensor memory.  One B buffer serves the passes in turn; the
 // next pass's loads go out as soon as a pass is staged, so they are in
 // flight while its MMAs run.  Shared memory is sized by T, and three CTAs
-// fit an SM (the up kernel: up to T = 48).  Both kernels have a single-pass
-// instantiation for T <= 16 (MULTI = false: fewer registers, no pass loop),
-// measured 10 % faster there.
+// fit an SM (the up kernel: up to T = 48).  For T <= 16 the up kernel has a
+// single-pass instantiation (MULTI = false: fewer registers, no pass loop)
+// and the down kernel a single-pass kernel of its own, measured 4-10 %
+// faster there than the general forms.
 //
-// hc_down_w_kernel: grid (32 column chunks, 5 row groups), clusters of the 8
+// Down kernels: grid (32 column chunks, 5 row groups), clusters of the 8
 // chunks of one stream, 256 threads.  A CTA owns rows 64 g .. 64 g + 63 of
-// W_down x 320 columns; warp w stages tokens w and w + 8 of each pass
-// (x = R' * w_norm, the sums of squares by warp shuffles), and after the last
-// pass each accumulator row's partial sum per token (hi + lo column) goes
-// through distributed shared memory to the rank that finishes it (rank q:
-// rows 8 q .. 8 q + 7), which adds the 8 chunks in a fixed order, applies rs
-// and writes part[s][t][k] exactly as the other down kernels do.
+// W_down x 320 columns and stages x = R' * w_norm (the sums of squares by
+// shuffles); after its MMAs each accumulator row's partial sum per token
+// (hi + lo column) goes through distributed shared memory to the rank that
+// finishes it (rank q: rows 8 q .. 8 q + 7), which adds the 8 chunks in a
+// fixed order, applies rs and writes part[s][t][k] exactly as the other down
+// kernels do.  hc_down_w1_kernel (T <= 16) stages every token at once, warp w
+// taking tokens w and w + 8.  hc_down_w_kernel (T > 16) stages B one K slice
+// at a time, for every token, into a ring of slices, so a single chain of 20
+// MMAs with N = 2 T covers all tokens: a tcgen05.mma of M = 64 costs about
+// the same ~56 cycles at N = 16, 32 or 64 (measured), so 16-token passes
+// would pay for the chain once per pass.
 //
 // hc_up_w_kernel: 160 CTAs of 16 columns x 4 streams = 64 rows of W_up (the
 // stream mean of a column stays inside the CTA), clusters of UCL.  lo is the
@@ -82,7 +89,7 @@ struct WGeo {
   static constexpr int RPR = M / CPS;             // rows each rank finishes
   static constexpr int KC4 = KC / 4;              // float4 of a token's chunk
   static constexpr int C4L = (KC4 + 31) / 32;     // ... per lane
-  static constexpr int DN_BAR = 0;                // bar_w, bar_mma[NPASS]
+  static constexpr int DN_BAR = 0;                // bar_w, bar_slot[2]
   static constexpr int DN_TSLOT = 64;
   static constexpr int DN_A = 1024;
   static constexpr int DN_B = DN_A + NSL_D * SLICE_A;
@@ -104,21 +111,39 @@ struct WGeo {
 
   __host__ __device__ static constexpr int npass(int T) { return (T + TP - 1) / TP; }
   __host__ __device__ static constexpr int r16(int b) { return (b + 15) / 16 * 16; }
-  // down kernel, T-sized regions after the B buffer.  The partials received
-  // from the cluster ([CPS][T][RPR]) get their own region up to RP_OWN_T
-  // tokens (three CTAs per SM still fit); above, they go over the A tile once
-  // every CTA of the cluster is past its MMAs (one more cluster barrier).
-  static constexpr int RP_OWN_T = 44;
-  __host__ __device__ static constexpr bool dn_rp_own(int T) { return T <= RP_OWN_T; }
-  __host__ __device__ static constexpr int dn_ssv(int T) { return DN_B + BBUF_D; }               // [T]
-  __host__ __device__ static constexpr int dn_rss(int T) { return dn_ssv(T) + r16(4 * T); }      // [CPS][T]
-  __host__ __device__ static constexpr int dn_rs(int T) { return dn_rss(T) + r16(4 * CPS * T); } // [T]
-  __host__ __device__ static constexpr int dn_rp(int T) { return dn_rp_own(T) ? dn_rs(T) + r16(4 * T) : DN_A; }
-  __host__ __device__ static constexpr int dn_bytes(int T) {
-    return (dn_rp_own(T) ? dn_rp(T) + 4 * CPS * T * RPR : dn_rs(T) + r16(4 * T)) + 1024;
+  // down kernel: B is a ring of K slices, each slice the 64 columns of one
+  // TMA box for every token (dn_brows rows: hi, lo per token, padded to a
+  // multiple of 8), so one chain of 20 MMAs with N = dn_brows covers all T
+  // tokens.  After the ring: this chunk's sums of squares [T], those received
+  // [CPS][T], rs [T], and the partials received from the cluster
+  // ([CPS][T][RPR]) in their own region, or over the A tile once every CTA of
+  // the cluster is past its MMAs (one more cluster barrier).  Two ring slots
+  // and the own region are used while three CTAs still fit an SM.
+  static constexpr int SMEM3 = 76800;  // at most this per CTA for three CTAs per SM
+  __host__ __device__ static constexpr int dn_brows(int T) { return (2 * T + 7) / 8 * 8; }
+  __host__ __device__ static constexpr int dn_slot(int T) { return dn_brows(T) * 128; }
+  __host__ __device__ static constexpr int dn_layout(int T, int nbuf, bool own) {
+    return DN_B + nbuf * dn_slot(T) + r16(4 * T) + r16(4 * CPS * T) + r16(4 * T) + (own ? 4 * CPS * T * RPR : 0) + 1024;
   }
-  // The most any T takes (the largest own receive region or the largest T).
-  static constexpr int DN_BYTES_MAX = dn_bytes(RP_OWN_T) > dn_bytes(TW) ? dn_bytes(RP_OWN_T) : dn_bytes(TW);
+  __host__ __device__ static constexpr int dn_nbuf(int T) {
+    return dn_layout(T, 2, false) <= SMEM3 ? 2 : 1;
+  }
+  __host__ __device__ static constexpr bool dn_rp_own(int T) { return dn_layout(T, dn_nbuf(T), true) <= SMEM3; }
+  __host__ __device__ static constexpr int dn_ssv(int T) { return DN_B + dn_nbuf(T) * dn_slot(T); }  // [T]
+  __host__ __device__ static constexpr int dn_rss(int T) { return dn_ssv(T) + r16(4 * T); }          // [CPS][T]
+  __host__ __device__ static constexpr int dn_rs(int T) { return dn_rss(T) + r16(4 * CPS * T); }     // [T]
+  __host__ __device__ static constexpr int dn_rp(int T) { return dn_rp_own(T) ? dn_rs(T) + r16(4 * T) : DN_A; }
+  __host__ __device__ static constexpr int dn_bytes(int T) { return dn_layout(T, dn_nbuf(T), dn_rp_own(T)); }
+  // single-pass down kernel (T <= TP): one B buffer of TP tokens over all
+  // K slices, then [T], [CPS][T], [T] and its own [CPS][T][RPR] region
+  __host__ __device__ static constexpr int d1_ssv(int T) { return DN_B + BBUF_D; }
+  __host__ __device__ static constexpr int d1_rss(int T) { return d1_ssv(T) + r16(4 * T); }
+  __host__ __device__ static constexpr int d1_rs(int T) { return d1_rss(T) + r16(4 * CPS * T); }
+  __host__ __device__ static constexpr int d1_rp(int T) { return d1_rs(T) + r16(4 * T); }
+  __host__ __device__ static constexpr int d1_bytes(int T) { return d1_rp(T) + 4 * CPS * T * RPR + 1024; }
+  __host__ __device__ static constexpr int imax(int x, int y) { return x > y ? x : y; }
+  __host__ __device__ static constexpr int dn_bytes_max(int T) { return T == 0 ? 0 : imax(dn_bytes(T), dn_bytes_max(T - 1)); }
+  static constexpr int DN_BYTES_MAX = dn_bytes_max(TW);
   // up kernel
   __host__ __device__ static constexpr int up_sig(int T) { return UP_B + BBUF_U; }               // [M]
   __host__ __device__ static constexpr int up_rp(int T) { return up_sig(T) + 4 * M; }            // [T][M]
@@ -132,8 +157,9 @@ struct WGeo {
   static_assert(SLICE_A % 1024 == 0 && SLICE_B % 1024 == 0 && DN_B % 1024 == 0 && UP_B % 1024 == 0,
                 "swizzled operands start on 1024-byte atoms");
   static_assert(4 * CPS * TW * RPR <= NSL_D * SLICE_A, "the received partials fit over the A tile");
-  static_assert(dn_bytes(RP_OWN_T) <= 75 * 1024 && dn_bytes(TW) <= 75 * 1024 && up_bytes(48) <= 75 * 1024,
+  static_assert(DN_BYTES_MAX <= SMEM3 && d1_bytes(TP) <= SMEM3 && up_bytes(48) <= SMEM3,
                 "three CTAs per SM (up kernel: T <= 48)");
+  static_assert(dn_brows(TW) <= TMEM_COLS && dn_brows(TW) <= 256, "one MMA chain covers every token");
   static_assert(up_bytes(TW) <= 113 * 1024, "two CTAs per SM at any T");
   static_assert(3 * TMEM_COLS <= 512, "three CTAs' accumulators fit the tensor memory");
 };
@@ -163,24 +189,26 @@ __device__ __forceinline__ void umma_pass(uint32_t tmem_d, uint32_t a0, uint32_t
   }
 }
 
-// ------------------------------------------------------------------ kernel 1
-template <int D, int KD, bool MULTI>
-__global__ void __launch_bounds__(WGeo<D, KD>::THREADS, 3) hc_down_w_kernel(const __grid_constant__ DownUArgs args) {
+// ------------------------------------------------------------------ kernel 1, T <= 16
+// One pass of at most 16 tokens: every token staged at once (the loads of
+// all of them in flight together), one chain of 20 MMAs.
+template <int D, int KD>
+__global__ void __launch_bounds__(WGeo<D, KD>::THREADS, 3) hc_down_w1_kernel(const __grid_constant__ DownUArgs args) {
   using W = WGeo<D, KD>;
   const DownArgs& a = args.a;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   unsigned char* smem = aligned_smem(smem_raw);
   const int T = a.T;
-  const int npass = MULTI ? W::npass(T) : 1;  // MULTI = false: T <= TP
+  const int npass = 1;  // T <= TP
   uint64_t* bar_w = reinterpret_cast<uint64_t*>(smem + W::DN_BAR);
   uint64_t* bar_mma = bar_w + 1;  // [NPASS]
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + W::DN_TSLOT);
   unsigned char* sa = smem + W::DN_A;
   unsigned char* sb = smem + W::DN_B;
-  float* ssv = reinterpret_cast<float*>(smem + W::dn_ssv(T));
-  float* rss = reinterpret_cast<float*>(smem + W::dn_rss(T));
-  float* rpr = reinterpret_cast<float*>(smem + W::dn_rp(T));  // own region, or over the A tile
-  float* rs_s = reinterpret_cast<float*>(smem + W::dn_rs(T));
+  float* ssv = reinterpret_cast<float*>(smem + W::d1_ssv(T));
+  float* rss = reinterpret_cast<float*>(smem + W::d1_rss(T));
+  float* rpr = reinterpret_cast<float*>(smem + W::d1_rp(T));  // own region, or over the A tile
+  float* rs_s = reinterpret_cast<float*>(smem + W::d1_rs(T));
 
   const uint64_t t_entry = ptx::globaltimer_ns();
   const int chunk = blockIdx.x;
@@ -322,14 +350,6 @@ __global__ void __launch_bounds__(WGeo<D, KD>::THREADS, 3) hc_down_w_kernel(cons
 #pragma unroll
     for (int q = 0; q < W::CPS; ++q) cluster.map_shared_rank(rss, q)[rank * T + tid] = v;
   }
-  if (!W::dn_rp_own(T)) {
-    // The received partials go over the A tile: every CTA of the cluster is
-    // past its MMAs before anyone writes into a peer.
-    __syncwarp();
-    ptx::tc_fence_before();
-    ptx::cluster_arrive_release();
-    ptx::cluster_wait();
-  }
   __syncwarp();
   ptx::tc_fence_after();
 
@@ -350,6 +370,237 @@ __global__ void __launch_bounds__(WGeo<D, KD>::THREADS, 3) hc_down_w_kernel(cons
         for (int e = 0; e < 8; ++e) {
           const int col = c + 2 * e;
           const int t = (col / W::PCOLS) * W::TP + (col % W::PCOLS) / 2;
+          if (t < T) {
+            dst[((int)rank * T + t) * W::RPR + row % W::RPR] =
+                __fadd_rn(__uint_as_float(d[2 * e]), __uint_as_float(d[2 * e + 1]));
+          }
+        }
+      }
+    }
+  }
+  __syncwarp();
+  ptx::tc_fence_before();
+  if (late_launch) ptx::launch_dependents();
+  ptx::cluster_arrive_release();
+  ptx::cluster_wait();  // every chunk's sums of squares and partials are here
+  ptx::tc_fence_after();
+  if (warp == 0) ptx::tmem_dealloc(tmem, W::TMEM_COLS);
+
+  for (int t = tid; t < T; t += W::THREADS) {
+    float ss = 0.f;
+#pragma unroll
+    for (int q = 0; q < W::CPS; ++q) ss += rss[q * T + t];
+    const float rs = rsqrtf(ss * (1.0f / (float)D) + a.eps);
+    rs_s[t] = rs;
+    if (rg == 0 && rank == 0 && a.rs_out != nullptr) a.rs_out[t * kStreams + stream] = rs;
+  }
+  __syncthreads();
+  float* part = a.part + (size_t)stream * a.T_max * KD;
+  for (int idx = tid; idx < T * W::RPR; idx += W::THREADS) {
+    const int t = idx / W::RPR, r8 = idx - t * W::RPR;
+    float p = 0.f;
+#pragma unroll
+    for (int q = 0; q < W::CPS; ++q) p += rpr[(q * T + t) * W::RPR + r8];
+    __stcg(part + (size_t)t * KD + row0 + (int)rank * W::RPR + r8, __fmul_rn(rs_s[t], p));
+  }
+  if (a.independent) ptx::wait_prerequisites();  // complete only after the previous read
+}
+
+// ------------------------------------------------------------------ kernel 1, T > 16
+// TT: tokens per staging thread (T <= 16 TT); NPF slices of loads in flight.
+template <int D, int KD, int TT>
+__global__ void __launch_bounds__(WGeo<D, KD>::THREADS, 3) hc_down_w_kernel(const __grid_constant__ DownUArgs args) {
+  using W = WGeo<D, KD>;
+  const DownArgs& a = args.a;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  unsigned char* smem = aligned_smem(smem_raw);
+  const int T = a.T;
+  const int nbuf = W::dn_nbuf(T);        // ring slots (1 or 2)
+  const int brows = W::dn_brows(T);      // B rows = MMA N (hi, lo per token, padded to 8)
+  const int slot_bytes = W::dn_slot(T);
+  uint64_t* bar_w = reinterpret_cast<uint64_t*>(smem + W::DN_BAR);
+  uint64_t* bar_slot = bar_w + 1;  // [2] the MMAs of the slice in a ring slot are done
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + W::DN_TSLOT);
+  unsigned char* sa = smem + W::DN_A;
+  unsigned char* sb = smem + W::DN_B;
+  float* ssv = reinterpret_cast<float*>(smem + W::dn_ssv(T));
+  float* rss = reinterpret_cast<float*>(smem + W::dn_rss(T));
+  float* rpr = reinterpret_cast<float*>(smem + W::dn_rp(T));  // own region, or over the A tile
+  float* rs_s = reinterpret_cast<float*>(smem + W::dn_rs(T));
+
+  const uint64_t t_entry = ptx::globaltimer_ns();
+  const int chunk = blockIdx.x;
+  const int stream = chunk / W::CPS;
+  const int rg = blockIdx.y;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int col0 = chunk * W::KC;
+  const int row0 = rg * W::M;
+
+  cg::cluster_group cluster = cg::this_cluster();
+  const unsigned rank = cluster.block_rank();
+  ptx::cluster_arrive_relaxed();
+
+  // The W_down tile (weights, independent of earlier kernels).
+  if (tid == 0) {
+    ptx::mbar_init(bar_w, 1);
+    ptx::mbar_init(&bar_slot[0], 1);
+    ptx::mbar_init(&bar_slot[1], 1);
+    ptx::fence_barrier_init();
+    ptx::mbar_arrive_expect_tx(bar_w, W::M * W::KC * 2);
+    const uint64_t once = ptx::policy_evict_first();
+#pragma unroll
+    for (int j = 0; j < W::NSL_D; ++j) ptx::tma_load_2d(sa + j * W::SLICE_A, &args.w, col0 + 64 * j, row0, bar_w, once);
+  }
+  if (warp == 1) {
+    __syncwarp();  // tcgen05.alloc is .aligned
+    ptx::tmem_alloc(tslot, W::TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  // Independent reads on the batch lanes let the up kernel launch only at
+  // the end (see hc_down_kernel).
+  const bool late_launch = a.late_launch && a.independent;
+  if (!late_launch) ptx::launch_dependents();
+  ptx::tc_fence_before();
+  __syncthreads();  // tensor-memory address and mbarriers visible to all
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tslot;
+  if (!a.independent) ptx::wait_prerequisites();
+  ptx::cluster_wait();  // every CTA of the cluster runs before anyone writes a peer
+
+  // Thread (tg = tid / 16, c4 = tid % 16) stages tokens tg + 16 m (m < TT)
+  // at columns 4 c4 .. 4 c4 + 3 of every K slice: R' = R + P, x = R' * w_norm
+  // split into B rows 2 t (hi) and 2 t + 1 (lo), and its share of each
+  // token's sum of squares.  The loads of NPF slices are in flight at once
+  // (all five at T <= 16); a slice's registers are refilled with the loads
+  // of slice j + NPF as soon as it is staged.
+  constexpr int NPF = TT == 1 ? W::NSL_D : TT == 2 ? 2 : 1;  // more would spill at TT = 4
+  const int tg = tid >> 4, c4 = tid & 15;
+  float4 rv[NPF][TT], pv[NPF][TT], wn[NPF];
+  float ssr[TT];
+#pragma unroll
+  for (int m = 0; m < TT; ++m) ssr[m] = 0.f;
+  auto load_slice = [&](int j, float4 (&r)[TT], float4 (&q)[TT], float4& w) {
+    const int col = col0 + 64 * j + 4 * c4;
+    w = __ldg(reinterpret_cast<const float4*>(a.w_norm + col));
+#pragma unroll
+    for (int m = 0; m < TT; ++m) {
+      const int t = tg + 16 * m;
+      r[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+      q[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (t < T) {
+        r[m] = __ldcg(reinterpret_cast<const float4*>(a.R + (size_t)t * W::N + col));
+        if (a.P) q[m] = __ldcg(reinterpret_cast<const float4*>(a.P + (size_t)t * W::N + col));
+      }
+    }
+  };
+  bool ok = true;
+  const uint32_t a0 = ptx::smem_u32(sa);
+  const uint32_t idesc = ptx::umma_idesc_bf16(W::M, brows);
+#pragma unroll
+  for (int j = 0; j < NPF; ++j) load_slice(j, rv[j], pv[j], wn[j]);
+#pragma unroll
+  for (int j = 0; j < W::NSL_D; ++j) {
+    const int slot = j % nbuf;
+    const int f = j % NPF;  // register set of the slice (compile-time: the loop is unrolled)
+    unsigned char* bp = sb + slot * slot_bytes;
+    // The slot was last read by the MMAs of slice j - nbuf.
+    if (j >= nbuf) {
+      if (ok) ok = wait_bar(&bar_slot[slot], (uint32_t)((j / nbuf - 1) & 1), a.err, kErrDownWeights);
+      ptx::tc_fence_after();
+    }
+#pragma unroll
+    for (int m = 0; m < TT; ++m) {
+      const int t = tg + 16 * m;
+      if (t < T) {
+        float4 r = rv[f][m];
+        r.x = __fadd_rn(r.x, pv[f][m].x);
+        r.y = __fadd_rn(r.y, pv[f][m].y);
+        r.z = __fadd_rn(r.z, pv[f][m].z);
+        r.w = __fadd_rn(r.w, pv[f][m].w);
+        const float4 w = wn[f];
+        const float4 x = make_float4(__fmul_rn(r.x, w.x), __fmul_rn(r.y, w.y), __fmul_rn(r.z, w.z), __fmul_rn(r.w, w.w));
+        uint2 hi, lo;
+        split4(x, hi, lo);
+        *reinterpret_cast<uint2*>(bp + sw128_off<1>(2 * t, 4 * c4)) = hi;  // within one 64-column slice
+        *reinterpret_cast<uint2*>(bp + sw128_off<1>(2 * t + 1, 4 * c4)) = lo;
+        ssr[m] = __fmaf_rn(r.x, r.x, ssr[m]);
+        ssr[m] = __fmaf_rn(r.y, r.y, ssr[m]);
+        ssr[m] = __fmaf_rn(r.z, r.z, ssr[m]);
+        ssr[m] = __fmaf_rn(r.w, r.w, ssr[m]);
+      }
+    }
+    if (j + NPF < W::NSL_D) load_slice(j + NPF, rv[f], pv[f], wn[f]);
+    if (j == 0) ok = wait_bar_from(bar_w, 0, a.err, kErrDownWeights, t_entry, first_wait_limit(a.wait_ns)) && ok;
+    ptx::fence_proxy_async_smem();  // this thread's B stores, visible to the tensor cores
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    if (tid == 0) {
+      if (ok) {
+        // K-steps 4 j .. 4 j + 3 of the chain, N = brows (every token).
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          ptx::umma_bf16(tmem, ptx::umma_desc_sw128(a0 + j * W::SLICE_A + k * 32),
+                         ptx::umma_desc_sw128(ptx::smem_u32(bp) + k * 32), idesc, (j | k) ? 1u : 0u);
+        }
+        ptx::umma_commit(&bar_slot[slot]);
+      } else {
+        mbar_arrive_local(&bar_slot[slot]);  // nothing issued: release the waiters
+      }
+    }
+  }
+  // The last slice's commit tracks every MMA of the CTA.
+  {
+    const int jl = W::NSL_D - 1;
+    if (ok) ok = wait_bar(&bar_slot[jl % nbuf], (uint32_t)((jl / nbuf) & 1), a.err, kErrDownWeights);
+  }
+  if (!ok) drain(bar_w, 0);
+  // Each token's sum of squares over the chunk: the 16 threads of a token,
+  // in a fixed order.
+#pragma unroll
+  for (int m = 0; m < TT; ++m) {
+    float v = ssr[m];
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (c4 == 0 && tg + 16 * m < T) ssv[tg + 16 * m] = v;
+  }
+  __syncthreads();
+  // This chunk's sums of squares to every rank of the cluster.
+  if (tid < T) {
+    const float v = ssv[tid];
+#pragma unroll
+    for (int q = 0; q < W::CPS; ++q) cluster.map_shared_rank(rss, q)[rank * T + tid] = v;
+  }
+  if (!W::dn_rp_own(T)) {
+    // The received partials go over the A tile: every CTA of the cluster is
+    // past its MMAs before anyone writes into a peer.
+    __syncwarp();
+    ptx::tc_fence_before();
+    ptx::cluster_arrive_release();
+    ptx::cluster_wait();
+  }
+  __syncwarp();
+  ptx::tc_fence_after();
+
+  // Accumulators: warp w reads lane quadrant w % 4 (tile rows 16 (w % 4) ..
+  // + 15 in its lanes 0..15) over half w / 4 of the columns in use (token t
+  // in columns 2 t, 2 t + 1); each row's partial per token goes to the rank
+  // that finishes the row.
+  {
+    const int qd = warp & 3, h = warp >> 2;
+    const int ncols = (2 * T + 31) / 32 * 32;
+    const int row = 16 * qd + (lane & 15);
+    float* dst = cluster.map_shared_rank(rpr, row / W::RPR);
+    for (int c = h * (ncols / 2); c < (h + 1) * (ncols / 2); c += 16) {
+      uint32_t d[16];
+      ptx::tmem_ld16(tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)c, d);
+      ptx::tmem_wait_ld();
+      if (lane < 16) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int t = c / 2 + e;
           if (t < T) {
             dst[((int)rank * T + t) * W::RPR + row % W::RPR] =
                 __fadd_rn(__uint_as_float(d[2 * e]), __uint_as_float(d[2 * e + 1]));

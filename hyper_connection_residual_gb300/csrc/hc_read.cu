@@ -169,14 +169,15 @@ template <int D, int KD>
 cudaError_t configure_wide() {
   using W = hc::WGeo<D, KD>;
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(hc::hc_down_w_kernel<D, KD, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                W::dn_bytes(W::TP))) != cudaSuccess)
+  if ((e = cudaFuncSetAttribute(hc::hc_down_w1_kernel<D, KD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                W::d1_bytes(W::TP))) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(hc::hc_down_w_kernel<D, KD, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                W::DN_BYTES_MAX)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(hc::hc_down_w_kernel<D, KD, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                W::DN_BYTES_MAX)) != cudaSuccess)
     return e;
   if ((e = cudaFuncSetAttribute(hc::hc_up_w_kernel<D, KD, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 W::up_bytes(W::TP))) != cudaSuccess)
-    return e;
-  if ((e = cudaFuncSetAttribute(hc::hc_down_w_kernel<D, KD, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                W::DN_BYTES_MAX)) != cudaSuccess)
     return e;
   return cudaFuncSetAttribute(hc::hc_up_w_kernel<D, KD, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               W::up_bytes(W::TW));
@@ -295,8 +296,13 @@ cudaError_t launch_pair_w(const DownArgs& da, const UpArgs& ua, const CUtensorMa
   // T <= 16: the single-pass instantiations.
   const bool multi = da.T > W::TP;
   cudaLaunchConfig_t c1 = pdl_config(dim3(W::CHUNKS, W::ROW_GROUPS), W::dn_bytes(da.T), st, attr, W::CPS, W::THREADS);
-  cudaError_t e = multi ? cudaLaunchKernelEx(&c1, hc::hc_down_w_kernel<D, KD, true>, dargs)
-                        : cudaLaunchKernelEx(&c1, hc::hc_down_w_kernel<D, KD, false>, dargs);
+  // Down kernel: T <= 16 the single pass (measured 4 % faster there than
+  // the K-slice ring), above it the ring with 2 or 4 tokens per staging
+  // thread (8-10 % faster at T = 17..48 than 16-token passes).
+  if (da.T <= W::TP) c1.dynamicSmemBytes = W::d1_bytes(da.T);
+  cudaError_t e = da.T <= W::TP ? cudaLaunchKernelEx(&c1, hc::hc_down_w1_kernel<D, KD>, dargs)
+                  : da.T <= 32  ? cudaLaunchKernelEx(&c1, hc::hc_down_w_kernel<D, KD, 2>, dargs)
+                                : cudaLaunchKernelEx(&c1, hc::hc_down_w_kernel<D, KD, 4>, dargs);
   if (e != cudaSuccess) return e;
   hc::UpWArgs uargs;
   uargs.w = w_up;
