@@ -97,17 +97,12 @@ struct WGeo {
   static constexpr int UC = M / kStreams;
   static constexpr int UP_CTAS = D / UC;
   static constexpr int UCL = 4;                   // cluster size
-  static constexpr int TPR = TP / UCL;            // tokens of a pass each rank combines
-  static constexpr int RROWS = 2 * TPR;           // ... B rows
   static constexpr int NSL_U = KD / 64;
-  static constexpr int BBUF_U = NSL_U * SLICE_B;
   static constexpr int KD4 = KD / 4;
   static constexpr int UP_BAR = 0;                // bar_w, bar_mma[NPASS], bar_b[NPASS]
   static constexpr int UP_TSLOT = 96;
   static constexpr int UP_A = 1024;
   static constexpr int UP_B = UP_A + NSL_U * SLICE_A;
-  // bytes a CTA receives from its peers per pass
-  static constexpr int UP_RECV = (UCL - 1) * NSL_U * RROWS * 128;
 
   __host__ __device__ static constexpr int npass(int T) { return (T + TP - 1) / TP; }
   __host__ __device__ static constexpr int r16(int b) { return (b + 15) / 16 * 16; }
@@ -144,25 +139,50 @@ struct WGeo {
   __host__ __device__ static constexpr int imax(int x, int y) { return x > y ? x : y; }
   __host__ __device__ static constexpr int dn_bytes_max(int T) { return T == 0 ? 0 : imax(dn_bytes(T), dn_bytes_max(T - 1)); }
   static constexpr int DN_BYTES_MAX = dn_bytes_max(TW);
-  // up kernel
-  __host__ __device__ static constexpr int up_sig(int T) { return UP_B + BBUF_U; }               // [M]
-  __host__ __device__ static constexpr int up_rp(int T) { return up_sig(T) + 4 * M; }            // [T][M]
-  __host__ __device__ static constexpr int up_bytes(int T) { return up_rp(T) + 4 * M * T + 1024; }
 
   static_assert(D == 2560 && KD == 320, "wide tensor-memory kernels: d = 2560, K = 320");
   static_assert(KC % 64 == 0 && KD % 64 == 0, "whole 64-wide K slices");
   static_assert(CHUNKS == kStreams * CPS && RPR == 8, "clusters of one stream's 8 chunks");
   static_assert(TP == 2 * WARPS, "warp w stages tokens w and w + 8 of a pass");
-  static_assert(UP_CTAS % UCL == 0 && TP % UCL == 0 && (RROWS * 128) % 16 == 0, "up clusters split a pass by tokens");
+  static_assert(UP_CTAS % UCL == 0, "up clusters");
   static_assert(SLICE_A % 1024 == 0 && SLICE_B % 1024 == 0 && DN_B % 1024 == 0 && UP_B % 1024 == 0,
                 "swizzled operands start on 1024-byte atoms");
   static_assert(4 * CPS * TW * RPR <= NSL_D * SLICE_A, "the received partials fit over the A tile");
-  static_assert(DN_BYTES_MAX <= SMEM3 && d1_bytes(TP) <= SMEM3 && up_bytes(48) <= SMEM3,
-                "three CTAs per SM (up kernel: T <= 48)");
+  static_assert(DN_BYTES_MAX <= SMEM3 && d1_bytes(TP) <= SMEM3, "three down CTAs per SM");
   static_assert(dn_brows(TW) <= TMEM_COLS && dn_brows(TW) <= 256, "one MMA chain covers every token");
-  static_assert(up_bytes(TW) <= 113 * 1024, "two CTAs per SM at any T");
   static_assert(3 * TMEM_COLS <= 512, "three CTAs' accumulators fit the tensor memory");
 };
+
+// The up kernel's pass geometry: passes of TP tokens (2 TP B rows, 2 TP
+// accumulator columns), each rank of a cluster combining TP / UCL tokens of
+// a pass.  TP = 16 keeps three CTAs per SM up to T = 48; above, where the R'
+// of 64 tokens already limits the kernel to two CTAs per SM, TP = 32 halves
+// the passes (and their MMA chains, buffer-reuse barriers and exchanges).
+template <int D, int KD, int TP_>
+struct UpPass {
+  using W = WGeo<D, KD>;
+  static constexpr int TP = TP_;
+  static constexpr int BROWS = 2 * TP;                 // B rows of a pass
+  static constexpr int SLICE_B = BROWS * 128;          // a 64-wide K slice of B
+  static constexpr int PCOLS = 2 * TP;                 // accumulator columns of a pass
+  static constexpr int NPASS = W::TW / TP;
+  static constexpr int TPR = TP / W::UCL;              // tokens of a pass each rank combines
+  static constexpr int RROWS = 2 * TPR;                // ... B rows
+  static constexpr int BBUF_U = W::NSL_U * SLICE_B;    // the B buffer
+  static constexpr int UP_RECV = (W::UCL - 1) * W::NSL_U * RROWS * 128;  // bytes from the peers per pass
+  __host__ __device__ static constexpr int npass(int T) { return (T + TP - 1) / TP; }
+  __host__ __device__ static constexpr int up_sig(int T) { return W::UP_B + BBUF_U; }     // [M]
+  __host__ __device__ static constexpr int up_rp(int T) { return up_sig(T) + 4 * W::M; }  // [T][M]
+  __host__ __device__ static constexpr int up_bytes(int T) { return up_rp(T) + 4 * W::M * T + 1024; }
+  static_assert(TP % W::UCL == 0 && (RROWS * 128) % 16 == 0, "clusters split a pass by tokens");
+  static_assert(NPASS * PCOLS == W::TMEM_COLS, "the passes' accumulators fill the tensor memory");
+  static_assert(8 * (1 + 2 * NPASS) <= W::UP_TSLOT, "the barriers fit before the tensor-memory slot");
+  static_assert(SLICE_B % 1024 == 0 && W::UP_B % 1024 == 0, "swizzled operands start on 1024-byte atoms");
+  static_assert(up_bytes(W::TW) <= 113 * 1024, "two CTAs per SM at any T");
+};
+
+static_assert(UpPass<2560, 320, 16>::up_bytes(48) <= WGeo<2560, 320>::SMEM3,
+              "three up CTAs per SM with 16-token passes up to T = 48");
 
 // Byte offset of element (n, k) of a K-major BF16 operand of ROWS rows in the
 // 128-byte swizzle layout: 64-wide K slices of ROWS * 128 bytes, rows of 128
@@ -638,22 +658,24 @@ __global__ void __launch_bounds__(WGeo<D, KD>::THREADS, 3) hc_down_w_kernel(cons
 }
 
 // ------------------------------------------------------------------ kernel 2
-template <int D, int KD, bool MULTI>
-__global__ void __launch_bounds__(WGeo<D, KD>::THREADS, 3) hc_up_w_kernel(const __grid_constant__ UpWArgs args) {
+template <int D, int KD, bool MULTI, int TPU>
+__global__ void __launch_bounds__(WGeo<D, KD>::THREADS, TPU == 16 ? 3 : 2)
+    hc_up_w_kernel(const __grid_constant__ UpWArgs args) {
   using W = WGeo<D, KD>;
+  using P = UpPass<D, KD, TPU>;
   const UpArgs& a = args.a;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   unsigned char* smem = aligned_smem(smem_raw);
   const int T = a.T;
-  const int npass = MULTI ? W::npass(T) : 1;  // MULTI = false: T <= TP
+  const int npass = MULTI ? P::npass(T) : 1;  // MULTI = false: T <= TP
   uint64_t* bar_w = reinterpret_cast<uint64_t*>(smem + W::UP_BAR);
   uint64_t* bar_mma = bar_w + 1;            // [NPASS]
-  uint64_t* bar_b = bar_w + 1 + W::NPASS;   // [NPASS] the peers' B rows of a pass have landed
+  uint64_t* bar_b = bar_w + 1 + P::NPASS;   // [NPASS] the peers' B rows of a pass have landed
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + W::UP_TSLOT);
   unsigned char* sa = smem + W::UP_A;
   unsigned char* sb = smem + W::UP_B;
-  float* sig = reinterpret_cast<float*>(smem + W::up_sig(T));
-  float* rp = reinterpret_cast<float*>(smem + W::up_rp(T));
+  float* sig = reinterpret_cast<float*>(smem + P::up_sig(T));
+  float* rp = reinterpret_cast<float*>(smem + P::up_rp(T));
 
   const int c0 = blockIdx.x * W::UC;
   const int tid = threadIdx.x;
@@ -671,13 +693,13 @@ __global__ void __launch_bounds__(WGeo<D, KD>::THREADS, 3) hc_up_w_kernel(const 
   if (tid == 0) {
     ptx::mbar_init(bar_w, 1);
 #pragma unroll
-    for (int p = 0; p < W::NPASS; ++p) {
+    for (int p = 0; p < P::NPASS; ++p) {
       ptx::mbar_init(&bar_mma[p], 1);
       ptx::mbar_init(&bar_b[p], 1);
     }
     ptx::fence_barrier_init();
     ptx::mbar_arrive_expect_tx(bar_w, W::M * KD * 2);
-    for (int p = 0; p < npass; ++p) ptx::mbar_arrive_expect_tx(&bar_b[p], W::UP_RECV);
+    for (int p = 0; p < npass; ++p) ptx::mbar_arrive_expect_tx(&bar_b[p], P::UP_RECV);
     const uint64_t once = ptx::policy_evict_first();
 #pragma unroll
     for (int s = 0; s < kStreams; ++s) {
@@ -704,7 +726,7 @@ __global__ void __launch_bounds__(WGeo<D, KD>::THREADS, 3) hc_up_w_kernel(const 
 
   // R' = R + P of the tile's rows for every token, into rp[t][row]: 16
   // float4 per token (four streams x 16 columns).
-  constexpr int RP4 = ((MULTI ? W::TW : W::TP) * 16 + W::THREADS - 1) / W::THREADS;
+  constexpr int RP4 = ((MULTI ? W::TW : P::TP) * 16 + W::THREADS - 1) / W::THREADS;
   float4 rr[RP4], pp[RP4];
   auto load_rp = [&]() {
 #pragma unroll
@@ -740,19 +762,19 @@ __global__ void __launch_bounds__(WGeo<D, KD>::THREADS, 3) hc_up_w_kernel(const 
 
   const uint32_t a0 = ptx::smem_u32(sa);
   bool ok = true;  // thread 0: the weight tile and the peers' rows landed
-  constexpr int CI = (W::TPR * W::KD4 + W::THREADS - 1) / W::THREADS;  // combine items per thread
+  constexpr int CI = (P::TPR * W::KD4 + W::THREADS - 1) / W::THREADS;  // combine items per thread
   using Part = float4[CI][kStreams];
   // This rank's tokens of pass p: the four streams' partials over all K.
   auto load_pass = [&](int p, Part& pv) {
-    const int t0 = p * W::TP;
+    const int t0 = p * P::TP;
 #pragma unroll
     for (int i = 0; i < CI; ++i) {
       const int idx = tid + i * W::THREADS;
-      const int t = t0 + (int)rank * W::TPR + idx / W::KD4;
+      const int t = t0 + (int)rank * P::TPR + idx / W::KD4;
 #pragma unroll
       for (int s = 0; s < kStreams; ++s) {
         pv[i][s] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (idx < W::TPR * W::KD4 && t < T) {
+        if (idx < P::TPR * W::KD4 && t < T) {
           pv[i][s] = __ldcg(reinterpret_cast<const float4*>(a.part + ((size_t)s * a.T_max + t) * KD) + idx % W::KD4);
         }
       }
@@ -761,7 +783,7 @@ __global__ void __launch_bounds__(WGeo<D, KD>::THREADS, 3) hc_up_w_kernel(const 
   Part pv;
   load_pass(0, pv);
   for (int p = 0; p < npass; ++p) {
-    const int t0 = p * W::TP;
+    const int t0 = p * P::TP;
     unsigned char* bp = sb;
     if (p >= 1) {
       // The buffer of every CTA of the cluster was last read by the MMAs of
@@ -777,8 +799,8 @@ __global__ void __launch_bounds__(WGeo<D, KD>::THREADS, 3) hc_up_w_kernel(const 
 #pragma unroll
     for (int i = 0; i < CI; ++i) {
       const int idx = tid + i * W::THREADS;
-      const int tl = (int)rank * W::TPR + idx / W::KD4;  // token within the pass
-      if (idx < W::TPR * W::KD4 && t0 + tl < T) {
+      const int tl = (int)rank * P::TPR + idx / W::KD4;  // token within the pass
+      if (idx < P::TPR * W::KD4 && t0 + tl < T) {
         const int k = 4 * (idx % W::KD4);
         float4 l;
         l.x = ((pv[i][0].x + pv[i][1].x) + pv[i][2].x) + pv[i][3].x;
@@ -788,8 +810,8 @@ __global__ void __launch_bounds__(WGeo<D, KD>::THREADS, 3) hc_up_w_kernel(const 
         if (cq == 0) *reinterpret_cast<float4*>(a.lo + (size_t)(t0 + tl) * KD + k) = l;
         uint2 hi, lo;
         split4(l, hi, lo);
-        *reinterpret_cast<uint2*>(bp + sw128_off<W::BROWS>(2 * tl, k)) = hi;
-        *reinterpret_cast<uint2*>(bp + sw128_off<W::BROWS>(2 * tl + 1, k)) = lo;
+        *reinterpret_cast<uint2*>(bp + sw128_off<P::BROWS>(2 * tl, k)) = hi;
+        *reinterpret_cast<uint2*>(bp + sw128_off<P::BROWS>(2 * tl + 1, k)) = lo;
       }
     }
     // The registers are free: the next pass's partial loads go out now.
@@ -799,14 +821,14 @@ __global__ void __launch_bounds__(WGeo<D, KD>::THREADS, 3) hc_up_w_kernel(const 
     if (tid == 0) {
       // This rank's B rows (whole 128-byte rows of every K slice) into the
       // same place of every peer.
-      const uint32_t rows = ptx::smem_u32(bp) + rank * (uint32_t)(W::RROWS * 128);
+      const uint32_t rows = ptx::smem_u32(bp) + rank * (uint32_t)(P::RROWS * 128);
       const uint32_t bar = ptx::smem_u32(&bar_b[p]);
 #pragma unroll
       for (int j = 0; j < W::NSL_U; ++j) {
 #pragma unroll
         for (int q = 1; q < W::UCL; ++q) {
           const uint32_t peer = (rank + (uint32_t)q) % W::UCL;
-          ptx::bulk_s2peer(rows + j * W::SLICE_B, rows + j * W::SLICE_B, W::RROWS * 128, bar, peer);
+          ptx::bulk_s2peer(rows + j * P::SLICE_B, rows + j * P::SLICE_B, P::RROWS * 128, bar, peer);
         }
       }
       // The peers' rows of the pass, then the MMAs.
@@ -814,8 +836,8 @@ __global__ void __launch_bounds__(WGeo<D, KD>::THREADS, 3) hc_up_w_kernel(const 
       if (p == 0) ok = wait_bar(bar_w, 0, a.err, kErrUpWeights) && ok;
       ptx::tc_fence_after();
       if (ok) {
-        umma_pass<KD, W::SLICE_A, W::SLICE_B>(tmem + (uint32_t)(p * W::PCOLS), a0, ptx::smem_u32(bp), W::M,
-                                              (2 * min(W::TP, T - t0) + 7) & ~7);
+        umma_pass<KD, W::SLICE_A, P::SLICE_B>(tmem + (uint32_t)(p * P::PCOLS), a0, ptx::smem_u32(bp), W::M,
+                                              (2 * min(P::TP, T - t0) + 7) & ~7);
         ptx::umma_commit(&bar_mma[p]);
       } else {
         mbar_arrive_local(&bar_mma[p]);
@@ -836,7 +858,7 @@ __global__ void __launch_bounds__(WGeo<D, KD>::THREADS, 3) hc_up_w_kernel(const 
   // by out in rp for the stream mean.
   {
     const int s = warp & 3, h = warp >> 2;
-    const int ncols = npass * W::PCOLS;
+    const int ncols = npass * P::PCOLS;
     const int row = 16 * s + (lane & 15);
     for (int c = h * (ncols / 2); c < (h + 1) * (ncols / 2); c += 16) {
       uint32_t d[16];
@@ -846,7 +868,7 @@ __global__ void __launch_bounds__(WGeo<D, KD>::THREADS, 3) hc_up_w_kernel(const 
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int col = c + 2 * e;
-          const int t = (col / W::PCOLS) * W::TP + (col % W::PCOLS) / 2;
+          const int t = (col / P::PCOLS) * P::TP + (col % P::PCOLS) / 2;
           if (t < T) {
             const float u = __fadd_rn(__uint_as_float(d[2 * e]), __uint_as_float(d[2 * e + 1]));
             const float r = rp[t * W::M + row];

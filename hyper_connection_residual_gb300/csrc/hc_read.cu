@@ -30,6 +30,8 @@ constexpr int kBatchLanes = 6;
 // Reads of at least this many tokens (d = 2560) take the wide tensor-memory
 // pair (hc_kernels_wide.cuh).
 constexpr int kWideMinT = 9;
+// ... and from this many tokens the wide up kernel runs 32-token passes.
+constexpr int kUpPass32MinT = 49;
 
 // The tensor maps of the weight matrices a handle has seen, by address:
 // W_down in boxes of 64 columns x 64 rows (the tensor-memory down kernels),
@@ -176,11 +178,15 @@ cudaError_t configure_wide() {
       (e = cudaFuncSetAttribute(hc::hc_down_w_kernel<D, KD, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 W::DN_BYTES_MAX)) != cudaSuccess)
     return e;
-  if ((e = cudaFuncSetAttribute(hc::hc_up_w_kernel<D, KD, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                W::up_bytes(W::TP))) != cudaSuccess)
+  using P16 = hc::UpPass<D, KD, 16>;
+  using P32 = hc::UpPass<D, KD, 32>;
+  if ((e = cudaFuncSetAttribute(hc::hc_up_w_kernel<D, KD, false, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                P16::up_bytes(16))) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(hc::hc_up_w_kernel<D, KD, true, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                P16::up_bytes(kUpPass32MinT - 1))) != cudaSuccess)
     return e;
-  return cudaFuncSetAttribute(hc::hc_up_w_kernel<D, KD, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              W::up_bytes(W::TW));
+  return cudaFuncSetAttribute(hc::hc_up_w_kernel<D, KD, true, 32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              P32::up_bytes(W::TW));
 }
 
 template <int D, int KD>
@@ -308,9 +314,18 @@ cudaError_t launch_pair_w(const DownArgs& da, const UpArgs& ua, const CUtensorMa
   uargs.w = w_up;
   uargs.a = ua;
   cudaLaunchAttribute attr2[2];
-  cudaLaunchConfig_t c2 = pdl_config(dim3(W::UP_CTAS), W::up_bytes(ua.T), st, attr2, W::UCL, W::THREADS);
-  return multi ? cudaLaunchKernelEx(&c2, hc::hc_up_w_kernel<D, KD, true>, uargs)
-               : cudaLaunchKernelEx(&c2, hc::hc_up_w_kernel<D, KD, false>, uargs);
+  // Up kernel: one 16-token pass (T <= 16), 16-token passes (three CTAs per
+  // SM, T <= 48), or 32-token passes (two CTAs per SM either way, half the
+  // passes).
+  if (ua.T >= kUpPass32MinT) {
+    cudaLaunchConfig_t c2 = pdl_config(dim3(W::UP_CTAS), hc::UpPass<D, KD, 32>::up_bytes(ua.T), st, attr2, W::UCL,
+                                       W::THREADS);
+    return cudaLaunchKernelEx(&c2, hc::hc_up_w_kernel<D, KD, true, 32>, uargs);
+  }
+  cudaLaunchConfig_t c2 = pdl_config(dim3(W::UP_CTAS), hc::UpPass<D, KD, 16>::up_bytes(ua.T), st, attr2, W::UCL,
+                                     W::THREADS);
+  return multi ? cudaLaunchKernelEx(&c2, hc::hc_up_w_kernel<D, KD, true, 16>, uargs)
+               : cudaLaunchKernelEx(&c2, hc::hc_up_w_kernel<D, KD, false, 16>, uargs);
 }
 
 // From T = 2 on the tensor-core kernels are faster on GB300 (measured: T=2

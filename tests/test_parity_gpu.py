@@ -64,7 +64,10 @@ def test_parity_real_geometry(dev, orc, g1, rd1, T, pending):
     assert_parity(o, oracle_read(orc, g, ws, act), T, f"T={T} pending={pending}")
 
 
-@pytest.mark.parametrize("T", [9, 13, 16, 33, 64])
+# Route boundaries of the wide pair: 16/17 (single pass / K-slice ring), 32/33
+# (tokens per staging thread), 44/45 (partials' own region / over the weight
+# tile), 48/49 (16- / 32-token up passes).
+@pytest.mark.parametrize("T", [9, 13, 16, 17, 32, 33, 44, 45, 48, 49, 64])
 def test_parity_token_groups(dev, orc, g1, rd1, T):
     """T > 8 runs in groups of 8 tokens with a ragged last group."""
     g, ws, w = g1
