@@ -427,8 +427,10 @@ __global__ void __launch_bounds__(WGeo<D, KD>::THREADS, 3) hc_down_w1_kernel(con
 }
 
 // ------------------------------------------------------------------ kernel 1, T > 16
-// TT: tokens per staging thread (T <= 16 TT); NPF slices of loads in flight.
-template <int D, int KD, int TT>
+// TT: tokens per staging thread (T <= 16 TT); HASP: the read has a pending
+// write (without it the P loads and their registers go away, and more K
+// slices of R loads fit in flight).
+template <int D, int KD, int TT, bool HASP>
 __global__ void __launch_bounds__(WGeo<D, KD>::THREADS, 3) hc_down_w_kernel(const __grid_constant__ DownUArgs args) {
   using W = WGeo<D, KD>;
   const DownArgs& a = args.a;
@@ -492,10 +494,12 @@ __global__ void __launch_bounds__(WGeo<D, KD>::THREADS, 3) hc_down_w_kernel(cons
   // Thread (tg = tid / 16, c4 = tid % 16) stages tokens tg + 16 m (m < TT)
   // at columns 4 c4 .. 4 c4 + 3 of every K slice: R' = R + P, x = R' * w_norm
   // split into B rows 2 t (hi) and 2 t + 1 (lo), and its share of each
-  // token's sum of squares.  The loads of NPF slices are in flight at once
-  // (all five at T <= 16); a slice's registers are refilled with the loads
-  // of slice j + NPF as soon as it is staged.
-  constexpr int NPF = TT == 1 ? W::NSL_D : TT == 2 ? 2 : 1;  // more would spill at TT = 4
+  // token's sum of squares.  The loads of NPF slices are in flight at once,
+  // as many as the 85 registers of three CTAs per SM hold without spilling
+  // (at TT = 4 two without P, one with it; three at TT = 4 or five at TT = 2
+  // fit too but measured slower); a slice's registers are refilled with the
+  // loads of slice j + NPF as soon as it is staged.
+  constexpr int NPF = TT == 1 ? W::NSL_D : TT == 2 ? (HASP ? 2 : 3) : (HASP ? 1 : 2);
   const int tg = tid >> 4, c4 = tid & 15;
   float4 rv[NPF][TT], pv[NPF][TT], wn[NPF];
   float ssr[TT];
@@ -511,7 +515,7 @@ __global__ void __launch_bounds__(WGeo<D, KD>::THREADS, 3) hc_down_w_kernel(cons
       q[m] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (t < T) {
         r[m] = __ldcg(reinterpret_cast<const float4*>(a.R + (size_t)t * W::N + col));
-        if (a.P) q[m] = __ldcg(reinterpret_cast<const float4*>(a.P + (size_t)t * W::N + col));
+        if (HASP) q[m] = __ldcg(reinterpret_cast<const float4*>(a.P + (size_t)t * W::N + col));
       }
     }
   };
@@ -535,10 +539,12 @@ __global__ void __launch_bounds__(WGeo<D, KD>::THREADS, 3) hc_down_w_kernel(cons
       const int t = tg + 16 * m;
       if (t < T) {
         float4 r = rv[f][m];
-        r.x = __fadd_rn(r.x, pv[f][m].x);
-        r.y = __fadd_rn(r.y, pv[f][m].y);
-        r.z = __fadd_rn(r.z, pv[f][m].z);
-        r.w = __fadd_rn(r.w, pv[f][m].w);
+        if (HASP) {
+          r.x = __fadd_rn(r.x, pv[f][m].x);
+          r.y = __fadd_rn(r.y, pv[f][m].y);
+          r.z = __fadd_rn(r.z, pv[f][m].z);
+          r.w = __fadd_rn(r.w, pv[f][m].w);
+        }
         const float4 w = wn[f];
         const float4 x = make_float4(__fmul_rn(r.x, w.x), __fmul_rn(r.y, w.y), __fmul_rn(r.z, w.z), __fmul_rn(r.w, w.w));
         uint2 hi, lo;

@@ -173,9 +173,13 @@ cudaError_t configure_wide() {
   cudaError_t e;
   if ((e = cudaFuncSetAttribute(hc::hc_down_w1_kernel<D, KD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 W::d1_bytes(W::TP))) != cudaSuccess ||
-      (e = cudaFuncSetAttribute(hc::hc_down_w_kernel<D, KD, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      (e = cudaFuncSetAttribute(hc::hc_down_w_kernel<D, KD, 2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 W::DN_BYTES_MAX)) != cudaSuccess ||
-      (e = cudaFuncSetAttribute(hc::hc_down_w_kernel<D, KD, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      (e = cudaFuncSetAttribute(hc::hc_down_w_kernel<D, KD, 2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                W::DN_BYTES_MAX)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(hc::hc_down_w_kernel<D, KD, 4, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                W::DN_BYTES_MAX)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(hc::hc_down_w_kernel<D, KD, 4, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 W::DN_BYTES_MAX)) != cudaSuccess)
     return e;
   using P16 = hc::UpPass<D, KD, 16>;
@@ -306,9 +310,12 @@ cudaError_t launch_pair_w(const DownArgs& da, const UpArgs& ua, const CUtensorMa
   // the K-slice ring), above it the ring with 2 or 4 tokens per staging
   // thread (8-10 % faster at T = 17..48 than 16-token passes).
   if (da.T <= W::TP) c1.dynamicSmemBytes = W::d1_bytes(da.T);
+  const bool hasp = da.P != nullptr;
   cudaError_t e = da.T <= W::TP ? cudaLaunchKernelEx(&c1, hc::hc_down_w1_kernel<D, KD>, dargs)
-                  : da.T <= 32  ? cudaLaunchKernelEx(&c1, hc::hc_down_w_kernel<D, KD, 2>, dargs)
-                                : cudaLaunchKernelEx(&c1, hc::hc_down_w_kernel<D, KD, 4>, dargs);
+                  : da.T <= 32  ? (hasp ? cudaLaunchKernelEx(&c1, hc::hc_down_w_kernel<D, KD, 2, true>, dargs)
+                                        : cudaLaunchKernelEx(&c1, hc::hc_down_w_kernel<D, KD, 2, false>, dargs))
+                  : hasp        ? cudaLaunchKernelEx(&c1, hc::hc_down_w_kernel<D, KD, 4, true>, dargs)
+                                : cudaLaunchKernelEx(&c1, hc::hc_down_w_kernel<D, KD, 4, false>, dargs);
   if (e != cudaSuccess) return e;
   hc::UpWArgs uargs;
   uargs.w = w_up;

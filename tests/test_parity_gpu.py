@@ -67,16 +67,18 @@ def test_parity_real_geometry(dev, orc, g1, rd1, T, pending):
 # Route boundaries of the wide pair: 16/17 (single pass / K-slice ring), 32/33
 # (tokens per staging thread), 44/45 (partials' own region / over the weight
 # tile), 48/49 (16- / 32-token up passes).
+# Pending off and on take different down kernels above 16 tokens.
+@pytest.mark.parametrize("pending", [False, True], ids=["pend_off", "pend_on"])
 @pytest.mark.parametrize("T", [9, 13, 16, 17, 32, 33, 44, 45, 48, 49, 64])
-def test_parity_token_groups(dev, orc, g1, rd1, T):
-    """T > 8 runs in groups of 8 tokens with a ragged last group."""
+def test_parity_token_groups(dev, orc, g1, rd1, T, pending):
+    """T >= 9: the wide tensor-memory pair, tokens in passes with a ragged last one."""
     g, ws, w = g1
-    act = synth.activations(g, T, True, s0=200 + T)
+    act = synth.activations(g, T, pending, s0=200 + T)
     a = dev_act(act, dev)
     o = outputs(g, T, dev)
     run(rd1, w, a, T, o)
     torch.cuda.synchronize()
-    assert_parity(o, oracle_read(orc, g, ws, act), T, f"T={T}")
+    assert_parity(o, oracle_read(orc, g, ws, act), T, f"T={T} pending={pending}")
 
 
 @pytest.mark.parametrize("T", [1, 5, 8, 12])
