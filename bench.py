@@ -285,7 +285,7 @@ class Sweep:
     hc_read call per read on the stream, all into one set of output buffers."""
 
     def __init__(self, hc, torch, dev, g: synth.Geometry, Ts, pendings, sets: int, calls: int,
-                 stream, batch: bool = True, q8: bool = False):
+                 stream, batch: bool = True, q8: bool = False, down_tiles: bool = False):
         self.g, self.calls, self.batch, self.q8 = g, calls, batch, q8
         self.torch, self.hc, self.dev, self.stream = torch, hc, dev, stream
         Tmax = max(Ts)
@@ -316,6 +316,9 @@ class Sweep:
                 blk["P"] = torch.from_numpy(a.P).to(dev).unsqueeze(0).repeat(calls, 1, 1).contiguous()
             self.act[T] = blk
         self.rd = hc.Read(g.n, g.d, g.K, T_max=max(8, Tmax), eps=EPS)
+        # down_tiles: every weight set's W_down also in tile order, registered
+        # with the handle before capture (hc_read_register_down_tiles).
+        self.tiles = [self.rd.down_tiles(w["W_down"]) for w in self.ws] if down_tiles else []
         self.cases = [(T, p) for T in Ts for p in pendings]
         self.graphs = {}
         for case in self.cases:
@@ -752,6 +755,26 @@ def run_gpu(args):
         extra["wide_d4096_K512_pend"] = {f"T{T}": {"us_per_read": 1e6 * pc[(T, p)] / (5 * CALLS),
                                                    "GBps": read_bytes(g2, T, p) * 5 * CALLS / pc[(T, p)] / 1e9}
                                          for (T, p) in wide.cases}
+        wide.close()
+        # The same sweeps with every W_down also in tile order (bit-identical
+        # reads; the 32-row-tile down kernels copy one block per CTA).
+        tl = Sweep(hc, torch, dev, g, SWEEP_T, (False, True), SETS, CALLS, stream, down_tiles=True)
+        tt, pc = time_cases(torch, tl, 5, 3, stream)
+        extra["sweep_down_tiles"] = {
+            "note": "the sweep with each weight set's W_down registered in tile order "
+                    "(hc_read_register_down_tiles); T <= 4 take the tiles, T >= 5 read W_down itself",
+            "us_per_read": {f"T{T}_{'pend' if p else 'nopend'}": 1e6 * pc[(T, p)] / (5 * CALLS)
+                            for (T, p) in tl.cases},
+            "frac_of_measured_hbm": {f"T{T}_{'pend' if p else 'nopend'}":
+                                     read_bytes(g, T, p) * 5 * CALLS / pc[(T, p)] / 1e9 / hbm
+                                     for (T, p) in tl.cases},
+            "GBps": sum(tl.bytes_per_replay(c) for c in tl.cases) * 5 / tt / 1e9}
+        tl.close()
+        wide = Sweep(hc, torch, dev, g2, SWEEP_T, (True,), 12, CALLS, stream, down_tiles=True)
+        tw, pc = time_cases(torch, wide, 5, 3, stream)
+        extra["wide_d4096_K512_pend_down_tiles"] = {
+            f"T{T}": {"us_per_read": 1e6 * pc[(T, p)] / (5 * CALLS),
+                      "GBps": read_bytes(g2, T, p) * 5 * CALLS / pc[(T, p)] / 1e9} for (T, p) in wide.cases}
         wide.close()
 
     if rank != 0:

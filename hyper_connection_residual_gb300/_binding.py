@@ -27,6 +27,7 @@ EXPORTS = (
     "hc_read_batch_q8", "hc_read_batch_q8_plan", "hc_read_batch_q8_groups",
     "hc_q2_0_matvec", "hc_q2_0_matvec_batch", "hc_q2_0_matvec_batch_plan",
     "hc_read_set_wait_limit", "hc_read_set_overlap", "hc_read_noalloc_check",
+    "hc_read_down_tiles_bytes", "hc_read_register_down_tiles", "hc_read_forget_down_tiles",
 )
 
 
@@ -136,6 +137,12 @@ def load(path: str | None = None):
     lib.hc_read_set_wait_limit.argtypes = [_vp, ctypes.c_uint64]
     lib.hc_read_set_overlap.restype = ctypes.c_int
     lib.hc_read_set_overlap.argtypes = [_vp, ctypes.c_int]
+    lib.hc_read_down_tiles_bytes.restype = ctypes.c_int64
+    lib.hc_read_down_tiles_bytes.argtypes = [_vp]
+    lib.hc_read_register_down_tiles.restype = ctypes.c_int
+    lib.hc_read_register_down_tiles.argtypes = [_vp, _vp, _vp, _vp]
+    lib.hc_read_forget_down_tiles.restype = ctypes.c_int
+    lib.hc_read_forget_down_tiles.argtypes = [_vp, _vp]
     lib.hc_read_noalloc_check.restype = ctypes.c_int
     lib.hc_read_noalloc_check.argtypes = []
     if path is None:
@@ -342,6 +349,30 @@ def hc_read_set_overlap(h: int, enabled: bool) -> bool:
     return st == 1
 
 
+def hc_read_down_tiles_bytes(h: int) -> int:
+    """Bytes of the tile-ordered copy of a W_down for the handle's geometry."""
+    n = load().hc_read_down_tiles_bytes(h)
+    if n < 0:
+        _check(int(n), "hc_read_down_tiles_bytes")
+    return int(n)
+
+
+def hc_read_register_down_tiles(h: int, geometry, W_down, tiles, stream=None) -> None:
+    """Write W_down in tile order into ``tiles`` and register the pair with
+    the handle (see include/hc_read.h); returns when the copy is done."""
+    n, d, K = geometry
+    nbytes = hc_read_down_tiles_bytes(h)
+    _check(load().hc_read_register_down_tiles(
+        h, _ptr(W_down, "W_down", _BF16, K * n * d), _ptr(tiles, "tiles", _BF16, nbytes // 2),
+        _stream_ptr(stream)), "hc_read_register_down_tiles")
+
+
+def hc_read_forget_down_tiles(h: int, W_down=None) -> None:
+    """Drop the handle's tile-ordered copy of W_down (all of them for None)."""
+    _check(load().hc_read_forget_down_tiles(h, _ptr(W_down, "W_down", _BF16, None)),
+           "hc_read_forget_down_tiles")
+
+
 def _descs(geometry, reads, T: int):
     """hc_read_desc array of a list of reads (tensors checked; ints pass as addresses)."""
     n, d, K = geometry
@@ -535,6 +566,18 @@ class Read:
 
     def set_overlap(self, enabled: bool) -> bool:
         return hc_read_set_overlap(self.h, enabled)
+
+    def down_tiles(self, W_down, stream=None):
+        """A tile-ordered copy of W_down, registered with this handle: later
+        reads with this W_down take their down weights from it (bit-identical
+        results).  The returned tensor must stay alive while registered."""
+        import torch
+        tiles = torch.empty(hc_read_down_tiles_bytes(self.h) // 2, dtype=torch.int16, device=W_down.device)
+        hc_read_register_down_tiles(self.h, self.geometry, W_down, tiles, stream)
+        return tiles
+
+    def forget_down_tiles(self, W_down=None) -> None:
+        hc_read_forget_down_tiles(self.h, W_down)
 
     def error_word(self) -> int:
         return hc_read_error_word(self.h)

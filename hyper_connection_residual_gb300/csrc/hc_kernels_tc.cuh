@@ -258,13 +258,18 @@ __global__ void __launch_bounds__(kThreads, tc_min_blocks<D, NT>()) hc_down_tc_k
     if (lane == 0) {
       ptx::mbar_init(bar_w, 1);
       ptx::fence_barrier_init();
-      ptx::mbar_arrive_expect_tx(bar_w, G::DN_ROWS * WROW);
+      ptx::mbar_arrive_expect_tx(bar_w, (!Q8 && a.W_tiles) ? G::DN_ROWS * S::WPITCH : G::DN_ROWS * WROW);
     }
     __syncwarp();
     const uint64_t once = ptx::policy_evict_first();
-    const void* src = Q8 ? static_cast<const void*>(a.Wq + (size_t)(row0 + lane) * G::N + col0)
-                         : static_cast<const void*>(a.W_down + (size_t)(row0 + lane) * G::N + col0);
-    ptx::bulk_g2s(w_s + lane * S::WPITCH + S::Q8_OFF, src, WROW, bar_w, once);
+    if (Q8 || a.W_tiles == nullptr) {
+      const void* src = Q8 ? static_cast<const void*>(a.Wq + (size_t)(row0 + lane) * G::N + col0)
+                           : static_cast<const void*>(a.W_down + (size_t)(row0 + lane) * G::N + col0);
+      ptx::bulk_g2s(w_s + lane * S::WPITCH + S::Q8_OFF, src, WROW, bar_w, once);
+    } else if (lane < kTileCopies) {
+      static_assert(Q8 || S::WPITCH == G::DN_PITCH, "BF16 tiles at the tile order's pitch");
+      copy_down_tile<G>(w_s, a.W_tiles, rg, slab, lane, bar_w, once);
+    }
   }
   if constexpr (Q8) {
     // The slab's block scales of the CTA's 32 rows (binary16), copied

@@ -11,6 +11,7 @@
 #include <mutex>
 #include <new>
 #include <numeric>
+#include <unordered_map>
 #include <vector>
 
 #include "hc_kernels.cuh"
@@ -72,6 +73,8 @@ struct hc_read_s {
     int parity;
   } lanes[kBatchLanes];
   MapCache* map_cache;  // created on first use
+  // W_down -> its tile-ordered copy (hc_read_register_down_tiles); created on first use.
+  std::unordered_map<const void*, const void*>* down_tiles;
   unsigned long long wait_ns;  // limit of the down kernels' first bulk-copy wait (0: the default)
   bool overlap;       // reads may overlap their predecessor (independent mode), hc_read_set_overlap
   int nlanes;         // lanes created (0: batches run on the caller's stream only)
@@ -141,9 +144,12 @@ cudaLaunchConfig_t pdl_config(dim3 grid, size_t smem, cudaStream_t st, cudaLaunc
 
 template <int D, int KD, int TT>
 cudaError_t configure_one() {
-  cudaError_t e = cudaFuncSetAttribute(hc::hc_down_kernel<D, KD, TT>,
+  cudaError_t e = cudaFuncSetAttribute(hc::hc_down_kernel<D, KD, TT, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        hc::DownSmem<D, KD, TT>::BYTES_MAX);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(hc::hc_down_kernel<D, KD, TT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           hc::DownSmem<D, KD, TT>::BYTES_MAX);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(hc::hc_up_kernel<D, KD, TT>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -215,7 +221,8 @@ cudaError_t launch_pair(const DownArgs& da, const UpArgs& ua, cudaStream_t st) {
   cudaLaunchConfig_t c1 = pdl_config(dim3(G::SLABS, G::ROW_GROUPS),
                                       hc::DownSmem<D, KD, TT>::bytes(da.T), st, attr,
                                       G::SLABS_PER_STREAM);
-  cudaError_t e = cudaLaunchKernelEx(&c1, hc::hc_down_kernel<D, KD, TT>, da);
+  cudaError_t e = da.W_tiles ? cudaLaunchKernelEx(&c1, hc::hc_down_kernel<D, KD, TT, true>, da)
+                             : cudaLaunchKernelEx(&c1, hc::hc_down_kernel<D, KD, TT, false>, da);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr2[2];
   cudaLaunchConfig_t c2 = pdl_config(dim3(G::UP_CTAS), hc::UpSmem<D, KD, TT>::bytes(ua.T), st,
@@ -673,6 +680,27 @@ const CUtensorMap* up_map_for(hc_read_t h, const ReadDesc& q, int T) {
   return weight_map(h, 1, q.W_up);
 }
 
+// The tile-ordered copy registered for a W_down, or null.
+const void* down_tiles_for(hc_read_t h, const void* W_down) {
+  if (h->down_tiles == nullptr) return nullptr;
+  const auto it = h->down_tiles->find(W_down);
+  return it == h->down_tiles->end() ? nullptr : it->second;
+}
+
+template <int D, int KD>
+constexpr size_t down_tiles_bytes() {
+  using G = hc::Geo<D, KD>;
+  return (size_t)G::ROW_GROUPS * G::SLABS * G::DN_ROWS * G::DN_PITCH;
+}
+
+template <int D, int KD>
+cudaError_t launch_pack_down_tiles(const void* W_down, void* tiles, cudaStream_t st) {
+  using G = hc::Geo<D, KD>;
+  hc::hc_pack_down_tiles_kernel<D, KD><<<dim3(G::SLABS, G::ROW_GROUPS), hc::kThreads, 0, st>>>(
+      static_cast<const uint16_t*>(W_down), static_cast<uint16_t*>(tiles));
+  return cudaGetLastError();
+}
+
 // Enqueues one validated read on `st` with partial-sum slot `part` (the two
 // kernels of the read; the caller alternates between its two slots).
 int enqueue_read(hc_read_t h, float* part, int device, const ReadDesc& q, int T, float* r_out, float* rs,
@@ -690,6 +718,7 @@ int enqueue_read(hc_read_t h, float* part, int device, const ReadDesc& q, int T,
   da.P = q.pending;
   da.w_norm = q.w_norm;
   da.W_down = q.W_down;
+  da.W_tiles = q.is_q8() ? nullptr : down_tiles_for(h, q.W_down);
   da.Wq = q.q8.Wd_q;
   da.Wscale = q.q8.Wd_scale;
   da.part = part;
@@ -1119,6 +1148,7 @@ HC_EXPORT void hc_read_destroy(hc_read_t h) {
     cudaSetDevice(prev);
   }
   delete h->map_cache;
+  delete h->down_tiles;
   delete h;
 }
 
@@ -1133,6 +1163,53 @@ HC_EXPORT int hc_read_set_overlap(hc_read_t h, int enabled) {
   const int prev = h->overlap ? 1 : 0;
   h->overlap = enabled != 0;
   return prev;
+}
+
+HC_EXPORT int64_t hc_read_down_tiles_bytes(hc_read_t h) {
+  if (h == nullptr) return -1;
+  return static_cast<int64_t>(h->d == 2560 ? down_tiles_bytes<2560, 320>() : down_tiles_bytes<4096, 512>());
+}
+
+HC_EXPORT int hc_read_register_down_tiles(hc_read_t h, const void* W_down, void* tiles, hc_stream_t stream) {
+  if (h == nullptr || W_down == nullptr || tiles == nullptr) return HC_ERR_ARG;
+  if (!aligned16(W_down) || !aligned16(tiles)) return HC_ERR_ALIGN;
+  const size_t bytes = static_cast<size_t>(hc_read_down_tiles_bytes(h));
+  if (overlaps(range_of(W_down, (size_t)h->K * h->n * h->d * 2), range_of(tiles, bytes))) return HC_ERR_ARG;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return HC_ERR_CUDA;
+  if (cur != h->device) return HC_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // The copy completes before this returns: a read enqueued later may load
+  // its weights before it waits for the kernels ahead of it.
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return HC_ERR_CUDA;
+  if (cs != cudaStreamCaptureStatusNone) return HC_ERR_ARG;
+  cudaError_t e = h->d == 2560 ? launch_pack_down_tiles<2560, 320>(W_down, tiles, st)
+                               : launch_pack_down_tiles<4096, 512>(W_down, tiles, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return HC_ERR_CUDA;
+  }
+  try {
+    if (h->down_tiles == nullptr) h->down_tiles = new std::unordered_map<const void*, const void*>();
+    (*h->down_tiles)[W_down] = tiles;
+  } catch (...) {
+    return HC_ERR_CUDA;
+  }
+  return HC_OK;
+}
+
+HC_EXPORT int hc_read_forget_down_tiles(hc_read_t h, const void* W_down) {
+  if (h == nullptr) return HC_ERR_ARG;
+  if (h->down_tiles != nullptr) {
+    if (W_down == nullptr) {
+      h->down_tiles->clear();
+    } else {
+      h->down_tiles->erase(W_down);
+    }
+  }
+  return HC_OK;
 }
 
 HC_EXPORT int64_t hc_read_scratch_bytes(hc_read_t h) {

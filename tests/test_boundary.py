@@ -66,6 +66,9 @@ def test_null_handle_rejected(lib):
     assert lib.hc_read_q8(None, *([None] * 8), 1, *([None] * 6)) == hc.HC_ERR_ARG
     assert lib.hc_read_set_wait_limit(None, 5) == hc.HC_ERR_ARG
     assert lib.hc_read_set_overlap(None, 1) == hc.HC_ERR_ARG
+    assert lib.hc_read_down_tiles_bytes(None) == -1
+    assert lib.hc_read_register_down_tiles(None, None, None, None) == hc.HC_ERR_ARG
+    assert lib.hc_read_forget_down_tiles(None, None) == hc.HC_ERR_ARG
 
 
 def test_q2_matvec_rejects_bad_arguments(lib):
