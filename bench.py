@@ -307,18 +307,21 @@ class Sweep:
                 w_norm=torch.from_numpy(w.w_norm).to(dev), gate=torch.from_numpy(w.gate).to(dev),
                 W_down=torch.from_numpy(w.W_down.view(np.int16)).to(dev),
                 W_up=torch.from_numpy(w.W_up.view(np.int16)).to(dev)))
-        # One activation draw per T, copied into every read's own buffers.
+        # One activation draw per T, copied into every read's own buffers; each
+        # case has its own buffers (the end-to-end leg refills one case's
+        # inputs while another case runs).
         self.act = {}
         nout = calls if batch else 1
         for T in sorted(set(Ts)):
             a = synth.activations(g, T, True)
             R1 = torch.from_numpy(a.R).to(dev)
-            blk = dict(R=R1.unsqueeze(0).repeat(calls, 1, 1).contiguous(),
-                       out=torch.empty(nout, T, g.N, device=dev), mean=torch.empty(nout, T, g.d, device=dev),
-                       lo=torch.empty(nout, T, g.K, device=dev))
-            if True in pendings:
-                blk["P"] = torch.from_numpy(a.P).to(dev).unsqueeze(0).repeat(calls, 1, 1).contiguous()
-            self.act[T] = blk
+            for p in pendings:
+                blk = dict(R=R1.unsqueeze(0).repeat(calls, 1, 1).contiguous(),
+                           out=torch.empty(nout, T, g.N, device=dev), mean=torch.empty(nout, T, g.d, device=dev),
+                           lo=torch.empty(nout, T, g.K, device=dev))
+                if p:
+                    blk["P"] = torch.from_numpy(a.P).to(dev).unsqueeze(0).repeat(calls, 1, 1).contiguous()
+                self.act[(T, p)] = blk
         self.rd = hc.Read(g.n, g.d, g.K, T_max=max(8, Tmax), eps=EPS)
         # down_tiles: every weight set's W_down also in tile order, registered
         # with the handle before capture (hc_read_register_down_tiles).
@@ -329,7 +332,7 @@ class Sweep:
             self.graphs[case] = self._capture(*case)
 
     def _desc(self, T, pending, j):
-        a = self.act[T]
+        a = self.act[(T, pending)]
         o = j if self.batch else 0
         return dict(R=a["R"][j], P=a["P"][j] if pending else None, out=a["out"][o], mean=a["mean"][o],
                     lo=a["lo"][o], **self.ws[j % len(self.ws)])
@@ -356,9 +359,9 @@ class Sweep:
         descs = [self._desc(T, pending, j) for j in range(self.calls)]
         return (self.rd.batch_q8_plan if self.q8 else self.rd.batch_plan)(descs, T)
 
-    def block(self, T):
-        """The case's device buffers: R, P, out, mean, lo, each [calls][T][...]."""
-        return self.act[T]
+    def block(self, case):
+        """The case's device buffers: R, (P), out, mean, lo, each [calls][T][...]."""
+        return self.act[case]
 
     def replay(self, case):
         self.hc.hc_graph_launch(self.graphs[case], self.stream)
@@ -676,33 +679,51 @@ def run_gpu(args):
                     for (T, p) in sweep.cases}
 
     # ---- end to end: every read's R (and P) in from pinned host memory and
-    # every read's out and mean back, every step
+    # every read's out and mean back, every step.  As a serving loop would:
+    # host-to-device copies on one stream, the reads on the compute stream,
+    # device-to-host copies on a third, ordered per case by events, so that a
+    # case's inputs arrive while the case before it runs.
     host = {}
-    for T in SWEEP_T:
-        b = sweep.block(T)
-        host[T] = {k: torch.empty(b[k].shape, dtype=b[k].dtype).pin_memory() for k in ("R", "P", "out", "mean")}
-        host[T]["R"].copy_(b["R"])
-        host[T]["P"].copy_(b["P"])
+    for case in sweep.cases:
+        b = sweep.block(case)
+        host[case] = {k: torch.empty(b[k].shape, dtype=b[k].dtype).pin_memory()
+                      for k in ("R", "P", "out", "mean") if k in b}
+        host[case]["R"].copy_(b["R"])
+        if "P" in b:
+            host[case]["P"].copy_(b["P"])
     h2d = sum(calls * T * g.N * 4 * (2 if p else 1) for (T, p) in sweep.cases)
     d2h = sum(calls * T * (g.N + g.d) * 4 for (T, p) in sweep.cases)
     e2e_steps = max(3, min(args.steps, 20))
+    up_st = torch.cuda.Stream(device=dev)
+    down_st = torch.cuda.Stream(device=dev)
+    ev = {c: {k: torch.cuda.Event() for k in ("in", "run", "out")} for c in sweep.cases}
     if pg:
         pg.barrier()
     torch.cuda.synchronize()
     ea = torch.cuda.Event(enable_timing=True)
     eb = torch.cuda.Event(enable_timing=True)
     ea.record(stream)
+    up_st.wait_event(ea)
     for _ in range(e2e_steps):
-        for (T, p) in sweep.cases:
-            b, hb = sweep.block(T), host[T]
-            with torch.cuda.stream(stream):
+        for case in sweep.cases:
+            b, hb, e = sweep.block(case), host[case], ev[case]
+            up_st.wait_event(e["run"])      # the case's previous run has read its inputs
+            with torch.cuda.stream(up_st):
                 b["R"].copy_(hb["R"], non_blocking=True)
-                if p:
+                if "P" in b:
                     b["P"].copy_(hb["P"], non_blocking=True)
-            sweep.replay((T, p))
-            with torch.cuda.stream(stream):
+            e["in"].record(up_st)
+            stream.wait_event(e["in"])
+            stream.wait_event(e["out"])     # the case's previous outputs are back on the host
+            sweep.replay(case)
+            e["run"].record(stream)
+            down_st.wait_event(e["run"])
+            with torch.cuda.stream(down_st):
                 hb["out"].copy_(b["out"], non_blocking=True)
                 hb["mean"].copy_(b["mean"], non_blocking=True)
+            e["out"].record(down_st)
+    stream.wait_stream(up_st)
+    stream.wait_stream(down_st)
     eb.record(stream)
     eb.synchronize()
     e2e_sec = ea.elapsed_time(eb) / 1e3
@@ -833,7 +854,9 @@ def run_gpu(args):
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "note": "per step, every read's own R (and P) copied in from pinned host memory and "
-                        "every read's out and mean copied back, around the same graph replays"},
+                        "every read's out and mean copied back, around the same graph replays; copies in, "
+                        "reads and copies out on three streams ordered per case by events, so one case's "
+                        "copies overlap another case's reads"},
         "gpu_launches": 2 * calls * len(sweep_cases()) * args.steps,
         "clocks": clocks.summary(),
         "extra": extra,
