@@ -7,10 +7,11 @@ independent reads rotated over 16 weight sets (16 x 13.1 MB > the 129 MB L2),
 each with its own output buffers, enqueued as one hc_read_batch (the library
 runs reads that share no memory side by side on its internal streams), each
 case captured once as a CUDA graph and replayed.  Before capture, every
-weight set's W_down is also registered in tile order with the handle
-(hc_read_register_down_tiles, a one-time setup outside the timed region):
-reads with T <= 4 fetch their down weights from it, with results bit for bit
-those of W_down as given, whose sweep is reported too.  `value` is the algorithmic
+weight set's W_down and W_up are also registered in tile order with the
+handle (hc_read_register_down_tiles / _up_tiles, a one-time setup outside
+the timed region): the kernels fetch their weight tiles from them, with
+results bit for bit those of the weights as given, whose sweep is reported
+too.  `value` is the algorithmic
 bytes of every read of the step divided by the step time (GB/s, higher is
 better); `us_per_read` gives the per-case times.
 
@@ -289,7 +290,7 @@ class Sweep:
     hc_read call per read on the stream, all into one set of output buffers."""
 
     def __init__(self, hc, torch, dev, g: synth.Geometry, Ts, pendings, sets: int, calls: int,
-                 stream, batch: bool = True, q8: bool = False, down_tiles: bool = False):
+                 stream, batch: bool = True, q8: bool = False, tiles: bool = False):
         self.g, self.calls, self.batch, self.q8 = g, calls, batch, q8
         self.torch, self.hc, self.dev, self.stream = torch, hc, dev, stream
         Tmax = max(Ts)
@@ -323,9 +324,14 @@ class Sweep:
                     blk["P"] = torch.from_numpy(a.P).to(dev).unsqueeze(0).repeat(calls, 1, 1).contiguous()
                 self.act[(T, p)] = blk
         self.rd = hc.Read(g.n, g.d, g.K, T_max=max(8, Tmax), eps=EPS)
-        # down_tiles: every weight set's W_down also in tile order, registered
-        # with the handle before capture (hc_read_register_down_tiles).
-        self.tiles = [self.rd.down_tiles(w["W_down"]) for w in self.ws] if down_tiles else []
+        # tiles: every weight set's W_down and W_up also in tile order,
+        # registered with the handle before capture (hc_read_register_down_tiles,
+        # hc_read_register_up_tiles; no up tiles where no kernel takes them).
+        self.tiles = []
+        if tiles:
+            for w in self.ws:
+                self.tiles.append(self.rd.down_tiles(w["W_down"]))
+                self.tiles.append(self.rd.up_tiles(w["W_up"]))
         self.cases = [(T, p) for T in Ts for p in pendings]
         self.graphs = {}
         for case in self.cases:
@@ -477,7 +483,7 @@ def run_profile_case():
     lo = torch.empty(8, g.K, device=dev)
     flush = torch.empty(64 * 1024 * 1024, device=dev)
     with hc.Read(g.n, g.d, g.K, T_max=8, eps=EPS) as rd:
-        tiles = [rd.down_tiles(w["W_down"]) for w in ws]  # as the headline sweep
+        tiles = [rd.down_tiles(w["W_down"]) for w in ws] + [rd.up_tiles(w["W_up"]) for w in ws]  # as the headline
         for T in (1, 8):
             for w in ws:
                 flush.zero_()
@@ -657,7 +663,7 @@ def run_gpu(args):
     stream = torch.cuda.Stream(device=dev)
     g = synth.G1
     calls = args.calls
-    sweep = Sweep(hc, torch, dev, g, SWEEP_T, (False, True), SETS, calls, stream, down_tiles=True)
+    sweep = Sweep(hc, torch, dev, g, SWEEP_T, (False, True), SETS, calls, stream, tiles=True)
     step_bytes = sum(sweep.bytes_per_replay(c) for c in sweep.cases)
     plans = {sweep.plan(c) for c in sweep.cases}
 
@@ -735,7 +741,7 @@ def run_gpu(args):
     extra = {}
     if not args.quick:
         single = Sweep(hc, torch, dev, g, SWEEP_T, (False, True), SETS, calls, stream, batch=False,
-                       down_tiles=True)
+                       tiles=True)
         ts, pc = time_cases(torch, single, 5, 3, stream)
         extra["sweep_one_stream_per_call"] = {
             "note": "the same 300 reads per case as hc_read calls on one stream, one set of outputs",
@@ -745,12 +751,13 @@ def run_gpu(args):
         single.close()
         extra["window_96_reads_T4"] = run_window(torch, hc, dev, stream, replays=100, batch=True)
         extra["window_96_reads_T4_per_call"] = run_window(torch, hc, dev, stream, replays=20, batch=False)
-        big = Sweep(hc, torch, dev, g, (16, 32, 64), (False,), SETS, CALLS, stream)
-        tb, pc = time_cases(torch, big, 5, 3, stream)
-        extra["batch_T16_32_64"] = {f"T{T}": {"us_per_read": 1e6 * pc[(T, p)] / (5 * CALLS),
-                                              "GBps": read_bytes(g, T, p) * 5 * CALLS / pc[(T, p)] / 1e9}
-                                    for (T, p) in big.cases}
-        big.close()
+        for key, tl in (("batch_T16_32_64", True), ("batch_T16_32_64_weights_as_given", False)):
+            big = Sweep(hc, torch, dev, g, (16, 32, 64), (False,), SETS, CALLS, stream, tiles=tl)
+            tb, pc = time_cases(torch, big, 5, 3, stream)
+            extra[key] = {f"T{T}": {"us_per_read": 1e6 * pc[(T, p)] / (5 * CALLS),
+                                    "GBps": read_bytes(g, T, p) * 5 * CALLS / pc[(T, p)] / 1e9}
+                          for (T, p) in big.cases}
+            big.close()
         q8 = Sweep(hc, torch, dev, g, SWEEP_T, (False, True), SETS, CALLS, stream, q8=True)
         tq, pc = time_cases(torch, q8, 5, 3, stream)
         extra["q8_0_sweep"] = {
@@ -788,9 +795,9 @@ def run_gpu(args):
         # and the scaled-up width with them (every T there takes them).
         tl = Sweep(hc, torch, dev, g, SWEEP_T, (False, True), SETS, CALLS, stream)
         tt, pc = time_cases(torch, tl, 5, 3, stream)
-        extra["sweep_w_down_as_given"] = {
-            "note": "the headline sweep with no tile-ordered W_down registered: every down kernel "
-                    "fetches its tile from W_down [K][N] row segment by row segment",
+        extra["sweep_weights_as_given"] = {
+            "note": "the headline sweep with no tile-ordered weights registered: every kernel "
+                    "fetches its tiles from W_down [K][N] and W_up [N][K] themselves",
             "us_per_read": {f"T{T}_{'pend' if p else 'nopend'}": 1e6 * pc[(T, p)] / (5 * CALLS)
                             for (T, p) in tl.cases},
             "frac_of_measured_hbm": {f"T{T}_{'pend' if p else 'nopend'}":
@@ -798,7 +805,7 @@ def run_gpu(args):
                                      for (T, p) in tl.cases},
             "GBps": sum(tl.bytes_per_replay(c) for c in tl.cases) * 5 / tt / 1e9}
         tl.close()
-        wide = Sweep(hc, torch, dev, g2, SWEEP_T, (True,), 12, CALLS, stream, down_tiles=True)
+        wide = Sweep(hc, torch, dev, g2, SWEEP_T, (True,), 12, CALLS, stream, tiles=True)
         tw, pc = time_cases(torch, wide, 5, 3, stream)
         extra["wide_d4096_K512_pend_down_tiles"] = {
             f"T{T}": {"us_per_read": 1e6 * pc[(T, p)] / (5 * CALLS),
@@ -842,10 +849,11 @@ def run_gpu(args):
                                "pending write off and on, 300 independent reads per case rotated over "
                                "16 weight sets, own inputs and outputs per read, one hc_read_batch per "
                                "case, CUDA-graph replay",
-                   "w_down_layout": "each weight set's W_down also registered in tile order with the "
-                                    "handle before capture (hc_read_register_down_tiles, outside the "
-                                    "timed region): reads with T <= 4 fetch their down weights from it, "
-                                    "bit-identical to W_down as given (extra.sweep_w_down_as_given)",
+                   "weight_layout": "each weight set's W_down and W_up also registered in tile order "
+                                    "with the handle before capture (hc_read_register_down_tiles, "
+                                    "hc_read_register_up_tiles; outside the timed region): the kernels "
+                                    "fetch their tiles from it, bit-identical to the weights as given "
+                                    "(extra.sweep_weights_as_given)",
                    "batch_plan": sorted(plans),
                    "l2": "inputs larger than L2 (16 x 13.1 MB weight sets rotated)",
                    "parallelism": f"replicas x{world}"},

@@ -48,6 +48,9 @@ from ._binding import (  # noqa: F401
     hc_read_down_tiles_bytes,
     hc_read_register_down_tiles,
     hc_read_forget_down_tiles,
+    hc_read_up_tiles_bytes,
+    hc_read_register_up_tiles,
+    hc_read_forget_up_tiles,
     hc_read_set_wait_limit,
     hc_read_reset,
     hc_read_scratch_bytes,

@@ -28,6 +28,7 @@ EXPORTS = (
     "hc_q2_0_matvec", "hc_q2_0_matvec_batch", "hc_q2_0_matvec_batch_plan",
     "hc_read_set_wait_limit", "hc_read_set_overlap", "hc_read_noalloc_check",
     "hc_read_down_tiles_bytes", "hc_read_register_down_tiles", "hc_read_forget_down_tiles",
+    "hc_read_up_tiles_bytes", "hc_read_register_up_tiles", "hc_read_forget_up_tiles",
 )
 
 
@@ -143,6 +144,12 @@ def load(path: str | None = None):
     lib.hc_read_register_down_tiles.argtypes = [_vp, _vp, _vp, _vp]
     lib.hc_read_forget_down_tiles.restype = ctypes.c_int
     lib.hc_read_forget_down_tiles.argtypes = [_vp, _vp]
+    lib.hc_read_up_tiles_bytes.restype = ctypes.c_int64
+    lib.hc_read_up_tiles_bytes.argtypes = [_vp]
+    lib.hc_read_register_up_tiles.restype = ctypes.c_int
+    lib.hc_read_register_up_tiles.argtypes = [_vp, _vp, _vp, _vp]
+    lib.hc_read_forget_up_tiles.restype = ctypes.c_int
+    lib.hc_read_forget_up_tiles.argtypes = [_vp, _vp]
     lib.hc_read_noalloc_check.restype = ctypes.c_int
     lib.hc_read_noalloc_check.argtypes = []
     if path is None:
@@ -373,6 +380,29 @@ def hc_read_forget_down_tiles(h: int, W_down=None) -> None:
            "hc_read_forget_down_tiles")
 
 
+def hc_read_up_tiles_bytes(h: int) -> int:
+    """Bytes of the tile-ordered copy of a W_up for the handle's geometry (0: none taken)."""
+    n = load().hc_read_up_tiles_bytes(h)
+    if n < 0:
+        _check(int(n), "hc_read_up_tiles_bytes")
+    return int(n)
+
+
+def hc_read_register_up_tiles(h: int, geometry, W_up, tiles, stream=None) -> None:
+    """Write W_up in tile order into ``tiles`` and register the pair with the
+    handle (see include/hc_read.h); returns when the copy is done."""
+    n, d, K = geometry
+    nbytes = hc_read_up_tiles_bytes(h)
+    _check(load().hc_read_register_up_tiles(
+        h, _ptr(W_up, "W_up", _BF16, K * n * d), _ptr(tiles, "tiles", _BF16, nbytes // 2),
+        _stream_ptr(stream)), "hc_read_register_up_tiles")
+
+
+def hc_read_forget_up_tiles(h: int, W_up=None) -> None:
+    """Drop the handle's tile-ordered copy of W_up (all of them for None)."""
+    _check(load().hc_read_forget_up_tiles(h, _ptr(W_up, "W_up", _BF16, None)), "hc_read_forget_up_tiles")
+
+
 def _descs(geometry, reads, T: int):
     """hc_read_desc array of a list of reads (tensors checked; ints pass as addresses)."""
     n, d, K = geometry
@@ -578,6 +608,21 @@ class Read:
 
     def forget_down_tiles(self, W_down=None) -> None:
         hc_read_forget_down_tiles(self.h, W_down)
+
+    def up_tiles(self, W_up, stream=None):
+        """A tile-ordered copy of W_up, registered with this handle (None at a
+        geometry where no kernel takes one).  Keep the tensor alive while
+        registered."""
+        import torch
+        nbytes = hc_read_up_tiles_bytes(self.h)
+        if nbytes == 0:
+            return None
+        tiles = torch.empty(nbytes // 2, dtype=torch.int16, device=W_up.device)
+        hc_read_register_up_tiles(self.h, self.geometry, W_up, tiles, stream)
+        return tiles
+
+    def forget_up_tiles(self, W_up=None) -> None:
+        hc_read_forget_up_tiles(self.h, W_up)
 
     def error_word(self) -> int:
         return hc_read_error_word(self.h)

@@ -161,6 +161,8 @@ struct DownArgs {
   unsigned long long wait_ns;  // limit of the first bulk-copy wait from the kernel's start (0: kWaitNs)
   const void* W_tiles;         // W_down in tile order (hc_pack_down_tiles_kernel) or null: the BF16
                                // kernels of 32-row tiles then copy each tile as one contiguous block
+  const void* W_tiles_sw;      // W_down in 64-row swizzled tile order (hc_pack_down_sw_kernel) or
+                               // null: the tensor-memory kernels then copy each tile as one block
 };
 
 struct UpArgs {
@@ -179,6 +181,8 @@ struct UpArgs {
   int T;
   int T_max;
   int independent;       // 1: no read in flight writes R or P (see below)
+  const void* W_up_tiles;  // W_up in swizzled up-tile order (hc_pack_up_sw_kernel) or null (the
+                           // wide tensor-memory up kernel then copies each tile as one block)
 };
 
 // R and P of one token group of this up CTA's rows (64 rows = 16 columns x

@@ -99,6 +99,18 @@ __device__ __forceinline__ int ucanon(int r, int k) {
 }
 
 // ------------------------------------------------------------------ kernel 1
+// One tile of a swizzled tile order (hc_pack_down_sw_kernel,
+// hc_pack_up_sw_kernel): BYTES contiguous bytes, already in the 128-byte
+// swizzle layout the TMA boxes would write, copied in four pieces.
+template <int BYTES>
+__device__ __forceinline__ void copy_sw_tile(unsigned char* dst, const void* tiles, size_t tile, uint64_t* bar,
+                                             uint64_t policy) {
+  static_assert(BYTES % 64 == 0, "four 16-byte-aligned pieces");
+  const unsigned char* src = static_cast<const unsigned char*>(tiles) + tile * BYTES;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) ptx::bulk_g2s(dst + q * (BYTES / 4), src + q * (BYTES / 4), BYTES / 4, bar, policy);
+}
+
 template <int D, int KD>
 __global__ void __launch_bounds__(UGeo<D, KD>::THREADS, 4) hc_down_u_kernel(const __grid_constant__ DownUArgs args) {
   using U = UGeo<D, KD>;
@@ -139,8 +151,12 @@ __global__ void __launch_bounds__(UGeo<D, KD>::THREADS, 4) hc_down_u_kernel(cons
     ptx::fence_barrier_init();
     ptx::mbar_arrive_expect_tx(bar_w, U::M * U::KC * 2);
     const uint64_t once = ptx::policy_evict_first();
+    if (a.W_tiles_sw == nullptr) {
 #pragma unroll
-    for (int j = 0; j < U::KC / 64; ++j) ptx::tma_load_2d(sa + j * U::SLICE, &args.w, col0 + 64 * j, row0, bar_w, once);
+      for (int j = 0; j < U::KC / 64; ++j) ptx::tma_load_2d(sa + j * U::SLICE, &args.w, col0 + 64 * j, row0, bar_w, once);
+    } else {
+      copy_sw_tile<U::M * U::KC * 2>(sa, a.W_tiles_sw, (size_t)rg * U::CHUNKS + chunk, bar_w, once);
+    }
   }
   const int c4 = tid;
   const bool has4 = c4 < U::KC / 4;

@@ -252,8 +252,12 @@ __global__ void __launch_bounds__(WGeo<D, KD>::THREADS, 3) hc_down_w1_kernel(con
     ptx::fence_barrier_init();
     ptx::mbar_arrive_expect_tx(bar_w, W::M * W::KC * 2);
     const uint64_t once = ptx::policy_evict_first();
+    if (a.W_tiles_sw == nullptr) {
 #pragma unroll
-    for (int j = 0; j < W::NSL_D; ++j) ptx::tma_load_2d(sa + j * W::SLICE_A, &args.w, col0 + 64 * j, row0, bar_w, once);
+      for (int j = 0; j < W::NSL_D; ++j) ptx::tma_load_2d(sa + j * W::SLICE_A, &args.w, col0 + 64 * j, row0, bar_w, once);
+    } else {
+      copy_sw_tile<W::M * W::KC * 2>(sa, a.W_tiles_sw, (size_t)rg * W::CHUNKS + chunk, bar_w, once);
+    }
   }
   // w_norm of this lane's float4 columns lane, lane + 32, ...
   float4 wn[W::C4L];
@@ -472,8 +476,12 @@ __global__ void __launch_bounds__(WGeo<D, KD>::THREADS, 3) hc_down_w_kernel(cons
     ptx::fence_barrier_init();
     ptx::mbar_arrive_expect_tx(bar_w, W::M * W::KC * 2);
     const uint64_t once = ptx::policy_evict_first();
+    if (a.W_tiles_sw == nullptr) {
 #pragma unroll
-    for (int j = 0; j < W::NSL_D; ++j) ptx::tma_load_2d(sa + j * W::SLICE_A, &args.w, col0 + 64 * j, row0, bar_w, once);
+      for (int j = 0; j < W::NSL_D; ++j) ptx::tma_load_2d(sa + j * W::SLICE_A, &args.w, col0 + 64 * j, row0, bar_w, once);
+    } else {
+      copy_sw_tile<W::M * W::KC * 2>(sa, a.W_tiles_sw, (size_t)rg * W::CHUNKS + chunk, bar_w, once);
+    }
   }
   if (warp == 1) {
     __syncwarp();  // tcgen05.alloc is .aligned
@@ -707,12 +715,16 @@ __global__ void __launch_bounds__(WGeo<D, KD>::THREADS, TPU == 16 ? 3 : 2)
     ptx::mbar_arrive_expect_tx(bar_w, W::M * KD * 2);
     for (int p = 0; p < npass; ++p) ptx::mbar_arrive_expect_tx(&bar_b[p], P::UP_RECV);
     const uint64_t once = ptx::policy_evict_first();
+    if (a.W_up_tiles == nullptr) {
 #pragma unroll
-    for (int s = 0; s < kStreams; ++s) {
+      for (int s = 0; s < kStreams; ++s) {
 #pragma unroll
-      for (int j = 0; j < W::NSL_U; ++j) {
-        ptx::tma_load_2d(sa + j * W::SLICE_A + s * (W::UC * 128), &args.w, 64 * j, s * D + c0, bar_w, once);
+        for (int j = 0; j < W::NSL_U; ++j) {
+          ptx::tma_load_2d(sa + j * W::SLICE_A + s * (W::UC * 128), &args.w, 64 * j, s * D + c0, bar_w, once);
+        }
       }
+    } else {
+      copy_sw_tile<W::M * KD * 2>(sa, a.W_up_tiles, blockIdx.x, bar_w, once);
     }
   }
   // Gates of the 64 rows (weights: before the dependency wait).
@@ -898,6 +910,41 @@ __global__ void __launch_bounds__(WGeo<D, KD>::THREADS, TPU == 16 ? 3 : 2)
     a.mean[(size_t)t * D + c0 + j] = (((o[0] + o[W::UC]) + o[2 * W::UC]) + o[3 * W::UC]) * 0.25f;
   }
   if (tid == 0 && !ok) drain(bar_w, 0);
+}
+
+// ---- Weights in swizzled tile order: each CTA's tile of the tensor-memory
+// kernels (64 rows x 320 columns of W_down for a down CTA, 64 rows x K of
+// W_up for a wide up CTA) as one contiguous block of five 64-column slices,
+// each 64 rows of 128 bytes whose 16-byte chunk p holds the row's chunk
+// p ^ (row mod 8): the layout the TMA boxes write into shared memory, so a
+// CTA copies its tile in four contiguous pieces and computes on the same
+// bytes.  One thread per 16-byte chunk.
+template <int D, int KD>
+__global__ void __launch_bounds__(256) hc_pack_down_sw_kernel(const uint16_t* __restrict__ W,
+                                                              uint16_t* __restrict__ tiles) {
+  using G = WGeo<D, KD>;
+  constexpr int CHUNKS16 = G::M * G::KC / 8;  // 16-byte chunks of a tile
+  const size_t tile = (size_t)blockIdx.y * G::CHUNKS + blockIdx.x;  // (row group, column chunk)
+  uint4* dst = reinterpret_cast<uint4*>(tiles) + tile * CHUNKS16;
+  for (int i = threadIdx.x; i < CHUNKS16; i += blockDim.x) {
+    const int j = i / (G::M * 8), r = (i / 8) % G::M, p = i % 8;  // slice, row, chunk position
+    const int k = 64 * j + 8 * (p ^ (r & 7));
+    dst[i] = __ldg(reinterpret_cast<const uint4*>(W + (size_t)(blockIdx.y * G::M + r) * G::N + blockIdx.x * G::KC + k));
+  }
+}
+
+template <int D, int KD>
+__global__ void __launch_bounds__(256) hc_pack_up_sw_kernel(const uint16_t* __restrict__ W,
+                                                            uint16_t* __restrict__ tiles) {
+  using G = WGeo<D, KD>;
+  constexpr int CHUNKS16 = G::M * KD / 8;
+  uint4* dst = reinterpret_cast<uint4*>(tiles) + (size_t)blockIdx.x * CHUNKS16;
+  for (int i = threadIdx.x; i < CHUNKS16; i += blockDim.x) {
+    const int j = i / (G::M * 8), r = (i / 8) % G::M, p = i % 8;  // slice, row 16 s + c, chunk position
+    const int k = 64 * j + 8 * (p ^ (r & 7));
+    const size_t row = (size_t)(r / G::UC) * D + blockIdx.x * G::UC + (r % G::UC);
+    dst[i] = __ldg(reinterpret_cast<const uint4*>(W + row * KD + k));
+  }
 }
 
 }  // namespace hc

@@ -73,8 +73,10 @@ struct hc_read_s {
     int parity;
   } lanes[kBatchLanes];
   MapCache* map_cache;  // created on first use
-  // W_down -> its tile-ordered copy (hc_read_register_down_tiles); created on first use.
+  // W_down -> its tile-ordered copies, W_up -> its (hc_read_register_down_tiles,
+  // hc_read_register_up_tiles); created on first use.
   std::unordered_map<const void*, const void*>* down_tiles;
+  std::unordered_map<const void*, const void*>* up_tiles;
   unsigned long long wait_ns;  // limit of the down kernels' first bulk-copy wait (0: the default)
   bool overlap;       // reads may overlap their predecessor (independent mode), hc_read_set_overlap
   int nlanes;         // lanes created (0: batches run on the caller's stream only)
@@ -680,17 +682,24 @@ const CUtensorMap* up_map_for(hc_read_t h, const ReadDesc& q, int T) {
   return weight_map(h, 1, q.W_up);
 }
 
-// The tile-ordered copy registered for a W_down, or null.
-const void* down_tiles_for(hc_read_t h, const void* W_down) {
-  if (h->down_tiles == nullptr) return nullptr;
-  const auto it = h->down_tiles->find(W_down);
-  return it == h->down_tiles->end() ? nullptr : it->second;
+// The tile-ordered copy registered for a weight, or null.
+const void* tiles_for(const std::unordered_map<const void*, const void*>* m, const void* W) {
+  if (m == nullptr) return nullptr;
+  const auto it = m->find(W);
+  return it == m->end() ? nullptr : it->second;
 }
 
+// The down-tile buffer: the 32-row tiles, then (d = 2560, where the
+// tensor-memory kernels run) the 64-row swizzled tiles.
 template <int D, int KD>
-constexpr size_t down_tiles_bytes() {
+constexpr size_t down_tiles_rows_bytes() {
   using G = hc::Geo<D, KD>;
   return (size_t)G::ROW_GROUPS * G::SLABS * G::DN_ROWS * G::DN_PITCH;
+}
+constexpr size_t kSwTilesBytes = (size_t)4 * 2560 * 320 * 2;  // all of W_down or W_up at d = 2560, K = 320
+
+size_t down_tiles_bytes(int d) {
+  return d == 2560 ? down_tiles_rows_bytes<2560, 320>() + kSwTilesBytes : down_tiles_rows_bytes<4096, 512>();
 }
 
 template <int D, int KD>
@@ -698,6 +707,12 @@ cudaError_t launch_pack_down_tiles(const void* W_down, void* tiles, cudaStream_t
   using G = hc::Geo<D, KD>;
   hc::hc_pack_down_tiles_kernel<D, KD><<<dim3(G::SLABS, G::ROW_GROUPS), hc::kThreads, 0, st>>>(
       static_cast<const uint16_t*>(W_down), static_cast<uint16_t*>(tiles));
+  if constexpr (D == 2560) {
+    using W = hc::WGeo<D, KD>;
+    hc::hc_pack_down_sw_kernel<D, KD><<<dim3(W::CHUNKS, W::ROW_GROUPS), 256, 0, st>>>(
+        static_cast<const uint16_t*>(W_down),
+        reinterpret_cast<uint16_t*>(static_cast<unsigned char*>(tiles) + down_tiles_rows_bytes<D, KD>()));
+  }
   return cudaGetLastError();
 }
 
@@ -718,7 +733,10 @@ int enqueue_read(hc_read_t h, float* part, int device, const ReadDesc& q, int T,
   da.P = q.pending;
   da.w_norm = q.w_norm;
   da.W_down = q.W_down;
-  da.W_tiles = q.is_q8() ? nullptr : down_tiles_for(h, q.W_down);
+  da.W_tiles = q.is_q8() ? nullptr : tiles_for(h->down_tiles, q.W_down);
+  da.W_tiles_sw = (da.W_tiles != nullptr && h->d == 2560)
+                      ? static_cast<const unsigned char*>(da.W_tiles) + down_tiles_rows_bytes<2560, 320>()
+                      : nullptr;
   da.Wq = q.q8.Wd_q;
   da.Wscale = q.q8.Wd_scale;
   da.part = part;
@@ -747,6 +765,7 @@ int enqueue_read(hc_read_t h, float* part, int device, const ReadDesc& q, int T,
   ua.T = T;
   ua.T_max = h->T_max;
   ua.independent = independent;
+  ua.W_up_tiles = q.is_q8() ? nullptr : tiles_for(h->up_tiles, q.W_up);
 
   cudaError_t e;
   if (q.is_q8()) {
@@ -1149,6 +1168,7 @@ HC_EXPORT void hc_read_destroy(hc_read_t h) {
   }
   delete h->map_cache;
   delete h->down_tiles;
+  delete h->up_tiles;
   delete h;
 }
 
@@ -1167,14 +1187,23 @@ HC_EXPORT int hc_read_set_overlap(hc_read_t h, int enabled) {
 
 HC_EXPORT int64_t hc_read_down_tiles_bytes(hc_read_t h) {
   if (h == nullptr) return -1;
-  return static_cast<int64_t>(h->d == 2560 ? down_tiles_bytes<2560, 320>() : down_tiles_bytes<4096, 512>());
+  return static_cast<int64_t>(down_tiles_bytes(h->d));
 }
 
-HC_EXPORT int hc_read_register_down_tiles(hc_read_t h, const void* W_down, void* tiles, hc_stream_t stream) {
-  if (h == nullptr || W_down == nullptr || tiles == nullptr) return HC_ERR_ARG;
-  if (!aligned16(W_down) || !aligned16(tiles)) return HC_ERR_ALIGN;
-  const size_t bytes = static_cast<size_t>(hc_read_down_tiles_bytes(h));
-  if (overlaps(range_of(W_down, (size_t)h->K * h->n * h->d * 2), range_of(tiles, bytes))) return HC_ERR_ARG;
+HC_EXPORT int64_t hc_read_up_tiles_bytes(hc_read_t h) {
+  if (h == nullptr) return -1;
+  return h->d == 2560 ? static_cast<int64_t>(kSwTilesBytes) : 0;
+}
+
+namespace {
+
+// Writes `tiles` from W (on `stream`, waited for) and registers W -> tiles in *map.
+int register_tiles(hc_read_t h, std::unordered_map<const void*, const void*>*& map, const void* W, size_t w_bytes,
+                   void* tiles, size_t tile_bytes, hc_stream_t stream, bool up) {
+  if (h == nullptr || W == nullptr || tiles == nullptr) return HC_ERR_ARG;
+  if (!aligned16(W) || !aligned16(tiles)) return HC_ERR_ALIGN;
+  if (tile_bytes == 0) return HC_ERR_SHAPE;
+  if (overlaps(range_of(W, w_bytes), range_of(tiles, tile_bytes))) return HC_ERR_ARG;
   int cur = -1;
   if (cudaGetDevice(&cur) != cudaSuccess) return HC_ERR_CUDA;
   if (cur != h->device) return HC_ERR_ARG;
@@ -1184,32 +1213,61 @@ HC_EXPORT int hc_read_register_down_tiles(hc_read_t h, const void* W_down, void*
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return HC_ERR_CUDA;
   if (cs != cudaStreamCaptureStatusNone) return HC_ERR_ARG;
-  cudaError_t e = h->d == 2560 ? launch_pack_down_tiles<2560, 320>(W_down, tiles, st)
-                               : launch_pack_down_tiles<4096, 512>(W_down, tiles, st);
+  cudaError_t e;
+  if (up) {
+    using Wg = hc::WGeo<2560, 320>;
+    hc::hc_pack_up_sw_kernel<2560, 320><<<Wg::UP_CTAS, 256, 0, st>>>(static_cast<const uint16_t*>(W),
+                                                                     static_cast<uint16_t*>(tiles));
+    e = cudaGetLastError();
+  } else {
+    e = h->d == 2560 ? launch_pack_down_tiles<2560, 320>(W, tiles, st) : launch_pack_down_tiles<4096, 512>(W, tiles, st);
+  }
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return HC_ERR_CUDA;
   }
   try {
-    if (h->down_tiles == nullptr) h->down_tiles = new std::unordered_map<const void*, const void*>();
-    (*h->down_tiles)[W_down] = tiles;
+    if (map == nullptr) map = new std::unordered_map<const void*, const void*>();
+    (*map)[W] = tiles;
   } catch (...) {
     return HC_ERR_CUDA;
   }
   return HC_OK;
 }
 
-HC_EXPORT int hc_read_forget_down_tiles(hc_read_t h, const void* W_down) {
+int forget_tiles(hc_read_t h, std::unordered_map<const void*, const void*>* map, const void* W) {
   if (h == nullptr) return HC_ERR_ARG;
-  if (h->down_tiles != nullptr) {
-    if (W_down == nullptr) {
-      h->down_tiles->clear();
+  if (map != nullptr) {
+    if (W == nullptr) {
+      map->clear();
     } else {
-      h->down_tiles->erase(W_down);
+      map->erase(W);
     }
   }
   return HC_OK;
+}
+
+}  // namespace
+
+HC_EXPORT int hc_read_register_down_tiles(hc_read_t h, const void* W_down, void* tiles, hc_stream_t stream) {
+  if (h == nullptr) return HC_ERR_ARG;
+  return register_tiles(h, h->down_tiles, W_down, (size_t)h->K * h->n * h->d * 2, tiles, down_tiles_bytes(h->d),
+                        stream, false);
+}
+
+HC_EXPORT int hc_read_forget_down_tiles(hc_read_t h, const void* W_down) {
+  return forget_tiles(h, h == nullptr ? nullptr : h->down_tiles, W_down);
+}
+
+HC_EXPORT int hc_read_register_up_tiles(hc_read_t h, const void* W_up, void* tiles, hc_stream_t stream) {
+  if (h == nullptr) return HC_ERR_ARG;
+  return register_tiles(h, h->up_tiles, W_up, (size_t)h->K * h->n * h->d * 2, tiles,
+                        static_cast<size_t>(hc_read_up_tiles_bytes(h)), stream, true);
+}
+
+HC_EXPORT int hc_read_forget_up_tiles(hc_read_t h, const void* W_up) {
+  return forget_tiles(h, h == nullptr ? nullptr : h->up_tiles, W_up);
 }
 
 HC_EXPORT int64_t hc_read_scratch_bytes(hc_read_t h) {

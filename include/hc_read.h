@@ -281,37 +281,51 @@ int hc_read_set_wait_limit(hc_read_t h, uint64_t ns);
  * concurrent read on the same handle. */
 int hc_read_set_overlap(hc_read_t h, int enabled);
 
-/* W_down in tile order: an optional second copy of a W_down that the down
- * kernels of 32-row tiles (BF16 reads with T <= 4 at d = 2560, every T at
- * d = 4096) copy as one contiguous block per CTA instead of 32 row segments
- * 2N bytes apart.  The values are the same, and so is every bit of every
- * result; the gain is
- * DRAM efficiency (measured at d = 2560 in a cold batch: about 10 % less time
- * per read at T = 1..4).  The other kernels keep reading W_down itself.
+/* Weights in tile order: optional second copies of a W_down or W_up, laid
+ * out so that every CTA of the read kernels fetches its weight tile as one
+ * contiguous block instead of many row segments far apart in [K][N] or
+ * [N][K].  The values are the same, and so is every bit of every result; the
+ * gain is DRAM efficiency (measured at d = 2560 in a cold batch: about 8 %
+ * less time per read at T = 1..4 and T = 9..16, 3-5 % at T = 32..64, 2 % at
+ * T = 5..8).  Reads whose kernels have no tiled path keep reading the
+ * weights themselves.
  *
- * hc_read_down_tiles_bytes: size of the copy for this handle's geometry
- * (6,635,520 bytes at d = 2560, K = 320; 16,908,288 at d = 4096, K = 512;
- * 1.2 % above W_down: 16 padding bytes per tile row), or -1 for a NULL handle.
+ * hc_read_down_tiles_bytes: size of a W_down's copy for this handle's
+ * geometry, or -1 for a NULL handle.  At d = 2560, K = 320: 13,189,120
+ * bytes, the 32-row tiles of the BF16 reads with T <= 4 (6,635,520 bytes:
+ * rows at a 1,296-byte pitch) followed by the 64-row tiles of the
+ * tensor-memory kernels (T >= 5; 6,553,600 bytes in the 128-byte swizzle of
+ * their shared memory).  At d = 4096, K = 512: the 32-row tiles alone,
+ * 16,908,288 bytes, which every T reads.
  *
- * hc_read_register_down_tiles: writes the tile-ordered copy of W_down
- * ([K][N] BF16 on the handle's device) into `tiles` (caller-owned device
- * memory of hc_read_down_tiles_bytes bytes, disjoint from W_down) on
- * `stream`, waits for it, and registers the pair: every later read through
- * this handle whose W_down is this pointer reads its down weights from
- * `tiles` where its kernels can.  A registration replaces one of the same
- * W_down.  `tiles` must stay allocated and W_down's contents unchanged until
- * hc_read_forget_down_tiles or hc_read_destroy (register again after
+ * hc_read_up_tiles_bytes: size of a W_up's copy (6,553,600 bytes at
+ * d = 2560, read by the up kernel of T >= 9; 0 at d = 4096, where no kernel
+ * takes one), or -1 for a NULL handle.
+ *
+ * hc_read_register_down_tiles / hc_read_register_up_tiles: write the copy of
+ * W_down ([K][N] BF16) or W_up ([N][K] BF16), on the handle's device, into
+ * `tiles` (caller-owned device memory of the size above, disjoint from the
+ * weights) on `stream`, wait for it, and register the pair: every later read
+ * through this handle whose W_down (W_up) is this pointer fetches its tiles
+ * from `tiles` where its kernels can.  A registration replaces one of the
+ * same pointer.  `tiles` must stay allocated and the weights unchanged until
+ * the matching forget call or hc_read_destroy (register again after
  * changing the weights); graphs captured meanwhile keep using `tiles`.  Not
  * during stream capture.  HC_ERR_ARG for a NULL handle or pointer, a
  * capturing stream, overlapping buffers or another device; HC_ERR_ALIGN if
- * either pointer is not 16-byte aligned; HC_ERR_CUDA if the copy fails.
+ * either pointer is not 16-byte aligned; HC_ERR_SHAPE for up tiles at a
+ * geometry without a kernel that takes them; HC_ERR_CUDA if the copy fails.
  *
- * hc_read_forget_down_tiles: drops the registration of W_down (all of them
- * for NULL); later reads read W_down itself.  HC_ERR_ARG for a NULL handle.
- * Neither call is thread-safe against a concurrent read on the same handle. */
+ * hc_read_forget_down_tiles / hc_read_forget_up_tiles: drop the registration
+ * of a W_down (W_up), all of them for NULL; later reads read the weights
+ * themselves.  HC_ERR_ARG for a NULL handle.  None of these calls is
+ * thread-safe against a concurrent read on the same handle. */
 int64_t hc_read_down_tiles_bytes(hc_read_t h);
 int hc_read_register_down_tiles(hc_read_t h, const void* W_down, void* tiles, hc_stream_t stream);
 int hc_read_forget_down_tiles(hc_read_t h, const void* W_down);
+int64_t hc_read_up_tiles_bytes(hc_read_t h);
+int hc_read_register_up_tiles(hc_read_t h, const void* W_up, void* tiles, hc_stream_t stream);
+int hc_read_forget_up_tiles(hc_read_t h, const void* W_up);
 
 /* hc_read without a handle and without any device allocation.
  *

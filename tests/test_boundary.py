@@ -69,6 +69,9 @@ def test_null_handle_rejected(lib):
     assert lib.hc_read_down_tiles_bytes(None) == -1
     assert lib.hc_read_register_down_tiles(None, None, None, None) == hc.HC_ERR_ARG
     assert lib.hc_read_forget_down_tiles(None, None) == hc.HC_ERR_ARG
+    assert lib.hc_read_up_tiles_bytes(None) == -1
+    assert lib.hc_read_register_up_tiles(None, None, None, None) == hc.HC_ERR_ARG
+    assert lib.hc_read_forget_up_tiles(None, None) == hc.HC_ERR_ARG
 
 
 def test_q2_matvec_rejects_bad_arguments(lib):

@@ -1,12 +1,14 @@
-"""GPU checks of W_down in tile order (hc_read_register_down_tiles).
+"""GPU checks of weights in tile order (hc_read_register_down_tiles,
+hc_read_register_up_tiles).
 
-A registered tile-ordered copy changes where the down kernels of 32-row
-tiles fetch their weights, not what they compute: every read with it must
-equal the same read without it bit for bit (direct calls, batches on the
-internal streams, graph replays), at d = 2560 (T = 1..4 take the tiles,
-larger T ignore them) and at d = 4096 (every T takes them).  That the
-kernels really read the tiles is shown by zeroing them: the down projection
-then sees zero weights, so lo = 0 and out = R + P exactly, until the
+A registered tile-ordered copy changes where the kernels fetch their weight
+tiles, not what they compute: every read with it must equal the same read
+without it bit for bit (direct calls, batches on the internal streams, graph
+replays), at d = 2560 (the down tiles serve every T: 32-row tiles up to
+T = 4, swizzled 64-row tiles above; the up tiles serve T >= 9) and at
+d = 4096 (down tiles, every T).  That the kernels really read the tiles is
+shown by zeroing them: zero down weights give lo = 0 and out = R + P
+exactly, zero up weights out = R + P with lo unchanged, until the
 registration is dropped."""
 
 import numpy as np
@@ -54,7 +56,9 @@ def _same(x, y, what):
 
 @pytest.mark.parametrize("geom,T,pending", [
     (synth.G1, 1, False), (synth.G1, 2, True), (synth.G1, 3, False), (synth.G1, 4, True),
-    (synth.G1, 6, True), (synth.G2, 1, True), (synth.G2, 5, True), (synth.G2, 8, False)],
+    (synth.G1, 5, False), (synth.G1, 6, True), (synth.G1, 8, False), (synth.G1, 9, True),
+    (synth.G1, 16, False), (synth.G1, 17, True), (synth.G1, 33, False), (synth.G1, 64, True),
+    (synth.G2, 1, True), (synth.G2, 5, True), (synth.G2, 8, False)],
     ids=lambda v: f"d{v.d}" if isinstance(v, synth.Geometry) else str(v))
 def test_tiles_bit_identical(dev, orc, geom, T, pending):
     g = geom
@@ -62,9 +66,11 @@ def test_tiles_bit_identical(dev, orc, geom, T, pending):
     w = dev_weights(ws, dev)
     act = synth.activations(g, T, pending, s0=6000 + T)
     a = dev_act(act, dev)
-    with hc.Read(g.n, g.d, g.K, T_max=8, eps=EPS) as plain, hc.Read(g.n, g.d, g.K, T_max=8, eps=EPS) as tiled:
+    with hc.Read(g.n, g.d, g.K, T_max=64, eps=EPS) as plain, hc.Read(g.n, g.d, g.K, T_max=64, eps=EPS) as tiled:
         tiles = tiled.down_tiles(w["W_down"])
+        up = tiled.up_tiles(w["W_up"])
         assert tiles.numel() * 2 == hc.hc_read_down_tiles_bytes(tiled.h)
+        assert (up is None) == (g.d != 2560)
         o1, o2 = _outs(g, T, dev), _outs(g, T, dev)
         _read(plain, w, a, T, o1)
         _read(tiled, w, a, T, o2)
@@ -78,24 +84,28 @@ def test_tiles_bit_identical(dev, orc, geom, T, pending):
         assert float(np.max(np.abs(got - want))) <= TOL * float(np.max(np.abs(want))), name
 
 
-@pytest.mark.parametrize("T,used", [(1, True), (4, True), (5, False)])
-def test_tiles_are_what_the_kernels_read(dev, T, used):
+@pytest.mark.parametrize("T,which,used", [(1, "down", True), (4, "down", True), (5, "down", True),
+                                          (16, "down", True), (4, "up", False), (16, "up", True)])
+def test_tiles_are_what_the_kernels_read(dev, T, which, used):
     g = synth.G1
     w = dev_weights(synth.weight_set(g, 70), dev)
     a = dev_act(synth.activations(g, T, True, s0=6100 + T), dev)
-    with hc.Read(g.n, g.d, g.K, T_max=8, eps=EPS) as r, hc.Read(g.n, g.d, g.K, T_max=8, eps=EPS) as ref:
-        tiles = r.down_tiles(w["W_down"])
+    with hc.Read(g.n, g.d, g.K, T_max=64, eps=EPS) as r, hc.Read(g.n, g.d, g.K, T_max=64, eps=EPS) as ref:
+        tiles = r.down_tiles(w["W_down"]) if which == "down" else r.up_tiles(w["W_up"])
         tiles.zero_()
         o, want = _outs(g, T, dev), _outs(g, T, dev)
         _read(r, w, a, T, o)
         _read(ref, w, a, T, want)
         torch.cuda.synchronize()
-        if used:
+        if not used:
+            _same(o, want, f"T={T} ({which} tiles not taken)")
+        elif which == "down":
             assert torch.count_nonzero(o["lo"]).item() == 0
             assert np.array_equal(bits(o["out"]), bits(a["R"] + a["P"]))
         else:
-            _same(o, want, f"T={T} (tiles not taken)")
-        r.forget_down_tiles(w["W_down"])
+            assert np.array_equal(bits(o["lo"]), bits(want["lo"]))
+            assert np.array_equal(bits(o["out"]), bits(a["R"] + a["P"]))
+        (r.forget_down_tiles if which == "down" else r.forget_up_tiles)()
         o2 = _outs(g, T, dev)
         _read(r, w, a, T, o2)
         torch.cuda.synchronize()
@@ -139,7 +149,7 @@ def test_tiles_argument_errors(dev):
     w = dev_weights(synth.weight_set(g, 90), dev)
     with hc.Read(g.n, g.d, g.K, T_max=8, eps=EPS) as r:
         nb = hc.hc_read_down_tiles_bytes(r.h)
-        assert nb == 6635520
+        assert nb == 6635520 + 6553600 and hc.hc_read_up_tiles_bytes(r.h) == 6553600
         buf = torch.empty(nb // 2 + 16, dtype=torch.int16, device=dev)
         lib = hc._binding.load()
         assert lib.hc_read_register_down_tiles(r.h, w["W_down"].data_ptr(), buf.data_ptr() + 2, None) == hc.HC_ERR_ALIGN
@@ -157,3 +167,8 @@ def test_tiles_argument_errors(dev):
         hc.hc_graph_destroy(graph)
         assert st == hc.HC_ERR_ARG
         assert lib.hc_read_forget_down_tiles(r.h, None) == hc.HC_OK
+    g2 = synth.G2
+    with hc.Read(g2.n, g2.d, g2.K, T_max=8, eps=EPS) as r2:
+        w2 = dev_weights(synth.weight_set(g2, 91), dev)
+        assert hc.hc_read_up_tiles_bytes(r2.h) == 0
+        assert lib.hc_read_register_up_tiles(r2.h, w2["W_up"].data_ptr(), buf.data_ptr(), None) == hc.HC_ERR_SHAPE
