@@ -270,7 +270,7 @@ __device__ __forceinline__ void drain(uint64_t* bar, uint32_t parity) {
 // padding), tiles in the order (rg, slab).  A CTA then copies its 40 KB as
 // kTileCopies pieces of contiguous memory instead of 32 row segments 2N bytes
 // apart, which HBM serves faster (measured at d = 2560 in a cold batch: about
-// 10 % less time per read at T = 1..4).  The values are the same, and so is
+// 8 % less time per read at T = 1..4).  The values are the same, and so is
 // every bit of every result.
 constexpr int kTileCopies = 4;
 
