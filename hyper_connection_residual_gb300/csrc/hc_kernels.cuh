@@ -270,7 +270,7 @@ __device__ __forceinline__ void drain(uint64_t* bar, uint32_t parity) {
 // padding), tiles in the order (rg, slab).  A CTA then copies its 40 KB as
 // kTileCopies pieces of contiguous memory instead of 32 row segments 2N bytes
 // apart, which HBM serves faster (measured at d = 2560 in a cold batch: about
-// 8 % less time per read at T = 1..4).  The values are the same, and so is
+// 8 % less time per read at T = 2..4).  The values are the same, and so is
 // every bit of every result.
 constexpr int kTileCopies = 4;
 
@@ -302,6 +302,129 @@ __global__ void __launch_bounds__(kThreads) hc_pack_down_tiles_kernel(const uint
     }
     dst[i] = v;
   }
+}
+
+// ------------------------------------------------------------------ kernel 1, T = 1 (d = 2560)
+// One CTA per 8 rows of W_down and one stream, over all the stream's D
+// columns: the stream's sum of squares, its rs and the rows' partial sums
+// are complete in the CTA, so there is no cluster and no exchange, and the
+// weight tile is 8 row segments of 2D bytes.  CUDA cores, fp32 (T = 1: 80
+// multiply-adds a thread).  Writes the same rs-scaled per-stream partials
+// as the other down kernels.
+template <int D, int KD>
+struct StreamGeo {
+  static constexpr int ROWS = 8;                   // rows of W_down per CTA
+  static constexpr int ROW_GROUPS = KD / ROWS;
+  static constexpr int N = kStreams * D;
+  static constexpr int PAIRS = D / (2 * kThreads);  // column pairs per thread
+  static constexpr int W_BYTES = ROWS * D * 2;
+  static constexpr int BAR = 0;                    // bar_w, bar_n
+  static constexpr int WN = 128;                   // w_norm of the stream [D]
+  static constexpr int W = WN + D * 4;             // [ROWS][D] bf16
+  static constexpr int RED = W + W_BYTES;          // [kWarps][ROWS + 1]: row sums, then the sum of squares
+  static constexpr int BYTES = RED + kWarps * (ROWS + 1) * 4;
+  static_assert(D % (2 * kThreads) == 0 && KD % ROWS == 0 && ROWS <= 32, "whole column pairs and row groups");
+  static_assert((D * 2) % 16 == 0 && W % 16 == 0, "16-byte bulk copies");
+};
+
+template <int D, int KD>
+__global__ void __launch_bounds__(kThreads, 4) hc_down_s_kernel(const DownArgs a) {
+  using G = StreamGeo<D, KD>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t* bar_w = reinterpret_cast<uint64_t*>(smem + G::BAR);
+  uint64_t* bar_n = bar_w + 1;
+  const float* wn_s = reinterpret_cast<const float*>(smem + G::WN);
+  const unsigned char* w_s = smem + G::W;
+  float* red = reinterpret_cast<float*>(smem + G::RED);
+  const int rg = blockIdx.x, stream = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int row0 = rg * G::ROWS, col0 = stream * D;
+  const uint64_t t_entry = ptx::globaltimer_ns();
+
+  // w_norm of the stream and the 8 weight rows: parameters, issued first.
+  if (warp == 0) {
+    if (lane == 0) {
+      ptx::mbar_init(bar_w, 1);
+      ptx::mbar_init(bar_n, 1);
+      ptx::fence_barrier_init();
+      ptx::mbar_arrive_expect_tx(bar_n, D * 4);
+      ptx::mbar_arrive_expect_tx(bar_w, G::W_BYTES);
+      ptx::bulk_g2s(smem + G::WN, a.w_norm + col0, D * 4, bar_n, ptx::policy_evict_last());
+    }
+    __syncwarp();
+    if (lane < G::ROWS) {
+      ptx::bulk_g2s(smem + G::W + lane * (D * 2), a.W_down + (size_t)(row0 + lane) * G::N + col0, D * 2, bar_w,
+                    ptx::policy_evict_first());
+    }
+  }
+  // Late launch of the up kernel on the batch lanes, as in hc_down_kernel.
+  const bool late_launch = a.late_launch && a.independent;
+  if (!late_launch) ptx::launch_dependents();
+  __syncthreads();  // the mbarriers are initialised before any thread waits on them
+  if (!a.independent) ptx::wait_prerequisites();
+
+  // This thread's columns: pairs 2 tid + 2 kThreads k (coalesced float2 and
+  // BF16 pair loads).  R' = R + P, x = R' * w_norm, and R'^2 summed.
+  float2 rv[G::PAIRS], pv[G::PAIRS];
+#pragma unroll
+  for (int k = 0; k < G::PAIRS; ++k) {
+    const int c = 2 * tid + 2 * kThreads * k;
+    rv[k] = __ldcg(reinterpret_cast<const float2*>(a.R + col0 + c));
+    pv[k] = a.P ? __ldcg(reinterpret_cast<const float2*>(a.P + col0 + c)) : make_float2(0.f, 0.f);
+  }
+  bool ok = wait_bar_from(bar_n, 0, a.err, kErrDownNorm, t_entry, first_wait_limit(a.wait_ns));
+  float x[2 * G::PAIRS];
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < G::PAIRS; ++k) {
+    const int c = 2 * tid + 2 * kThreads * k;
+    const float r0 = __fadd_rn(rv[k].x, pv[k].x), r1 = __fadd_rn(rv[k].y, pv[k].y);
+    x[2 * k] = __fmul_rn(r0, wn_s[c]);
+    x[2 * k + 1] = __fmul_rn(r1, wn_s[c + 1]);
+    ss = __fmaf_rn(r0, r0, ss);
+    ss = __fmaf_rn(r1, r1, ss);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if (lane == 0) red[warp * (G::ROWS + 1) + G::ROWS] = ss;
+
+  ok = wait_bar(bar_w, 0, a.err, kErrDownWeights) && ok;
+  if (late_launch) ptx::launch_dependents();
+  float acc[G::ROWS];
+#pragma unroll
+  for (int r = 0; r < G::ROWS; ++r) {
+    acc[r] = 0.f;
+#pragma unroll
+    for (int k = 0; k < G::PAIRS; ++k) {
+      const int c = 2 * tid + 2 * kThreads * k;
+      const uint32_t w2 = *reinterpret_cast<const uint32_t*>(w_s + r * (D * 2) + c * 2);
+      acc[r] = __fmaf_rn(__uint_as_float(w2 << 16), x[2 * k], acc[r]);
+      acc[r] = __fmaf_rn(__uint_as_float(w2 & 0xffff0000u), x[2 * k + 1], acc[r]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int r = 0; r < G::ROWS; ++r) red[warp * (G::ROWS + 1) + r] = acc[r];
+  }
+  __syncthreads();
+  if (tid < G::ROWS) {
+    float sq = 0.f, p = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      sq += red[w * (G::ROWS + 1) + G::ROWS];
+      p += red[w * (G::ROWS + 1) + tid];
+    }
+    const float rs = rsqrtf(sq * (1.0f / (float)D) + a.eps);
+    __stcg(a.part + (size_t)stream * a.T_max * KD + row0 + tid, __fmul_rn(rs, p));
+    if (rg == 0 && tid == 0 && a.rs_out != nullptr) a.rs_out[stream] = rs;
+  }
+  if (tid == 0 && !ok) {
+    drain(bar_n, 0);
+    drain(bar_w, 0);
+  }
+  if (a.independent) ptx::wait_prerequisites();  // complete only after the previous read
 }
 
 // ------------------------------------------------------------------ kernel 1

@@ -205,6 +205,9 @@ template <int D, int KD>
 cudaError_t configure_geometry() {
   cudaError_t e;
   if constexpr (D == 2560) {
+    if ((e = cudaFuncSetAttribute(hc::hc_down_s_kernel<D, KD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  hc::StreamGeo<D, KD>::BYTES)) != cudaSuccess)
+      return e;
     if ((e = configure_umma<D, KD>()) != cudaSuccess) return e;
     if ((e = configure_wide<D, KD>()) != cudaSuccess) return e;
   }
@@ -230,6 +233,21 @@ cudaError_t launch_pair(const DownArgs& da, const UpArgs& ua, cudaStream_t st) {
   cudaLaunchConfig_t c2 = pdl_config(dim3(G::UP_CTAS), hc::UpSmem<D, KD, TT>::bytes(ua.T), st,
                                       attr2, 1);
   return cudaLaunchKernelEx(&c2, hc::hc_up_kernel<D, KD, TT>, ua);
+}
+
+// T = 1 at d = 2560: the stream-wide down kernel (no cluster) with the
+// CUDA-core up kernel.
+template <int D, int KD>
+cudaError_t launch_pair_s(const DownArgs& da, const UpArgs& ua, cudaStream_t st) {
+  using S = hc::StreamGeo<D, KD>;
+  using G = hc::Geo<D, KD>;
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t c1 = pdl_config(dim3(S::ROW_GROUPS, hc::kStreams), S::BYTES, st, attr, 1);
+  cudaError_t e = cudaLaunchKernelEx(&c1, hc::hc_down_s_kernel<D, KD>, da);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr2[2];
+  cudaLaunchConfig_t c2 = pdl_config(dim3(G::UP_CTAS), hc::UpSmem<D, KD, 1>::bytes(ua.T), st, attr2, 1);
+  return cudaLaunchKernelEx(&c2, hc::hc_up_kernel<D, KD, 1>, ua);
 }
 
 template <int D, int KD, int NT, int Q8 = 0>
@@ -355,7 +373,11 @@ cudaError_t launch_pair_w(const DownArgs& da, const UpArgs& ua, const CUtensorMa
 template <int D, int KD>
 cudaError_t launch_geometry(int T, const DownArgs& da, const UpArgs& ua, cudaStream_t st,
                             const CUtensorMap* w_down, const CUtensorMap* w_up = nullptr) {
-  if (T == 1) return launch_pair<D, KD, 1>(da, ua, st);
+  if constexpr (D == 2560) {
+    if (T == 1) return launch_pair_s<D, KD>(da, ua, st);
+  } else {
+    if (T == 1) return launch_pair<D, KD, 1>(da, ua, st);
+  }
   if constexpr (D == 2560) {
     if (w_down != nullptr && w_up != nullptr && T >= kWideMinT) return launch_pair_w<D, KD>(da, ua, *w_down, *w_up, st);
     if (w_down != nullptr && T <= hc::UGeo<D, KD>::TMAX) return launch_pair_u<D, KD>(da, ua, *w_down, st);

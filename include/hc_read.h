@@ -286,13 +286,13 @@ int hc_read_set_overlap(hc_read_t h, int enabled);
  * contiguous block instead of many row segments far apart in [K][N] or
  * [N][K].  The values are the same, and so is every bit of every result; the
  * gain is DRAM efficiency (measured at d = 2560 in a cold batch: about 8 %
- * less time per read at T = 1..4, 4-5 % at T = 9..16, 3-4 % at T = 32, 2 %
+ * less time per read at T = 2..4, 4-5 % at T = 9..16, 3-4 % at T = 32, 2 %
  * at T = 64, within 1 % at T = 5..8).  Reads whose kernels have no tiled
  * path keep reading the weights themselves.
  *
  * hc_read_down_tiles_bytes: size of a W_down's copy for this handle's
  * geometry, or -1 for a NULL handle.  At d = 2560, K = 320: 13,189,120
- * bytes, the 32-row tiles of the BF16 reads with T <= 4 (6,635,520 bytes:
+ * bytes, the 32-row tiles of the BF16 reads with T = 2..4 (6,635,520 bytes:
  * rows at a 1,296-byte pitch) followed by the 64-row tiles of the
  * tensor-memory kernels (T >= 5; 6,553,600 bytes in the 128-byte swizzle of
  * their shared memory).  At d = 4096, K = 512: the 32-row tiles alone,

@@ -4,8 +4,9 @@ hc_read_register_up_tiles).
 A registered tile-ordered copy changes where the kernels fetch their weight
 tiles, not what they compute: every read with it must equal the same read
 without it bit for bit (direct calls, batches on the internal streams, graph
-replays), at d = 2560 (the down tiles serve every T: 32-row tiles up to
-T = 4, swizzled 64-row tiles above; the up tiles serve T >= 9) and at
+replays), at d = 2560 (the down tiles serve T = 2..4 with their 32-row
+tiles and T >= 5 with their swizzled 64-row tiles, T = 1 reads W_down in
+8-row stream-wide tiles of its own; the up tiles serve T >= 9) and at
 d = 4096 (down tiles, every T).  That the kernels really read the tiles is
 shown by zeroing them: zero down weights give lo = 0 and out = R + P
 exactly, zero up weights out = R + P with lo unchanged, until the
@@ -84,7 +85,7 @@ def test_tiles_bit_identical(dev, orc, geom, T, pending):
         assert float(np.max(np.abs(got - want))) <= TOL * float(np.max(np.abs(want))), name
 
 
-@pytest.mark.parametrize("T,which,used", [(1, "down", True), (4, "down", True), (5, "down", True),
+@pytest.mark.parametrize("T,which,used", [(1, "down", False), (2, "down", True), (4, "down", True), (5, "down", True),
                                           (16, "down", True), (4, "up", False), (16, "up", True)])
 def test_tiles_are_what_the_kernels_read(dev, T, which, used):
     g = synth.G1
