@@ -53,6 +53,7 @@
 // direct calls and graph replays give the same bits.
 #pragma once
 
+#include <cuda_fp16.h>
 #include <cooperative_groups.h>
 
 #include <cstdint>
@@ -308,28 +309,32 @@ __global__ void __launch_bounds__(kThreads) hc_pack_down_tiles_kernel(const uint
 // One CTA per 8 rows of W_down and one stream, over all the stream's D
 // columns: the stream's sum of squares, its rs and the rows' partial sums
 // are complete in the CTA, so there is no cluster and no exchange, and the
-// weight tile is 8 row segments of 2D bytes.  CUDA cores, fp32 (T = 1: 80
-// multiply-adds a thread).  Writes the same rs-scaled per-stream partials
-// as the other down kernels.
-template <int D, int KD>
+// weight tile is 8 row segments of 2D bytes (Q8: D bytes of quants and D/16
+// of block scales).  CUDA cores, fp32 (T = 1: 80 multiply-adds a thread;
+// a Q8_0 weight is scale * q, exact in fp32).  Writes the same rs-scaled
+// per-stream partials as the other down kernels.
+template <int D, int KD, bool Q8 = false>
 struct StreamGeo {
   static constexpr int ROWS = 8;                   // rows of W_down per CTA
   static constexpr int ROW_GROUPS = KD / ROWS;
   static constexpr int N = kStreams * D;
   static constexpr int PAIRS = D / (2 * kThreads);  // column pairs per thread
-  static constexpr int W_BYTES = ROWS * D * 2;
+  static constexpr int ROW_BYTES = Q8 ? D : D * 2;  // a weight row (quants for Q8)
+  static constexpr int SC_BYTES = Q8 ? D / 32 * 2 : 0;  // a row's binary16 block scales
+  static constexpr int W_BYTES = ROWS * ROW_BYTES;
   static constexpr int BAR = 0;                    // bar_w, bar_n
   static constexpr int WN = 128;                   // w_norm of the stream [D]
-  static constexpr int W = WN + D * 4;             // [ROWS][D] bf16
-  static constexpr int RED = W + W_BYTES;          // [kWarps][ROWS + 1]: row sums, then the sum of squares
+  static constexpr int W = WN + D * 4;             // [ROWS][D] bf16 (int8 for Q8)
+  static constexpr int SC = W + W_BYTES;           // [ROWS][D/32] binary16 (Q8)
+  static constexpr int RED = SC + ROWS * SC_BYTES;  // [kWarps][ROWS + 1]: row sums, then the sum of squares
   static constexpr int BYTES = RED + kWarps * (ROWS + 1) * 4;
   static_assert(D % (2 * kThreads) == 0 && KD % ROWS == 0 && ROWS <= 32, "whole column pairs and row groups");
-  static_assert((D * 2) % 16 == 0 && W % 16 == 0, "16-byte bulk copies");
+  static_assert(ROW_BYTES % 16 == 0 && SC_BYTES % 16 == 0 && W % 16 == 0 && SC % 16 == 0, "16-byte bulk copies");
 };
 
-template <int D, int KD>
+template <int D, int KD, bool Q8 = false>
 __global__ void __launch_bounds__(kThreads, 4) hc_down_s_kernel(const DownArgs a) {
-  using G = StreamGeo<D, KD>;
+  using G = StreamGeo<D, KD, Q8>;
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* bar_w = reinterpret_cast<uint64_t*>(smem + G::BAR);
   uint64_t* bar_n = bar_w + 1;
@@ -348,13 +353,21 @@ __global__ void __launch_bounds__(kThreads, 4) hc_down_s_kernel(const DownArgs a
       ptx::mbar_init(bar_n, 1);
       ptx::fence_barrier_init();
       ptx::mbar_arrive_expect_tx(bar_n, D * 4);
-      ptx::mbar_arrive_expect_tx(bar_w, G::W_BYTES);
+      ptx::mbar_arrive_expect_tx(bar_w, G::W_BYTES + G::ROWS * G::SC_BYTES);
       ptx::bulk_g2s(smem + G::WN, a.w_norm + col0, D * 4, bar_n, ptx::policy_evict_last());
     }
     __syncwarp();
     if (lane < G::ROWS) {
-      ptx::bulk_g2s(smem + G::W + lane * (D * 2), a.W_down + (size_t)(row0 + lane) * G::N + col0, D * 2, bar_w,
-                    ptx::policy_evict_first());
+      const uint64_t once = ptx::policy_evict_first();
+      if constexpr (Q8) {
+        ptx::bulk_g2s(smem + G::W + lane * G::ROW_BYTES, a.Wq + (size_t)(row0 + lane) * G::N + col0, G::ROW_BYTES,
+                      bar_w, once);
+        ptx::bulk_g2s(smem + G::SC + lane * G::SC_BYTES, a.Wscale + (size_t)(row0 + lane) * (G::N / 32) + col0 / 32,
+                      G::SC_BYTES, bar_w, once);
+      } else {
+        ptx::bulk_g2s(smem + G::W + lane * (D * 2), a.W_down + (size_t)(row0 + lane) * G::N + col0, D * 2, bar_w,
+                      once);
+      }
     }
   }
   // Late launch of the up kernel on the batch lanes, as in hc_down_kernel.
@@ -397,9 +410,20 @@ __global__ void __launch_bounds__(kThreads, 4) hc_down_s_kernel(const DownArgs a
 #pragma unroll
     for (int k = 0; k < G::PAIRS; ++k) {
       const int c = 2 * tid + 2 * kThreads * k;
-      const uint32_t w2 = *reinterpret_cast<const uint32_t*>(w_s + r * (D * 2) + c * 2);
-      acc[r] = __fmaf_rn(__uint_as_float(w2 << 16), x[2 * k], acc[r]);
-      acc[r] = __fmaf_rn(__uint_as_float(w2 & 0xffff0000u), x[2 * k + 1], acc[r]);
+      float w0, w1;
+      if constexpr (Q8) {
+        // Both columns in the block c / 32: scale * q, exact in fp32.
+        const char2 q = *reinterpret_cast<const char2*>(w_s + r * G::ROW_BYTES + c);
+        const float sc = __half2float(reinterpret_cast<const __half*>(smem + G::SC + r * G::SC_BYTES)[c / 32]);
+        w0 = __fmul_rn(sc, (float)q.x);
+        w1 = __fmul_rn(sc, (float)q.y);
+      } else {
+        const uint32_t w2 = *reinterpret_cast<const uint32_t*>(w_s + r * (D * 2) + c * 2);
+        w0 = __uint_as_float(w2 << 16);
+        w1 = __uint_as_float(w2 & 0xffff0000u);
+      }
+      acc[r] = __fmaf_rn(w0, x[2 * k], acc[r]);
+      acc[r] = __fmaf_rn(w1, x[2 * k + 1], acc[r]);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);

@@ -206,7 +206,9 @@ cudaError_t configure_geometry() {
   cudaError_t e;
   if constexpr (D == 2560) {
     if ((e = cudaFuncSetAttribute(hc::hc_down_s_kernel<D, KD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  hc::StreamGeo<D, KD>::BYTES)) != cudaSuccess)
+                                  hc::StreamGeo<D, KD>::BYTES)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(hc::hc_down_s_kernel<D, KD, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  hc::StreamGeo<D, KD, true>::BYTES)) != cudaSuccess)
       return e;
     if ((e = configure_umma<D, KD>()) != cudaSuccess) return e;
     if ((e = configure_wide<D, KD>()) != cudaSuccess) return e;
@@ -391,8 +393,23 @@ cudaError_t launch_geometry(int T, const DownArgs& da, const UpArgs& ua, cudaStr
 template <int D, int KD>
 cudaError_t launch_geometry_q8(int T, const DownArgs& da, const UpArgs& ua, cudaStream_t st) {
   constexpr int kOneGroupMaxT = D == 2560 ? 8 : 4;
-  // One token group: quants decoded in registers (mode 1); several groups:
-  // the tile widened once in shared memory (mode 2), reused by every group.
+  // T = 1 at d = 2560: the stream-wide down kernel over the quants (no
+  // cluster) with the mma.sync Q8_0 up kernel.  One token group: quants
+  // decoded in registers (mode 1); several groups: the tile widened once in
+  // shared memory (mode 2), reused by every group.
+  if constexpr (D == 2560) {
+    if (T == 1) {
+      using S = hc::StreamGeo<D, KD, true>;
+      cudaLaunchAttribute attr[2];
+      cudaLaunchConfig_t c1 = pdl_config(dim3(S::ROW_GROUPS, hc::kStreams), S::BYTES, st, attr, 1);
+      cudaError_t e = cudaLaunchKernelEx(&c1, hc::hc_down_s_kernel<D, KD, true>, da);
+      if (e != cudaSuccess) return e;
+      cudaLaunchAttribute attr2[2];
+      cudaLaunchConfig_t c2 = pdl_config(dim3(hc::Geo<D, KD>::UP_CTAS), hc::UpTcSmem<D, KD, 1, 1>::bytes(ua.T), st,
+                                         attr2, 1);
+      return cudaLaunchKernelEx(&c2, hc::hc_up_tc_kernel<D, KD, 1, 1>, ua);
+    }
+  }
   if (T <= 4) return launch_pair_tc<D, KD, 1, 1>(da, ua, st);
   return T <= kOneGroupMaxT ? launch_pair_tc<D, KD, 1, 2>(da, ua, st) : launch_pair_tc<D, KD, 2, 2>(da, ua, st);
 }
