@@ -127,13 +127,18 @@ struct DownSmem {
   static constexpr int BYTES_MAX = RECV + 4 * kMaxT * 4 + 4 * kMaxT * 32 * 4;
 };
 
-template <int D, int KD, int TT>
+template <int D, int KD, int TT, bool Q8 = false>
 struct UpSmem {
   using G = Geo<D, KD>;
   static constexpr int BAR = 0;
   static constexpr int FLAG = 16;
   static constexpr int W = 128;
-  static constexpr int GATE = W + G::UP_ROWS * G::UP_PITCH;
+  // Q8_0: quant rows at a pitch of 16 (mod 32) bytes, so that eight lanes
+  // reading 16-byte chunks of eight consecutive rows meet no bank twice;
+  // then the rows' binary16 block scales, [64][K/32].
+  static constexpr int WPITCH = Q8 ? KD + 16 : G::UP_PITCH;
+  static constexpr int SCALE = W + G::UP_ROWS * WPITCH;
+  static constexpr int GATE = SCALE + (Q8 ? G::UP_ROWS * (KD / 32) * 2 : 0);
   static constexpr int SIG = GATE + G::UP_ROWS * 4;
   static constexpr int LO = SIG + G::UP_ROWS * 4;
   static constexpr int RED = LO + TT * KD * 4;
@@ -217,6 +222,22 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float (&w)[8]) {
   w[5] = __uint_as_float(v.z & 0xffff0000u);
   w[6] = __uint_as_float(v.w << 16);
   w[7] = __uint_as_float(v.w & 0xffff0000u);
+}
+
+// Sixteen int8 quants (one 16-byte chunk) as fp32.  Each byte b, biased to
+// b + 128 by flipping its top bit, is placed in the mantissa of 2^23, which
+// makes the float 2^23 + 128 + b; taking away 2^23 + 128 leaves b exactly.
+__device__ __forceinline__ void q8x16_to_f32(const uint4 v, float* w) {
+  const unsigned words[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const unsigned u = words[k] ^ 0x80808080u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float f = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540u + i));
+      w[4 * k + i] = __fsub_rn(f, 8388736.0f);
+    }
+  }
 }
 
 // Every thread waits for the barrier's phase `parity` itself (observing the
@@ -673,11 +694,41 @@ __global__ void __launch_bounds__(kThreads, D == 2560 ? 3 : 2) hc_down_kernel(co
   if (a.independent) ptx::wait_prerequisites();  // complete only after the previous read
 }
 
+// One 8-column chunk of the up product: w[0..3] and w[4..7] feed two
+// accumulators per token, columns in order.
+template <int KD, int TT>
+__device__ __forceinline__ void up_chunk(const float* w, const float* lw, float (&acc0)[TT],
+                                         float (&acc1)[TT]) {
+#pragma unroll
+  for (int t = 0; t < TT; ++t) {
+    const float4 la = *reinterpret_cast<const float4*>(lw + t * KD);
+    const float4 lb = *reinterpret_cast<const float4*>(lw + t * KD + 4);
+    float v0 = acc0[t], v1 = acc1[t];
+    v0 = __fmaf_rn(w[0], la.x, v0);
+    v1 = __fmaf_rn(w[4], lb.x, v1);
+    v0 = __fmaf_rn(w[1], la.y, v0);
+    v1 = __fmaf_rn(w[5], lb.y, v1);
+    v0 = __fmaf_rn(w[2], la.z, v0);
+    v1 = __fmaf_rn(w[6], lb.z, v1);
+    v0 = __fmaf_rn(w[3], la.w, v0);
+    v1 = __fmaf_rn(w[7], lb.w, v1);
+    acc0[t] = v0;
+    acc1[t] = v1;
+  }
+}
+
 // ------------------------------------------------------------------ kernel 2
-template <int D, int KD, int TT>
+//
+// Q8 = true (Q8_0 projections): the quant rows and their block scales are
+// copied instead; each 16-quant chunk (inside one 32-weight block) is decoded
+// to fp32 in the loop, its products with lo are summed as a BF16 chunk's
+// would be, and the two sums are added to the accumulators times the block's
+// scale.
+template <int D, int KD, int TT, bool Q8 = false>
 __global__ void __launch_bounds__(kThreads, D == 2560 ? 3 : 2) hc_up_kernel(const UpArgs a) {
   using G = Geo<D, KD>;
-  using S = UpSmem<D, KD, TT>;
+  using S = UpSmem<D, KD, TT, Q8>;
+  static_assert(!Q8 || G::UP_KQ % 16 == 0, "a K quarter must split into 16-quant chunks");
   constexpr int EPI = (TT * G::UP_ROWS + kThreads - 1) / kThreads;  // epilogue items per thread
   constexpr int LO4 = (TT * KD / 4 + kThreads - 1) / kThreads;       // lo float4 per thread
   extern __shared__ __align__(128) unsigned char smem[];
@@ -701,7 +752,7 @@ __global__ void __launch_bounds__(kThreads, D == 2560 ? 3 : 2) hc_up_kernel(cons
       ptx::mbar_init(bar_w, 1);
       ptx::mbar_init(bar_g, 1);
       ptx::fence_barrier_init();
-      ptx::mbar_arrive_expect_tx(bar_w, G::UP_ROWS * KD * 2);
+      ptx::mbar_arrive_expect_tx(bar_w, Q8 ? G::UP_ROWS * KD + G::UP_ROWS * (KD / 32) * 2 : G::UP_ROWS * KD * 2);
       ptx::mbar_arrive_expect_tx(bar_g, G::UP_ROWS * 4);
     }
     __syncwarp();
@@ -713,7 +764,20 @@ __global__ void __launch_bounds__(kThreads, D == 2560 ? 3 : 2) hc_up_kernel(cons
     // Local row r = s * 16 + j holds global row s * d + c0 + j.
     for (int r = lane; r < G::UP_ROWS; r += 32) {
       const int grow = (r / G::UP_COLS) * D + c0 + (r % G::UP_COLS);
-      ptx::bulk_g2s(w_s + r * G::UP_PITCH, a.W_up + (size_t)grow * KD, KD * 2, bar_w, once);
+      if constexpr (Q8) {
+        ptx::bulk_g2s(w_s + r * S::WPITCH, a.Wq + (size_t)grow * KD, KD, bar_w, once);
+      } else {
+        ptx::bulk_g2s(w_s + r * G::UP_PITCH, a.W_up + (size_t)grow * KD, KD * 2, bar_w, once);
+      }
+    }
+    if constexpr (Q8) {
+      // The 16 rows of one stream are consecutive rows of the scales: one run.
+      constexpr int RUN = G::UP_COLS * (KD / 32) * 2;
+      static_assert(RUN % 16 == 0, "scale runs must be whole 16-byte pieces");
+      if (lane < kStreams) {
+        ptx::bulk_g2s(smem + S::SCALE + lane * RUN, a.Wscale + (size_t)(lane * D + c0) * (KD / 32), RUN,
+                      bar_w, once);
+      }
     }
   }
   __syncthreads();  // the mbarriers are initialised before any thread waits on them
@@ -791,30 +855,35 @@ __global__ void __launch_bounds__(kThreads, D == 2560 ? 3 : 2) hc_up_kernel(cons
     const int half = warp & 1;
     const int kq = warp >> 1;
     const int row = half * 32 + lane;
-    const unsigned char* wrow = w_s + row * G::UP_PITCH + kq * G::UP_KQ * 2;
     const float* lw = lo_s + kq * G::UP_KQ;
     float acc0[TT], acc1[TT];
 #pragma unroll
     for (int t = 0; t < TT; ++t) acc0[t] = acc1[t] = 0.f;
-#pragma unroll 2
-    for (int j = 0; j < G::UP_CHUNKS; ++j) {
-      float w[8];
-      bf16x8_to_f32(*reinterpret_cast<const uint4*>(wrow + j * 16), w);
+    if constexpr (Q8) {
+      const unsigned char* qrow = w_s + row * S::WPITCH + kq * G::UP_KQ;
+      const __half* srow = reinterpret_cast<const __half*>(smem + S::SCALE) + row * (KD / 32);
 #pragma unroll
-      for (int t = 0; t < TT; ++t) {
-        const float4 la = *reinterpret_cast<const float4*>(lw + t * KD + j * 8);
-        const float4 lb = *reinterpret_cast<const float4*>(lw + t * KD + j * 8 + 4);
-        float v0 = acc0[t], v1 = acc1[t];
-        v0 = __fmaf_rn(w[0], la.x, v0);
-        v1 = __fmaf_rn(w[4], lb.x, v1);
-        v0 = __fmaf_rn(w[1], la.y, v0);
-        v1 = __fmaf_rn(w[5], lb.y, v1);
-        v0 = __fmaf_rn(w[2], la.z, v0);
-        v1 = __fmaf_rn(w[6], lb.z, v1);
-        v0 = __fmaf_rn(w[3], la.w, v0);
-        v1 = __fmaf_rn(w[7], lb.w, v1);
-        acc0[t] = v0;
-        acc1[t] = v1;
+      for (int j = 0; j < G::UP_KQ / 16; ++j) {
+        float w[16], b0[TT], b1[TT];
+        q8x16_to_f32(*reinterpret_cast<const uint4*>(qrow + j * 16), w);
+#pragma unroll
+        for (int t = 0; t < TT; ++t) b0[t] = b1[t] = 0.f;
+        up_chunk<KD, TT>(w, lw + j * 16, b0, b1);
+        up_chunk<KD, TT>(w + 8, lw + j * 16 + 8, b0, b1);
+        const float sc = __half2float(srow[(kq * G::UP_KQ + j * 16) / 32]);
+#pragma unroll
+        for (int t = 0; t < TT; ++t) {
+          acc0[t] = __fmaf_rn(sc, b0[t], acc0[t]);
+          acc1[t] = __fmaf_rn(sc, b1[t], acc1[t]);
+        }
+      }
+    } else {
+      const unsigned char* wrow = w_s + row * G::UP_PITCH + kq * G::UP_KQ * 2;
+#pragma unroll 2
+      for (int j = 0; j < G::UP_CHUNKS; ++j) {
+        float w[8];
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(wrow + j * 16), w);
+        up_chunk<KD, TT>(w, lw + j * 8, acc0, acc1);
       }
     }
 #pragma unroll

@@ -208,7 +208,9 @@ cudaError_t configure_geometry() {
     if ((e = cudaFuncSetAttribute(hc::hc_down_s_kernel<D, KD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   hc::StreamGeo<D, KD>::BYTES)) != cudaSuccess ||
         (e = cudaFuncSetAttribute(hc::hc_down_s_kernel<D, KD, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  hc::StreamGeo<D, KD, true>::BYTES)) != cudaSuccess)
+                                  hc::StreamGeo<D, KD, true>::BYTES)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(hc::hc_up_kernel<D, KD, 1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  hc::UpSmem<D, KD, 1, true>::BYTES_MAX)) != cudaSuccess)
       return e;
     if ((e = configure_umma<D, KD>()) != cudaSuccess) return e;
     if ((e = configure_wide<D, KD>()) != cudaSuccess) return e;
@@ -265,6 +267,15 @@ cudaError_t launch_pair_tc(const DownArgs& da, const UpArgs& ua, cudaStream_t st
   cudaLaunchConfig_t c2 = pdl_config(dim3(G::UP_CTAS), hc::UpTcSmem<D, KD, NT, Q8>::bytes(ua.T), st,
                                       attr2, 1);
   return cudaLaunchKernelEx(&c2, hc::hc_up_tc_kernel<D, KD, NT, Q8>, ua);
+}
+
+// The Q8_0 CUDA-core up kernel (token groups of TT).
+template <int D, int KD, int TT>
+cudaError_t launch_up_q8_cc(const UpArgs& ua, cudaStream_t st) {
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t c = pdl_config(dim3(hc::Geo<D, KD>::UP_CTAS), hc::UpSmem<D, KD, TT, true>::bytes(ua.T), st,
+                                     attr, 1);
+  return cudaLaunchKernelEx(&c, hc::hc_up_kernel<D, KD, TT, true>, ua);
 }
 
 // The driver's tensor-map encoder (null when the driver does not offer it;
@@ -388,26 +399,24 @@ cudaError_t launch_geometry(int T, const DownArgs& da, const UpArgs& ua, cudaStr
   return T <= kOneGroupMaxT ? launch_pair_tc<D, KD, 1>(da, ua, st) : launch_pair_tc<D, KD, 2>(da, ua, st);
 }
 
-// The Q8_0 read: the tensor-core kernels at every T (no CUDA-core variant),
-// token groups as for BF16.
+// The Q8_0 read: at T = 1 and d = 2560 the CUDA-core pair, elsewhere the
+// tensor-core kernels, token groups as for BF16.  One token group: quants
+// decoded in registers (mode 1); several groups: the tile widened once in
+// shared memory (mode 2), reused by every group.
 template <int D, int KD>
 cudaError_t launch_geometry_q8(int T, const DownArgs& da, const UpArgs& ua, cudaStream_t st) {
   constexpr int kOneGroupMaxT = D == 2560 ? 8 : 4;
-  // T = 1 at d = 2560: the stream-wide down kernel over the quants (no
-  // cluster) with the mma.sync Q8_0 up kernel.  One token group: quants
-  // decoded in registers (mode 1); several groups: the tile widened once in
-  // shared memory (mode 2), reused by every group.
   if constexpr (D == 2560) {
     if (T == 1) {
+      // The stream-wide down kernel over the quants (no cluster) and the
+      // CUDA-core up kernel: for one token its decoding costs the chain less
+      // than the tensor-core kernel's fragment decoding.
       using S = hc::StreamGeo<D, KD, true>;
       cudaLaunchAttribute attr[2];
       cudaLaunchConfig_t c1 = pdl_config(dim3(S::ROW_GROUPS, hc::kStreams), S::BYTES, st, attr, 1);
       cudaError_t e = cudaLaunchKernelEx(&c1, hc::hc_down_s_kernel<D, KD, true>, da);
       if (e != cudaSuccess) return e;
-      cudaLaunchAttribute attr2[2];
-      cudaLaunchConfig_t c2 = pdl_config(dim3(hc::Geo<D, KD>::UP_CTAS), hc::UpTcSmem<D, KD, 1, 1>::bytes(ua.T), st,
-                                         attr2, 1);
-      return cudaLaunchKernelEx(&c2, hc::hc_up_tc_kernel<D, KD, 1, 1>, ua);
+      return launch_up_q8_cc<D, KD, 1>(ua, st);
     }
   }
   if (T <= 4) return launch_pair_tc<D, KD, 1, 1>(da, ua, st);
