@@ -326,6 +326,35 @@ __global__ void __launch_bounds__(kThreads) hc_pack_down_tiles_kernel(const uint
   }
 }
 
+// Sums V values over the 32 lanes of a warp (V a power of two, at most 32)
+// in V - 1 + 5 - log2(V) shuffles rather than 5 V: at each butterfly step
+// a lane keeps half of its values, sends the other half to its partner and
+// adds what the partner sent.  Afterwards v[0] of lane l holds the warp's sum
+// of value l >> (5 - log2 V) (lanes that share it hold the same sum).
+template <int V>
+__device__ __forceinline__ void warp_sum_transposed(float (&v)[V], int lane) {
+  static_assert(V >= 1 && V <= 32 && (V & (V - 1)) == 0, "V must be a power of two up to 32");
+  int n = V;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    if (n > 1) {
+      const int half = n / 2;
+      const bool upper = (lane & o) != 0;
+#pragma unroll
+      for (int i = 0; i < V / 2; ++i) {
+        if (i < half) {
+          const float send = upper ? v[i] : v[i + half];
+          const float keep = upper ? v[i + half] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+      }
+      n = half;
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+    }
+  }
+}
+
 // ------------------------------------------------------------------ kernel 1, T = 1 (d = 2560)
 // One CTA per 8 rows of W_down and one stream, over all the stream's D
 // columns: the stream's sum of squares, its rs and the rows' partial sums
@@ -446,13 +475,10 @@ __global__ void __launch_bounds__(kThreads, 4) hc_down_s_kernel(const DownArgs a
       acc[r] = __fmaf_rn(w0, x[2 * k], acc[r]);
       acc[r] = __fmaf_rn(w1, x[2 * k + 1], acc[r]);
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
   }
-  if (lane == 0) {
-#pragma unroll
-    for (int r = 0; r < G::ROWS; ++r) red[warp * (G::ROWS + 1) + r] = acc[r];
-  }
+  // The warp's 8 row sums in 9 shuffles: lane 4 r ends with row r.
+  warp_sum_transposed<G::ROWS>(acc, lane);
+  if ((lane & (32 / G::ROWS - 1)) == 0) red[warp * (G::ROWS + 1) + lane / (32 / G::ROWS)] = acc[0];
   __syncthreads();
   if (tid < G::ROWS) {
     float sq = 0.f, p = 0.f;
