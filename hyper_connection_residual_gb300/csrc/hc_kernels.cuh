@@ -360,10 +360,11 @@ __device__ __forceinline__ void warp_sum_transposed(float (&v)[V], int lane) {
 // columns: the stream's sum of squares, its rs and the rows' partial sums
 // are complete in the CTA, so there is no cluster and no exchange, and the
 // weight tile is 8 row segments of 2D bytes (Q8: D bytes of quants and D/16
-// of block scales).  CUDA cores, fp32 (T = 1: 80 multiply-adds a thread;
-// a Q8_0 weight is scale * q, exact in fp32).  Writes the same rs-scaled
-// per-stream partials as the other down kernels.
-template <int D, int KD, bool Q8 = false>
+// of block scales).  CUDA cores, fp32 (80 multiply-adds a thread and token;
+// a Q8_0 weight is scale * q, exact in fp32).  TT: tokens held in registers
+// (T <= TT).  Writes the same rs-scaled per-stream partials as the other down
+// kernels.
+template <int D, int KD, bool Q8 = false, int TT = 1>
 struct StreamGeo {
   static constexpr int ROWS = 8;                   // rows of W_down per CTA
   static constexpr int ROW_GROUPS = KD / ROWS;
@@ -376,15 +377,18 @@ struct StreamGeo {
   static constexpr int WN = 128;                   // w_norm of the stream [D]
   static constexpr int W = WN + D * 4;             // [ROWS][D] bf16 (int8 for Q8)
   static constexpr int SC = W + W_BYTES;           // [ROWS][D/32] binary16 (Q8)
-  static constexpr int RED = SC + ROWS * SC_BYTES;  // [kWarps][ROWS + 1]: row sums, then the sum of squares
-  static constexpr int BYTES = RED + kWarps * (ROWS + 1) * 4;
-  static_assert(D % (2 * kThreads) == 0 && KD % ROWS == 0 && ROWS <= 32, "whole column pairs and row groups");
+  static constexpr int RED = SC + ROWS * SC_BYTES;  // [kWarps][(ROWS + 1) TT]: row sums, then sums of squares
+  static constexpr int BYTES = RED + kWarps * (ROWS + 1) * TT * 4;
+  static_assert(D % (2 * kThreads) == 0 && KD % ROWS == 0 && ROWS * TT <= 32, "whole column pairs and row groups");
+  static_assert((TT & (TT - 1)) == 0, "tokens a pass: a power of two");
   static_assert(ROW_BYTES % 16 == 0 && SC_BYTES % 16 == 0 && W % 16 == 0 && SC % 16 == 0, "16-byte bulk copies");
 };
 
-template <int D, int KD, bool Q8 = false>
-__global__ void __launch_bounds__(kThreads, 4) hc_down_s_kernel(const DownArgs a) {
-  using G = StreamGeo<D, KD, Q8>;
+template <int D, int KD, bool Q8 = false, int TT = 1>
+__global__ void __launch_bounds__(kThreads, TT == 1 ? 4 : 2) hc_down_s_kernel(const DownArgs a) {
+  using G = StreamGeo<D, KD, Q8, TT>;
+  constexpr int V = G::ROWS * TT;  // row sums a thread holds: [ROWS][TT]
+  constexpr int RS = V + TT;       // a warp's scratch: V row sums, then TT sums of squares
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* bar_w = reinterpret_cast<uint64_t*>(smem + G::BAR);
   uint64_t* bar_n = bar_w + 1;
@@ -394,6 +398,7 @@ __global__ void __launch_bounds__(kThreads, 4) hc_down_s_kernel(const DownArgs a
   const int rg = blockIdx.x, stream = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int row0 = rg * G::ROWS, col0 = stream * D;
+  const int T = a.T;
   const uint64_t t_entry = ptx::globaltimer_ns();
 
   // w_norm of the stream and the 8 weight rows: parameters, issued first.
@@ -427,36 +432,49 @@ __global__ void __launch_bounds__(kThreads, 4) hc_down_s_kernel(const DownArgs a
   if (!a.independent) ptx::wait_prerequisites();
 
   // This thread's columns: pairs 2 tid + 2 kThreads k (coalesced float2 and
-  // BF16 pair loads).  R' = R + P, x = R' * w_norm, and R'^2 summed.
-  float2 rv[G::PAIRS], pv[G::PAIRS];
+  // BF16 pair loads).  R' = R + P, x = R' * w_norm, and R'^2 summed, per
+  // token (tokens past T are zero).
+  float2 rv[TT][G::PAIRS], pv[TT][G::PAIRS];
 #pragma unroll
-  for (int k = 0; k < G::PAIRS; ++k) {
-    const int c = 2 * tid + 2 * kThreads * k;
-    rv[k] = __ldcg(reinterpret_cast<const float2*>(a.R + col0 + c));
-    pv[k] = a.P ? __ldcg(reinterpret_cast<const float2*>(a.P + col0 + c)) : make_float2(0.f, 0.f);
+  for (int t = 0; t < TT; ++t) {
+#pragma unroll
+    for (int k = 0; k < G::PAIRS; ++k) {
+      const int c = 2 * tid + 2 * kThreads * k;
+      rv[t][k] = pv[t][k] = make_float2(0.f, 0.f);
+      if (t < T) {
+        const size_t off = (size_t)t * G::N + col0 + c;
+        rv[t][k] = __ldcg(reinterpret_cast<const float2*>(a.R + off));
+        if (a.P) pv[t][k] = __ldcg(reinterpret_cast<const float2*>(a.P + off));
+      }
+    }
   }
   bool ok = wait_bar_from(bar_n, 0, a.err, kErrDownNorm, t_entry, first_wait_limit(a.wait_ns));
-  float x[2 * G::PAIRS];
-  float ss = 0.f;
+  float x[TT][2 * G::PAIRS];
+  float ss[TT];
 #pragma unroll
-  for (int k = 0; k < G::PAIRS; ++k) {
-    const int c = 2 * tid + 2 * kThreads * k;
-    const float r0 = __fadd_rn(rv[k].x, pv[k].x), r1 = __fadd_rn(rv[k].y, pv[k].y);
-    x[2 * k] = __fmul_rn(r0, wn_s[c]);
-    x[2 * k + 1] = __fmul_rn(r1, wn_s[c + 1]);
-    ss = __fmaf_rn(r0, r0, ss);
-    ss = __fmaf_rn(r1, r1, ss);
+  for (int t = 0; t < TT; ++t) {
+    ss[t] = 0.f;
+#pragma unroll
+    for (int k = 0; k < G::PAIRS; ++k) {
+      const int c = 2 * tid + 2 * kThreads * k;
+      const float r0 = __fadd_rn(rv[t][k].x, pv[t][k].x), r1 = __fadd_rn(rv[t][k].y, pv[t][k].y);
+      x[t][2 * k] = __fmul_rn(r0, wn_s[c]);
+      x[t][2 * k + 1] = __fmul_rn(r1, wn_s[c + 1]);
+      ss[t] = __fmaf_rn(r0, r0, ss[t]);
+      ss[t] = __fmaf_rn(r1, r1, ss[t]);
+    }
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  if (lane == 0) red[warp * (G::ROWS + 1) + G::ROWS] = ss;
+  // Lane l ends with the warp's sum of squares of token l >> (5 - log2 TT).
+  warp_sum_transposed<TT>(ss, lane);
+  if ((lane & (32 / TT - 1)) == 0) red[warp * RS + V + lane / (32 / TT)] = ss[0];
 
   ok = wait_bar(bar_w, 0, a.err, kErrDownWeights) && ok;
   if (late_launch) ptx::launch_dependents();
-  float acc[G::ROWS];
+  float acc[V];  // [row][token]
 #pragma unroll
   for (int r = 0; r < G::ROWS; ++r) {
-    acc[r] = 0.f;
+#pragma unroll
+    for (int t = 0; t < TT; ++t) acc[r * TT + t] = 0.f;
 #pragma unroll
     for (int k = 0; k < G::PAIRS; ++k) {
       const int c = 2 * tid + 2 * kThreads * k;
@@ -472,24 +490,31 @@ __global__ void __launch_bounds__(kThreads, 4) hc_down_s_kernel(const DownArgs a
         w0 = __uint_as_float(w2 << 16);
         w1 = __uint_as_float(w2 & 0xffff0000u);
       }
-      acc[r] = __fmaf_rn(w0, x[2 * k], acc[r]);
-      acc[r] = __fmaf_rn(w1, x[2 * k + 1], acc[r]);
+#pragma unroll
+      for (int t = 0; t < TT; ++t) {
+        acc[r * TT + t] = __fmaf_rn(w0, x[t][2 * k], acc[r * TT + t]);
+        acc[r * TT + t] = __fmaf_rn(w1, x[t][2 * k + 1], acc[r * TT + t]);
+      }
     }
   }
-  // The warp's 8 row sums in 9 shuffles: lane 4 r ends with row r.
-  warp_sum_transposed<G::ROWS>(acc, lane);
-  if ((lane & (32 / G::ROWS - 1)) == 0) red[warp * (G::ROWS + 1) + lane / (32 / G::ROWS)] = acc[0];
+  // The warp's [row][token] sums, transposed: lane l ends with entry
+  // l >> (5 - log2 V) (T = 1: 9 shuffles, lane 4 r holds row r).
+  warp_sum_transposed<V>(acc, lane);
+  if ((lane & (32 / V - 1)) == 0) red[warp * RS + lane / (32 / V)] = acc[0];
   __syncthreads();
-  if (tid < G::ROWS) {
+  if (tid < V) {
+    const int r = tid / TT, t = tid % TT;
     float sq = 0.f, p = 0.f;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
-      sq += red[w * (G::ROWS + 1) + G::ROWS];
-      p += red[w * (G::ROWS + 1) + tid];
+      sq += red[w * RS + V + t];
+      p += red[w * RS + tid];
     }
-    const float rs = rsqrtf(sq * (1.0f / (float)D) + a.eps);
-    __stcg(a.part + (size_t)stream * a.T_max * KD + row0 + tid, __fmul_rn(rs, p));
-    if (rg == 0 && tid == 0 && a.rs_out != nullptr) a.rs_out[stream] = rs;
+    if (t < T) {
+      const float rs = rsqrtf(sq * (1.0f / (float)D) + a.eps);
+      __stcg(a.part + ((size_t)stream * a.T_max + t) * KD + row0 + r, __fmul_rn(rs, p));
+      if (rg == 0 && r == 0 && a.rs_out != nullptr) a.rs_out[t * kStreams + stream] = rs;
+    }
   }
   if (tid == 0 && !ok) {
     drain(bar_n, 0);

@@ -144,6 +144,12 @@ cudaLaunchConfig_t pdl_config(dim3 grid, size_t smem, cudaStream_t st, cudaLaunc
   return cfg;
 }
 
+template <int D, int KD, bool Q8, int TT>
+cudaError_t configure_down_s() {
+  return cudaFuncSetAttribute(hc::hc_down_s_kernel<D, KD, Q8, TT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              hc::StreamGeo<D, KD, Q8, TT>::BYTES);
+}
+
 template <int D, int KD, int TT>
 cudaError_t configure_one() {
   cudaError_t e = cudaFuncSetAttribute(hc::hc_down_kernel<D, KD, TT, false>,
@@ -205,10 +211,8 @@ template <int D, int KD>
 cudaError_t configure_geometry() {
   cudaError_t e;
   if constexpr (D == 2560) {
-    if ((e = cudaFuncSetAttribute(hc::hc_down_s_kernel<D, KD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  hc::StreamGeo<D, KD>::BYTES)) != cudaSuccess ||
-        (e = cudaFuncSetAttribute(hc::hc_down_s_kernel<D, KD, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  hc::StreamGeo<D, KD, true>::BYTES)) != cudaSuccess ||
+    if ((e = configure_down_s<D, KD, false, 1>()) != cudaSuccess || (e = configure_down_s<D, KD, true, 1>()) != cudaSuccess ||
+        (e = configure_down_s<D, KD, true, 2>()) != cudaSuccess ||
         (e = cudaFuncSetAttribute(hc::hc_up_kernel<D, KD, 1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   hc::UpSmem<D, KD, 1, true>::BYTES_MAX)) != cudaSuccess)
       return e;
@@ -239,19 +243,34 @@ cudaError_t launch_pair(const DownArgs& da, const UpArgs& ua, cudaStream_t st) {
   return cudaLaunchKernelEx(&c2, hc::hc_up_kernel<D, KD, TT>, ua);
 }
 
+// The stream-wide down kernel (no cluster), TT tokens held in registers.
+template <int D, int KD, bool Q8, int TT>
+cudaError_t launch_down_s(const DownArgs& da, cudaStream_t st) {
+  using S = hc::StreamGeo<D, KD, Q8, TT>;
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t c = pdl_config(dim3(S::ROW_GROUPS, hc::kStreams), S::BYTES, st, attr, 1);
+  return cudaLaunchKernelEx(&c, hc::hc_down_s_kernel<D, KD, Q8, TT>, da);
+}
+
 // T = 1 at d = 2560: the stream-wide down kernel (no cluster) with the
 // CUDA-core up kernel.
 template <int D, int KD>
 cudaError_t launch_pair_s(const DownArgs& da, const UpArgs& ua, cudaStream_t st) {
-  using S = hc::StreamGeo<D, KD>;
   using G = hc::Geo<D, KD>;
-  cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t c1 = pdl_config(dim3(S::ROW_GROUPS, hc::kStreams), S::BYTES, st, attr, 1);
-  cudaError_t e = cudaLaunchKernelEx(&c1, hc::hc_down_s_kernel<D, KD>, da);
+  cudaError_t e = launch_down_s<D, KD, false, 1>(da, st);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr2[2];
   cudaLaunchConfig_t c2 = pdl_config(dim3(G::UP_CTAS), hc::UpSmem<D, KD, 1>::bytes(ua.T), st, attr2, 1);
   return cudaLaunchKernelEx(&c2, hc::hc_up_kernel<D, KD, 1>, ua);
+}
+
+// The tensor-core up kernel alone (after another down kernel).
+template <int D, int KD, int NT, int Q8>
+cudaError_t launch_up_tc(const UpArgs& ua, cudaStream_t st) {
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t c = pdl_config(dim3(hc::Geo<D, KD>::UP_CTAS), hc::UpTcSmem<D, KD, NT, Q8>::bytes(ua.T), st,
+                                     attr, 1);
+  return cudaLaunchKernelEx(&c, hc::hc_up_tc_kernel<D, KD, NT, Q8>, ua);
 }
 
 template <int D, int KD, int NT, int Q8 = 0>
@@ -399,8 +418,8 @@ cudaError_t launch_geometry(int T, const DownArgs& da, const UpArgs& ua, cudaStr
   return T <= kOneGroupMaxT ? launch_pair_tc<D, KD, 1>(da, ua, st) : launch_pair_tc<D, KD, 2>(da, ua, st);
 }
 
-// The Q8_0 read: at T = 1 and d = 2560 the CUDA-core pair, elsewhere the
-// tensor-core kernels, token groups as for BF16.  One token group: quants
+// The Q8_0 read: at T = 1, 2 and d = 2560 the stream-wide down kernel,
+// elsewhere the tensor-core kernels, token groups as for BF16.  One token group: quants
 // decoded in registers (mode 1); several groups: the tile widened once in
 // shared memory (mode 2), reused by every group.
 template <int D, int KD>
@@ -411,12 +430,18 @@ cudaError_t launch_geometry_q8(int T, const DownArgs& da, const UpArgs& ua, cuda
       // The stream-wide down kernel over the quants (no cluster) and the
       // CUDA-core up kernel: for one token its decoding costs the chain less
       // than the tensor-core kernel's fragment decoding.
-      using S = hc::StreamGeo<D, KD, true>;
-      cudaLaunchAttribute attr[2];
-      cudaLaunchConfig_t c1 = pdl_config(dim3(S::ROW_GROUPS, hc::kStreams), S::BYTES, st, attr, 1);
-      cudaError_t e = cudaLaunchKernelEx(&c1, hc::hc_down_s_kernel<D, KD, true>, da);
+      cudaError_t e = launch_down_s<D, KD, true, 1>(da, st);
       if (e != cudaSuccess) return e;
       return launch_up_q8_cc<D, KD, 1>(ua, st);
+    }
+    if (T == 2) {
+      // The stream-wide down kernel with both tokens in registers and the
+      // tensor-core up kernel (mode 1).  Four tokens in registers (T = 3, 4)
+      // cost the batch more than they save the chain: 96 registers a thread,
+      // two CTAs an SM.
+      cudaError_t e = launch_down_s<D, KD, true, 2>(da, st);
+      if (e != cudaSuccess) return e;
+      return launch_up_tc<D, KD, 1, 1>(ua, st);
     }
   }
   if (T <= 4) return launch_pair_tc<D, KD, 1, 1>(da, ua, st);
