@@ -529,7 +529,7 @@ def run_profile_wide_case():
 def run_profile_q8_case():
     """Cold reads after a 256 MB L2 flush each: two BF16 and two Q8_0 reads at
     T=4 (the same tensor-core kernels over the two weight formats), then two
-    Q8_0 reads at T=1 and two at T=8 (pending on); a small case for ncu."""
+    Q8_0 reads each at T=1, T=2 and T=8 (pending on); a small case for ncu."""
     import torch
     import hyper_connection_residual_gb300 as hc
     dev = torch.device("cuda", 0)
@@ -556,7 +556,7 @@ def run_profile_q8_case():
         for w in bf:
             flush.zero_()
             rd(R, w["w_norm"], w["W_down"], w["W_up"], w["gate"], P, 4, out, mean, lo)
-        for T in (4, 1, 8):
+        for T in (4, 1, 2, 8):
             for w in q8:
                 flush.zero_()
                 rd.q8(R, w["w_norm"], w["Wd_q"], w["Wd_scale"], w["Wu_q"], w["Wu_scale"], w["gate"], P, T,
@@ -770,6 +770,12 @@ def run_gpu(args):
                               read_bytes_q8(g, T, p) * 5 * CALLS / pc[(T, p)] / 1e9 for (T, p) in q8.cases},
             "GBps": sum(q8.bytes_per_replay(c) for c in q8.cases) * 5 / tq / 1e9}
         q8.close()
+        q8s = Sweep(hc, torch, dev, g, SWEEP_T, (False,), SETS, calls, stream, batch=False, q8=True)
+        ts8, pc = time_cases(torch, q8s, 5, 3, stream)
+        extra["q8_0_sweep_one_stream_per_call"] = {
+            "note": "the Q8_0 sweep's reads (pending off) as hc_read_q8 calls on one stream, one set of outputs",
+            "us_per_read": {f"T{T}_nopend": 1e6 * pc[(T, p)] / (5 * calls) for (T, p) in q8s.cases}}
+        q8s.close()
         q2 = run_q2_sweep(torch, hc, dev, stream)
         hbm = measured_peaks()["hbm_gbs"]
         extra["q2_0_matvec_attn_q"] = {

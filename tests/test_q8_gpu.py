@@ -190,7 +190,7 @@ def _q8_read(w, R, P, o):
     return dict(R=R, P=P, out=o["out"], mean=o["mean"], lo=o["lo"], **w)
 
 
-@pytest.mark.parametrize("T", [1, 4, 8])
+@pytest.mark.parametrize("T", [1, 2, 4, 8])
 def test_q8_batch_on_lanes_equals_single_reads(dev, g1, rd, T):
     """Twelve independent Q8_0 reads as one batch run on the internal streams;
     every read's outputs equal hc_read_q8's bit for bit."""
