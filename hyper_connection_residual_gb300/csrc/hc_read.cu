@@ -214,7 +214,9 @@ cudaError_t configure_geometry() {
     if ((e = configure_down_s<D, KD, false, 1>()) != cudaSuccess || (e = configure_down_s<D, KD, true, 1>()) != cudaSuccess ||
         (e = configure_down_s<D, KD, true, 2>()) != cudaSuccess ||
         (e = cudaFuncSetAttribute(hc::hc_up_kernel<D, KD, 1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  hc::UpSmem<D, KD, 1, true>::BYTES_MAX)) != cudaSuccess)
+                                  hc::UpSmem<D, KD, 1, true>::BYTES_MAX)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(hc::hc_up_kernel<D, KD, 2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  hc::UpSmem<D, KD, 2, true>::BYTES_MAX)) != cudaSuccess)
       return e;
     if ((e = configure_umma<D, KD>()) != cudaSuccess) return e;
     if ((e = configure_wide<D, KD>()) != cudaSuccess) return e;
@@ -262,15 +264,6 @@ cudaError_t launch_pair_s(const DownArgs& da, const UpArgs& ua, cudaStream_t st)
   cudaLaunchAttribute attr2[2];
   cudaLaunchConfig_t c2 = pdl_config(dim3(G::UP_CTAS), hc::UpSmem<D, KD, 1>::bytes(ua.T), st, attr2, 1);
   return cudaLaunchKernelEx(&c2, hc::hc_up_kernel<D, KD, 1>, ua);
-}
-
-// The tensor-core up kernel alone (after another down kernel).
-template <int D, int KD, int NT, int Q8>
-cudaError_t launch_up_tc(const UpArgs& ua, cudaStream_t st) {
-  cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t c = pdl_config(dim3(hc::Geo<D, KD>::UP_CTAS), hc::UpTcSmem<D, KD, NT, Q8>::bytes(ua.T), st,
-                                     attr, 1);
-  return cudaLaunchKernelEx(&c, hc::hc_up_tc_kernel<D, KD, NT, Q8>, ua);
 }
 
 template <int D, int KD, int NT, int Q8 = 0>
@@ -418,8 +411,9 @@ cudaError_t launch_geometry(int T, const DownArgs& da, const UpArgs& ua, cudaStr
   return T <= kOneGroupMaxT ? launch_pair_tc<D, KD, 1>(da, ua, st) : launch_pair_tc<D, KD, 2>(da, ua, st);
 }
 
-// The Q8_0 read: at T = 1, 2 and d = 2560 the stream-wide down kernel,
-// elsewhere the tensor-core kernels, token groups as for BF16.  One token group: quants
+// The Q8_0 read: at T = 1, 2 and d = 2560 the stream-wide down kernel and the
+// CUDA-core up kernel, elsewhere the tensor-core kernels, token groups as for
+// BF16.  One token group: quants
 // decoded in registers (mode 1); several groups: the tile widened once in
 // shared memory (mode 2), reused by every group.
 template <int D, int KD>
@@ -436,12 +430,12 @@ cudaError_t launch_geometry_q8(int T, const DownArgs& da, const UpArgs& ua, cuda
     }
     if (T == 2) {
       // The stream-wide down kernel with both tokens in registers and the
-      // tensor-core up kernel (mode 1).  Four tokens in registers (T = 3, 4)
-      // cost the batch more than they save the chain: 96 registers a thread,
-      // two CTAs an SM.
+      // CUDA-core up kernel with both tokens.  Four tokens (T = 3, 4) cost
+      // more than they save in either kernel: 96 registers a thread in the
+      // down kernel, spills at 64 in the up kernel.
       cudaError_t e = launch_down_s<D, KD, true, 2>(da, st);
       if (e != cudaSuccess) return e;
-      return launch_up_tc<D, KD, 1, 1>(ua, st);
+      return launch_up_q8_cc<D, KD, 2>(ua, st);
     }
   }
   if (T <= 4) return launch_pair_tc<D, KD, 1, 1>(da, ua, st);
