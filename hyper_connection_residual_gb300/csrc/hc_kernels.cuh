@@ -384,8 +384,12 @@ struct StreamGeo {
   static_assert(ROW_BYTES % 16 == 0 && SC_BYTES % 16 == 0 && W % 16 == 0 && SC % 16 == 0, "16-byte bulk copies");
 };
 
+// Two tokens are held to 48 registers, five CTAs per SM (a 16-byte spill):
+// a cold batch of Q8_0 T = 2 reads ran 2.53 us per read at 63 registers
+// (four CTAs), 2.42 at 48.  One token needs no bound: 40 (BF16) and 47
+// (Q8_0) registers, and the BF16 tile's 51 KB of shared memory allows four.
 template <int D, int KD, bool Q8 = false, int TT = 1>
-__global__ void __launch_bounds__(kThreads, TT == 1 ? 4 : 2) hc_down_s_kernel(const DownArgs a) {
+__global__ void __launch_bounds__(kThreads, TT == 1 ? 4 : 5) hc_down_s_kernel(const DownArgs a) {
   using G = StreamGeo<D, KD, Q8, TT>;
   constexpr int V = G::ROWS * TT;  // row sums a thread holds: [ROWS][TT]
   constexpr int RS = V + TT;       // a warp's scratch: V row sums, then TT sums of squares
@@ -480,25 +484,18 @@ __global__ void __launch_bounds__(kThreads, TT == 1 ? 4 : 2) hc_down_s_kernel(co
       const int c = 2 * tid + 2 * kThreads * k;
       float w0, w1;
       if constexpr (Q8) {
-        // Both columns in the block c / 32: scale * q, exact in fp32.
+        // Both columns in the block c / 32: scale * q, exact in fp32, with no
+        // integer-to-float conversion: each byte b, biased to b + 128 by
+        // flipping its top bit, is placed in the mantissa of 2^23 (the float
+        // 2^23 + 128 + b), and subtracting 2^23 + 128 leaves b exactly.  The
+        // conversion instruction took more registers (64 against 47 at T = 1,
+        // 86 against 63 at T = 2) and fewer CTAs per SM: at T = 2, 3.11 ->
+        // 2.90 us per read in a cold batch; at T = 1, with the up kernel at
+        // five CTAs per SM, 2.07 -> 2.03 (and 4.9 -> 4.8 read after read).
         const float sc = __half2float(reinterpret_cast<const __half*>(smem + G::SC + r * G::SC_BYTES)[c / 32]);
-        if constexpr (TT == 1) {
-          const char2 q = *reinterpret_cast<const char2*>(w_s + r * G::ROW_BYTES + c);
-          w0 = __fmul_rn(sc, (float)q.x);
-          w1 = __fmul_rn(sc, (float)q.y);
-        } else {
-          // The same values with no integer-to-float conversion: each byte
-          // b, biased to b + 128 by flipping its top bit, is placed in the
-          // mantissa of 2^23 (the float 2^23 + 128 + b), and subtracting
-          // 2^23 + 128 leaves b exactly.  Fewer registers (63 against 86)
-          // let more CTAs share an SM: at T = 2, 3.11 -> 2.90 us per read in
-          // a cold batch, 5.7 -> 6.0 read after read; at T = 1 the batch
-          // gained 1.6 % and a lone chain of reads lost 7 %, so T = 1 keeps
-          // the conversion.
-          const unsigned u = *reinterpret_cast<const unsigned short*>(w_s + r * G::ROW_BYTES + c) ^ 0x8080u;
-          w0 = __fmul_rn(sc, __fsub_rn(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540u)), 8388736.0f));
-          w1 = __fmul_rn(sc, __fsub_rn(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541u)), 8388736.0f));
-        }
+        const unsigned u = *reinterpret_cast<const unsigned short*>(w_s + r * G::ROW_BYTES + c) ^ 0x8080u;
+        w0 = __fmul_rn(sc, __fsub_rn(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540u)), 8388736.0f));
+        w1 = __fmul_rn(sc, __fsub_rn(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541u)), 8388736.0f));
       } else {
         const uint32_t w2 = *reinterpret_cast<const uint32_t*>(w_s + r * (D * 2) + c * 2);
         w0 = __uint_as_float(w2 << 16);
@@ -788,10 +785,15 @@ __device__ __forceinline__ void up_chunk(const float* w, const float* lw, float 
 // copied instead; each 16-quant chunk (inside one 32-weight block) is decoded
 // to fp32 in the loop, its products with lo are summed as a BF16 chunk's
 // would be, and the two sums are added to the accumulators times the block's
-// scale.  Held to 64 registers (four CTAs per SM): at 72 registers three fit,
-// and a cold batch of T = 1 reads ran 2.53 against 2.14 us per read.
+// scale.
+//
+// At d = 2560 held to 48 registers, five CTAs per SM (the BF16 tile's 45 KB
+// of shared memory allows five, the Q8_0 tile's 26 KB eight): more CTAs per
+// SM keep more weight tiles in flight.  Cold batches of T = 1 reads: BF16
+// 2.28-2.38 -> 2.01-2.03 us per read (60 -> 48 registers); Q8_0 2.53 us at
+// 72 registers, 2.18 at 64, 2.07 at 48.
 template <int D, int KD, int TT, bool Q8 = false>
-__global__ void __launch_bounds__(kThreads, D == 2560 ? (Q8 ? 4 : 3) : 2) hc_up_kernel(const UpArgs a) {
+__global__ void __launch_bounds__(kThreads, D == 2560 ? 5 : 2) hc_up_kernel(const UpArgs a) {
   using G = Geo<D, KD>;
   using S = UpSmem<D, KD, TT, Q8>;
   static_assert(!Q8 || G::UP_KQ % 16 == 0, "a K quarter must split into 16-quant chunks");
