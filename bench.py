@@ -34,6 +34,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -105,14 +106,23 @@ def whole_job_gbs(world: int, bytes_per_step: int, steps: int, seconds: float) -
     return world * bytes_per_step * steps / seconds / 1e9
 
 
+def _code_only(text: str) -> str:
+    """C++ source without its comments, whitespace runs collapsed (the
+    sources hashed here hold no comment markers inside string literals)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(names=None) -> str:
-    """Hash of the CUDA sources (all of them, or the files in `names`)."""
+    """Hash of the CUDA sources' code (all of them, or the files in `names`);
+    comments and layout do not change it."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "hyper_connection_residual_gb300", "csrc")
     for name in sorted(names if names is not None else os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
             h.update(name.encode())
-            h.update(f.read())
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

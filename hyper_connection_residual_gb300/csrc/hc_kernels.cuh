@@ -788,7 +788,7 @@ __device__ __forceinline__ void up_chunk(const float* w, const float* lw, float 
 // scale.
 //
 // At d = 2560 held to 48 registers, five CTAs per SM (the BF16 tile's 45 KB
-// of shared memory allows five, the Q8_0 tile's 26 KB eight): more CTAs per
+// of shared memory allows five, the Q8_0 tile's 26 KB six): more CTAs per
 // SM keep more weight tiles in flight.  Cold batches of T = 1 reads: BF16
 // 2.28-2.38 -> 2.01-2.03 us per read (60 -> 48 registers); Q8_0 2.53 us at
 // 72 registers, 2.18 at 64, 2.07 at 48.
