@@ -49,6 +49,15 @@
 // part (fixed order); four quarters of K are summed in a fixed order; the
 // epilogue writes out = R' + sigmoid(g) * u and the mean.
 //
+// Kernel 1s, hc_down_s_kernel (T = 1, 2 at d = 2560): a CTA owns 8 rows of
+// W_down over one stream's whole width, so the stream's sum of squares and
+// the rows' dot products finish inside the CTA: no cluster, no exchange.
+//
+// In a batch of independent reads the kernels of many reads share the SMs,
+// and the weight tiles an SM holds in flight set the bandwidth: the T = 1
+// kernels are held to at most 48 registers so that registers do not cap the
+// CTAs per SM below what their shared memory allows.
+//
 // Every reduction has a fixed order, so results do not depend on scheduling:
 // direct calls and graph replays give the same bits.
 #pragma once
