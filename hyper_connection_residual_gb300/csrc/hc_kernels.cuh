@@ -364,7 +364,7 @@ __device__ __forceinline__ void warp_sum_transposed(float (&v)[V], int lane) {
   }
 }
 
-// ------------------------------------------------------------------ kernel 1, T = 1 (d = 2560)
+// ------------------------------------------------------------------ kernel 1, T = 1 (d = 2560; Q8_0 also T = 2)
 // One CTA per 8 rows of W_down and one stream, over all the stream's D
 // columns: the stream's sum of squares, its rs and the rows' partial sums
 // are complete in the CTA, so there is no cluster and no exchange, and the
@@ -389,7 +389,7 @@ struct StreamGeo {
   static constexpr int RED = SC + ROWS * SC_BYTES;  // [kWarps][(ROWS + 1) TT]: row sums, then sums of squares
   static constexpr int BYTES = RED + kWarps * (ROWS + 1) * TT * 4;
   static_assert(D % (2 * kThreads) == 0 && KD % ROWS == 0 && ROWS * TT <= 32, "whole column pairs and row groups");
-  static_assert((TT & (TT - 1)) == 0, "tokens a pass: a power of two");
+  static_assert((TT & (TT - 1)) == 0, "tokens held in registers: a power of two");
   static_assert(ROW_BYTES % 16 == 0 && SC_BYTES % 16 == 0 && W % 16 == 0 && SC % 16 == 0, "16-byte bulk copies");
 };
 
