@@ -389,7 +389,7 @@ struct StreamGeo {
   static constexpr int RED = SC + ROWS * SC_BYTES;  // [kWarps][(ROWS + 1) TT]: row sums, then sums of squares
   static constexpr int BYTES = RED + kWarps * (ROWS + 1) * TT * 4;
   static_assert(D % (2 * kThreads) == 0 && KD % ROWS == 0 && ROWS * TT <= 32, "whole column pairs and row groups");
-  static_assert((TT & (TT - 1)) == 0, "tokens held in registers: a power of two");
+  static_assert((TT & (TT - 1)) == 0, "tokens a pass: a power of two");
   static_assert(ROW_BYTES % 16 == 0 && SC_BYTES % 16 == 0 && W % 16 == 0 && SC % 16 == 0, "16-byte bulk copies");
 };
 
